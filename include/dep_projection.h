@@ -1,0 +1,203 @@
+/*
+ * dep_projection.h -- C ABI of the GB300 (sm_103a) decode projection library.
+ *
+ * The operation.  One decode-time linear layer at tensor-parallel degree 1:
+ *
+ *     y[B,N] = BF16( x[B,K] . W[N,K]^T ),  BF16 inputs, FP32 accumulation.
+ *
+ * Source: vllm.models.kimi_k3.nvidia.specialized_decode.runtime.dep (the
+ * "runtime.dep page"), class DepProjection: a TP1 linear that runs split-K at the
+ * batches its tactic table names and the stock FP32-accumulated BF16 GEMM
+ * (torch.mm(x, W.t(), out=out)) otherwise; the module overview's precision
+ * paragraph: BF16 outputs, FP32 accumulation, a split-K order that differs from
+ * the stock one.  The weights it serves are the packed DSA input projection
+ * (14560 x 7168), o_proj (7168 x 12288) and the packed KDA input projection
+ * (49376 x 7168), streamed whole once per decode step.
+ *
+ * Plans.  A plan is built once per weight shape (N, K) and set of batch sizes,
+ * like DepProjection.__init__ (runtime.dep page), and holds a tactic table keyed
+ * by "max rows" (runtime.dep page, _bins and dep_policies).  At run time a batch
+ * of B rows takes the entry with the smallest key >= B, else the entry with the
+ * largest key.  Every tactic accepts any B >= 1 (wider batches run in passes).
+ *
+ * Layouts.  x is [B,K], W is [N,K] (the nn.Linear weight), y is [B,N]; all three
+ * are row-major, contiguous, BF16, in device memory of the plan's device, and
+ * 16-byte aligned.  K must be a multiple of 8 (16-byte rows).  N is any value
+ * >= 1.  y must not overlap x or W.  The caller owns x, W and y; the library
+ * neither retains nor repacks W.
+ *
+ * Determinism.  Each tactic sums in one fixed order with a fixed-order
+ * cross-block split-K reduction and no floating-point atomics: the same call on
+ * the same plan gives the same bits every time.
+ *
+ * Errors.  Every call returns a dep_status_t; nothing aborts or throws across
+ * the ABI.  Launch failures are reported as DEP_ERR_CUDA.
+ *
+ * Concurrency.  A plan owns one split-K workspace.  Two runs of the same plan
+ * must not overlap on the GPU (use one plan per stream).  Runs are asynchronous
+ * on the given stream, allocate nothing and do not synchronise, so they can be
+ * captured in CUDA graphs (the runtime package page, specialized_decode_config:
+ * the deployment's decode batches are its CUDA-graph capture sizes).
+ */
+#ifndef DEP_PROJECTION_H
+#define DEP_PROJECTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque plan handle, owned by the library (free with dep_projection_plan_destroy). */
+typedef struct dep_plan_s *dep_plan_t;
+
+typedef enum {
+    DEP_OK = 0,
+    DEP_ERR_INVALID_ARG = 1,  /* null pointer, bad size, unknown tactic, wrong device */
+    DEP_ERR_UNSUPPORTED = 2,  /* shape or plan kind this build cannot run */
+    DEP_ERR_MISALIGNED = 3,   /* a pointer not 16-byte aligned, or K % 8 != 0 */
+    DEP_ERR_CUDA = 4,         /* a CUDA runtime/driver call or a launch failed */
+    DEP_ERR_OOM = 5,          /* plan-time device allocation failed */
+    DEP_ERR_TIMEOUT = 6,      /* a kernel gave up a bounded wait (device status) */
+    DEP_ERR_INTERNAL = 7,     /* an invariant of the library was broken */
+    DEP_ERR_IO = 8            /* plan file could not be read or written, or is malformed */
+} dep_status_t;
+
+/* Tactic kinds. */
+#define DEP_KIND_SPLITK_FMA 1 /* warp split-K on the FP32 FMA pipe, TMA-staged W */
+#define DEP_KIND_TC 2         /* tcgen05 MMA, TMEM accumulators, TMA-staged W and x */
+
+/* One table entry: the tactic that serves batches of up to max_rows rows. */
+typedef struct {
+    int32_t max_rows; /* table key (binning rule above) */
+    int32_t kind;     /* DEP_KIND_* */
+    int32_t ctas;     /* persistent blocks launched (work split evenly: stream-K) */
+    int32_t tile_n;   /* weight rows per tile */
+    int32_t tile_k;   /* reduction columns per pipeline stage */
+    int32_t stages;   /* pipeline depth (shared-memory stages) */
+    int32_t cols;     /* batch rows per pass (FMA: x rows held; TC: MMA N) */
+} dep_tactic_t;
+
+/* Plan flags. */
+#define DEP_PLAN_DEFAULT 0u /* fixed rule: FMA split-K for small batches, TC past them */
+#define DEP_PLAN_TUNE 1u    /* time candidate tactics per batch on scratch data; keep the fastest */
+
+/*
+ * Build a plan for weights of shape [N,K] on the current CUDA device.
+ *   batches/n_batches: the batch sizes the caller will run (the table's keys);
+ *                      n_batches == 0 takes 1,2,4,8,16,32,64,128,256.
+ *   flags:             DEP_PLAN_DEFAULT or DEP_PLAN_TUNE.
+ * Allocates the plan's workspace, counters and status word on the device.
+ * Errors: INVALID_ARG (N < 1, K < 8, batch < 1, null out), MISALIGNED (K % 8),
+ * OOM, CUDA.  On error *out is set to NULL.
+ */
+dep_status_t dep_projection_plan(int64_t N, int64_t K, const int32_t *batches,
+                                 int32_t n_batches, uint32_t flags, dep_plan_t *out);
+
+/*
+ * Build the default table for an explicit SM count without touching any GPU:
+ * for inspection, saving, and host-side tests.  Running such a plan returns
+ * DEP_ERR_UNSUPPORTED.  Errors as dep_projection_plan, plus INVALID_ARG for
+ * sm_count < 1.
+ */
+dep_status_t dep_projection_plan_host(int64_t N, int64_t K, const int32_t *batches,
+                                      int32_t n_batches, int32_t sm_count,
+                                      dep_plan_t *out);
+
+/*
+ * y[B,N] = BF16(x[B,K] . W[N,K]^T) on `stream` (a cudaStream_t; NULL = legacy
+ * default stream).  The tactic is the plan's table entry for B (binning rule).
+ * B == 0 launches nothing and returns DEP_OK; B < 0 is INVALID_ARG.
+ * Asynchronous: returns after enqueueing.  Errors: INVALID_ARG (null pointer,
+ * overlap of y with x or W, current device is not the plan's), MISALIGNED,
+ * UNSUPPORTED (host-only plan), CUDA (launch failure).
+ */
+dep_status_t dep_projection_run(dep_plan_t plan, const void *x, const void *W, void *y,
+                                int32_t B, void *stream);
+
+/*
+ * The same with an explicit tactic instead of the table's (tests and tuning).
+ * Errors as dep_projection_run, plus INVALID_ARG for a tactic this build does
+ * not implement or whose split-K workspace exceeds the plan's.
+ */
+dep_status_t dep_projection_run_tactic(dep_plan_t plan, const dep_tactic_t *tactic,
+                                       const void *x, const void *W, void *y,
+                                       int32_t B, void *stream);
+
+/*
+ * End-to-end call with the activations in host memory: copies x_host [B,K] to
+ * the plan's device staging buffer, runs the projection against the resident
+ * device weight W, and copies y back to y_host [B,N], all enqueued on `stream`
+ * (pinned host memory makes the copies asynchronous).  The caller synchronises
+ * the stream before reading y_host.  B must not exceed the plan's largest table
+ * key (the staging capacity).  Errors as dep_projection_run.
+ */
+dep_status_t dep_projection_run_host(dep_plan_t plan, const void *x_host, const void *W,
+                                     void *y_host, int32_t B, void *stream);
+
+/* The tactic the plan uses for a batch of B >= 1 rows. */
+dep_status_t dep_projection_plan_query(dep_plan_t plan, int32_t B, dep_tactic_t *out);
+
+/* Copy up to `cap` table entries (sorted by max_rows) to `out`; *n = entry count. */
+dep_status_t dep_projection_plan_table(dep_plan_t plan, dep_tactic_t *out, int32_t cap,
+                                       int32_t *n);
+
+/* Replace (or insert) the table entry with key tactic->max_rows.  The tactic is
+ * validated and the split-K workspace must already be large enough for it. */
+dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic);
+
+/* Bytes of device workspace the plan owns (split-K partials, counters, status). */
+dep_status_t dep_projection_plan_workspace(dep_plan_t plan, size_t *bytes);
+
+/*
+ * Save the table as text keyed by (device name, SM count, N, K), and load it
+ * back onto the current device (tuning need not be repeated).  Load checks the
+ * shape (INVALID_ARG if it differs) and the SM count (UNSUPPORTED if the file
+ * was made for another GPU).  Errors: IO for unreadable or malformed files.
+ */
+dep_status_t dep_projection_plan_save(dep_plan_t plan, const char *path);
+dep_status_t dep_projection_plan_load(const char *path, int64_t N, int64_t K,
+                                      dep_plan_t *out);
+
+/* Free the plan and its device memory (synchronises its device).  NULL is a no-op. */
+void dep_projection_plan_destroy(dep_plan_t plan);
+
+/*
+ * Read and clear the plan's device status word (synchronises `stream`).
+ * *code = 0 if every kernel since the last read finished its waits; otherwise
+ * the first nonzero code a kernel recorded (see DEP_DEV_* below), and the
+ * return value is DEP_ERR_TIMEOUT.
+ */
+dep_status_t dep_projection_device_status(dep_plan_t plan, void *stream, int32_t *code);
+
+#define DEP_DEV_TIMEOUT_PRODUCER 1 /* the load warp gave up waiting for a free stage */
+#define DEP_DEV_TIMEOUT_CONSUMER 2 /* a compute warp gave up waiting for a stage's data */
+#define DEP_DEV_TIMEOUT_MMA 3      /* the MMA warp gave up waiting */
+#define DEP_DEV_TIMEOUT_EPILOGUE 4 /* an epilogue warp gave up waiting for an accumulator */
+
+/*
+ * Bounded-wait self-test: launches one block whose waits can never be satisfied
+ * (an mbarrier that nothing arrives on) with a wait limit of `limit_us`
+ * microseconds, synchronises, and reports the code the kernel recorded in
+ * *code (expected: DEP_DEV_TIMEOUT_CONSUMER).  Returns DEP_OK if the kernel
+ * came back by itself.  Exercises the give-up path without faulting the GPU.
+ */
+dep_status_t dep_projection_selftest_timeout(int32_t limit_us, int32_t *code);
+
+/* The binning rule on its own: index into keys[0..n_keys) of the entry serving
+ * B rows -- smallest key >= B, else the largest key; -1 if n_keys < 1.  The keys
+ * need not be sorted.  Pure host function. */
+int32_t dep_bins_index(const int32_t *keys, int32_t n_keys, int32_t B);
+
+/* Static description of a status code.  Never NULL. */
+const char *dep_status_string(dep_status_t status);
+
+/* Library version, as MAJOR * 10000 + MINOR * 100 + PATCH. */
+int32_t dep_projection_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DEP_PROJECTION_H */

@@ -1,0 +1,581 @@
+// api.cpp -- the C ABI: plans (tactic tables), validation and dispatch.
+//
+// A plan mirrors DepProjection.__init__ (runtime.dep page): it is built once per
+// weight shape and batch set and keeps a table keyed by "max rows"; a batch takes
+// the entry of the smallest key >= B, else of the largest key (runtime.dep page,
+// _bins).  The run call mirrors DepProjection.run: it writes the projection into
+// the caller's preallocated output.
+#include <algorithm>
+#include <cerrno>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+using dep::RunArgs;
+
+struct dep_plan_s {
+    int64_t N = 0, K = 0;
+    bool host_only = true;
+    int device = -1;
+    int sm_count = 0;
+    std::string device_name;
+    std::vector<dep_tactic_t> table;  // sorted by max_rows, unique keys
+    void *dev_block = nullptr;        // one allocation, carved below
+    size_t dev_bytes = 0;
+    int *status = nullptr;
+    int *counters = nullptr;
+    size_t n_counters = 0;
+    float *ws = nullptr;
+    size_t ws_floats = 0;
+    uint16_t *x_stage = nullptr;
+    uint16_t *y_stage = nullptr;
+    int32_t stage_rows = 0;
+    uint64_t wait_limit_ns = 1000000000ull;  // 1 s per wait
+    bool fault_launch = false;
+    bool log = false;
+};
+
+namespace {
+
+const int32_t kDefaultBatches[] = {1, 2, 4, 8, 16, 32, 64, 128, 256};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t abytes, const void *b, size_t bbytes)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+bool env_is(const char *name, const char *value)
+{
+    const char *v = std::getenv(name);
+    return v && std::strcmp(v, value) == 0;
+}
+
+int32_t pow2_at_least(int32_t b)
+{
+    int32_t p = 1;
+    while (p < b)
+        p <<= 1;
+    return p;
+}
+
+bool tactic_valid(const dep_tactic_t &t)
+{
+    if (t.max_rows < 1)
+        return false;
+    if (t.kind == DEP_KIND_SPLITK_FMA)
+        return dep::fma_valid(t);
+    if (t.kind == DEP_KIND_TC)
+        return dep::tc_valid(t);
+    return false;
+}
+
+size_t ws_per_cta(const dep_tactic_t &t)
+{
+    return t.kind == DEP_KIND_SPLITK_FMA ? dep::fma_ws_per_cta(t) : dep::tc_ws_per_cta(t);
+}
+
+// Blocks a launch really uses: never more than the stream-K work units.
+int64_t effective_ctas(const dep_tactic_t &t, int64_t N, int64_t K)
+{
+    const int64_t U = t.kind == DEP_KIND_SPLITK_FMA ? dep::fma_units(t, N, K) : dep::tc_units(t, N, K);
+    return U < t.ctas ? U : t.ctas;
+}
+
+// Split-K partial floats a launch of tactic t on an [N,K] weight may write.
+size_t tactic_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K)
+{
+    return (size_t)effective_ctas(t, N, K) * ws_per_cta(t);
+}
+
+size_t tactic_counters(const dep_tactic_t &t, int64_t N)
+{
+    return t.kind == DEP_KIND_SPLITK_FMA ? dep::fma_counters(t, N) : dep::tc_counters(t, N);
+}
+
+// The fixed rule: warp split-K on the FMA pipe for small batches; the
+// tensor-core kernel past them (runtime.hybrid page, HybridAttention.__init__:
+// warp split-K up to 16 rows, the GEMM path past it).
+dep_tactic_t default_tactic(int32_t rows, int sm_count, bool host_only)
+{
+    dep_tactic_t t{};
+    t.max_rows = rows;
+    t.tile_k = 256;
+    t.kind = DEP_KIND_SPLITK_FMA;
+    t.cols = std::min<int32_t>(8, pow2_at_least(rows));
+    t.tile_n = t.cols >= 8 ? 32 : 64;
+    t.stages = t.cols >= 8 ? 6 : 4;
+    int per_sm = host_only ? 1 : dep::fma_blocks_per_sm(t);
+    if (per_sm < 1)
+        per_sm = 1;
+    t.ctas = sm_count * per_sm;
+    return t;
+}
+
+void sort_table(std::vector<dep_tactic_t> &table)
+{
+    std::sort(table.begin(), table.end(),
+              [](const dep_tactic_t &a, const dep_tactic_t &b) { return a.max_rows < b.max_rows; });
+}
+
+const dep_tactic_t *lookup(const dep_plan_s *p, int32_t B)
+{
+    std::vector<int32_t> keys;
+    keys.reserve(p->table.size());
+    for (const auto &t : p->table)
+        keys.push_back(t.max_rows);
+    const int32_t i = dep_bins_index(keys.data(), (int32_t)keys.size(), B);
+    return i < 0 ? nullptr : &p->table[(size_t)i];
+}
+
+// Allocate (or re-allocate) the plan's device block for its current table.
+dep_status_t allocate_device(dep_plan_s *p, size_t extra_ws_floats = 0)
+{
+    // Room for the table's tactics, and for any tactic of the same footprint
+    // per block on up to four blocks per SM (tests and tuning use other grids).
+    size_t ws = extra_ws_floats, cnt = 256;
+    int32_t rows = 1;
+    for (const auto &t : p->table) {
+        ws = std::max(ws, tactic_ws_floats(t, p->N, p->K));
+        ws = std::max(ws, (size_t)4 * (size_t)p->sm_count * ws_per_cta(t));
+        cnt = std::max(cnt, tactic_counters(t, p->N));
+        rows = std::max(rows, t.max_rows);
+    }
+    auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    const size_t status_b = 256, cnt_b = up(cnt * sizeof(int)), ws_b = up(ws * sizeof(float));
+    const size_t xs_b = up((size_t)rows * p->K * 2), ys_b = up((size_t)rows * p->N * 2);
+    const size_t total = status_b + cnt_b + ws_b + xs_b + ys_b;
+    if (p->dev_block && total <= p->dev_bytes)
+        return DEP_OK;
+    if (env_is("DEP_FAULT", "alloc"))
+        return DEP_ERR_OOM;
+    void *blk = nullptr;
+    if (cudaMalloc(&blk, total) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_OOM;
+    }
+    if (cudaMemset(blk, 0, status_b + cnt_b) != cudaSuccess) {
+        cudaFree(blk);
+        return DEP_ERR_CUDA;
+    }
+    if (p->dev_block) {
+        cudaDeviceSynchronize();
+        cudaFree(p->dev_block);
+    }
+    char *c = static_cast<char *>(blk);
+    p->dev_block = blk;
+    p->dev_bytes = total;
+    p->status = reinterpret_cast<int *>(c);
+    p->counters = reinterpret_cast<int *>(c + status_b);
+    p->n_counters = cnt_b / sizeof(int);
+    p->ws = reinterpret_cast<float *>(c + status_b + cnt_b);
+    p->ws_floats = ws_b / sizeof(float);
+    p->x_stage = reinterpret_cast<uint16_t *>(c + status_b + cnt_b + ws_b);
+    p->y_stage = reinterpret_cast<uint16_t *>(c + status_b + cnt_b + ws_b + xs_b);
+    p->stage_rows = rows;
+    return DEP_OK;
+}
+
+dep_status_t check_shape(int64_t N, int64_t K)
+{
+    if (N < 1 || K < 8 || N > INT32_MAX || K > INT32_MAX)
+        return K > 0 && K < 8 && K % 8 ? DEP_ERR_MISALIGNED : DEP_ERR_INVALID_ARG;
+    if (K % 8)
+        return DEP_ERR_MISALIGNED;
+    return DEP_OK;
+}
+
+dep_status_t make_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_batches,
+                       bool host_only, int32_t sm_count, dep_plan_t *out)
+{
+    if (!out)
+        return DEP_ERR_INVALID_ARG;
+    *out = nullptr;
+    dep_status_t st = check_shape(N, K);
+    if (st != DEP_OK)
+        return st;
+    if (n_batches < 0 || (n_batches > 0 && !batches))
+        return DEP_ERR_INVALID_ARG;
+    std::vector<int32_t> bs;
+    if (n_batches == 0)
+        bs.assign(std::begin(kDefaultBatches), std::end(kDefaultBatches));
+    else
+        bs.assign(batches, batches + n_batches);
+    for (int32_t b : bs)
+        if (b < 1)
+            return DEP_ERR_INVALID_ARG;
+    std::sort(bs.begin(), bs.end());
+    bs.erase(std::unique(bs.begin(), bs.end()), bs.end());
+
+    dep_plan_s *p = new (std::nothrow) dep_plan_s;
+    if (!p)
+        return DEP_ERR_OOM;
+    p->N = N;
+    p->K = K;
+    p->host_only = host_only;
+    p->log = env_is("DEP_LOG", "1");
+    p->fault_launch = env_is("DEP_FAULT", "launch");
+    if (host_only) {
+        if (sm_count < 1) {
+            delete p;
+            return DEP_ERR_INVALID_ARG;
+        }
+        p->sm_count = sm_count;
+        p->device_name = "host";
+    } else {
+        cudaDeviceProp prop;
+        if (cudaGetDevice(&p->device) != cudaSuccess ||
+            cudaGetDeviceProperties(&prop, p->device) != cudaSuccess) {
+            cudaGetLastError();
+            delete p;
+            return DEP_ERR_CUDA;
+        }
+        p->sm_count = prop.multiProcessorCount;
+        p->device_name = prop.name;
+        if (prop.major * 10 + prop.minor < 100) {
+            delete p;
+            return DEP_ERR_UNSUPPORTED;
+        }
+    }
+    for (int32_t b : bs)
+        p->table.push_back(default_tactic(b, p->sm_count, host_only));
+    sort_table(p->table);
+    if (!host_only) {
+        st = allocate_device(p);
+        if (st != DEP_OK) {
+            delete p;
+            return st;
+        }
+    }
+    if (p->log)
+        for (const auto &t : p->table)
+            std::fprintf(stderr, "[dep] N=%lld K=%lld rows<=%d kind=%d ctas=%d tile_n=%d stages=%d cols=%d\n",
+                         (long long)N, (long long)K, t.max_rows, t.kind, t.ctas, t.tile_n, t.stages, t.cols);
+    *out = p;
+    return DEP_OK;
+}
+
+dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const void *W, void *y,
+                      int32_t B, void *stream)
+{
+    if (!p || B < 0)
+        return DEP_ERR_INVALID_ARG;
+    if (p->host_only)
+        return DEP_ERR_UNSUPPORTED;
+    if (B == 0)
+        return DEP_OK;
+    if (!x || !W || !y || !t)
+        return DEP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y))
+        return DEP_ERR_MISALIGNED;
+    const size_t xb = (size_t)B * p->K * 2, wb = (size_t)p->N * p->K * 2, yb = (size_t)B * p->N * 2;
+    if (overlaps(y, yb, x, xb) || overlaps(y, yb, W, wb))
+        return DEP_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != p->device) {
+        cudaGetLastError();
+        return DEP_ERR_INVALID_ARG;
+    }
+    if (tactic_ws_floats(*t, p->N, p->K) > p->ws_floats || tactic_counters(*t, p->N) > p->n_counters)
+        return DEP_ERR_INVALID_ARG;
+    if (p->fault_launch)
+        return DEP_ERR_CUDA;
+    RunArgs a;
+    a.x = static_cast<const uint16_t *>(x);
+    a.W = static_cast<const uint16_t *>(W);
+    a.y = static_cast<uint16_t *>(y);
+    a.B = B;
+    a.N = p->N;
+    a.K = p->K;
+    a.ws = p->ws;
+    a.ws_floats = p->ws_floats;
+    a.counters = p->counters;
+    a.n_counters = p->n_counters;
+    a.status = p->status;
+    a.stream = static_cast<cudaStream_t>(stream);
+    a.wait_limit_ns = p->wait_limit_ns;
+    cudaError_t e = t->kind == DEP_KIND_SPLITK_FMA ? dep::fma_run(*t, a) : dep::tc_run(*t, a);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    return DEP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t dep_bins_index(const int32_t *keys, int32_t n_keys, int32_t B)
+{
+    if (!keys || n_keys < 1)
+        return -1;
+    int32_t best = -1, largest = 0;
+    for (int32_t i = 0; i < n_keys; ++i) {
+        if (keys[i] > keys[largest])
+            largest = i;
+        if (keys[i] >= B && (best < 0 || keys[i] < keys[best]))
+            best = i;
+    }
+    return best >= 0 ? best : largest;
+}
+
+dep_status_t dep_projection_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_batches,
+                                 uint32_t flags, dep_plan_t *out)
+{
+    if (flags & ~(DEP_PLAN_DEFAULT | DEP_PLAN_TUNE)) {
+        if (out)
+            *out = nullptr;
+        return DEP_ERR_INVALID_ARG;
+    }
+    dep_status_t st = make_plan(N, K, batches, n_batches, false, 0, out);
+    if (st != DEP_OK || !(flags & DEP_PLAN_TUNE))
+        return st;
+    return DEP_OK;  // tuning is added with the tuner
+}
+
+dep_status_t dep_projection_plan_host(int64_t N, int64_t K, const int32_t *batches,
+                                      int32_t n_batches, int32_t sm_count, dep_plan_t *out)
+{
+    return make_plan(N, K, batches, n_batches, true, sm_count, out);
+}
+
+dep_status_t dep_projection_run(dep_plan_t plan, const void *x, const void *W, void *y, int32_t B,
+                                void *stream)
+{
+    if (!plan || B < 0)
+        return DEP_ERR_INVALID_ARG;
+    if (B == 0)
+        return plan->host_only ? DEP_ERR_UNSUPPORTED : DEP_OK;
+    return run_impl(plan, lookup(plan, B), x, W, y, B, stream);
+}
+
+dep_status_t dep_projection_run_tactic(dep_plan_t plan, const dep_tactic_t *tactic, const void *x,
+                                       const void *W, void *y, int32_t B, void *stream)
+{
+    if (!tactic || !tactic_valid(*tactic))
+        return DEP_ERR_INVALID_ARG;
+    return run_impl(plan, tactic, x, W, y, B, stream);
+}
+
+dep_status_t dep_projection_run_host(dep_plan_t plan, const void *x_host, const void *W,
+                                     void *y_host, int32_t B, void *stream)
+{
+    if (!plan || B < 0)
+        return DEP_ERR_INVALID_ARG;
+    if (plan->host_only)
+        return DEP_ERR_UNSUPPORTED;
+    if (B == 0)
+        return DEP_OK;
+    if (!x_host || !y_host || B > plan->stage_rows)
+        return DEP_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t xb = (size_t)B * plan->K * 2, yb = (size_t)B * plan->N * 2;
+    if (cudaMemcpyAsync(plan->x_stage, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    dep_status_t st = run_impl(plan, lookup(plan, B), plan->x_stage, W, plan->y_stage, B, stream);
+    if (st != DEP_OK)
+        return st;
+    if (cudaMemcpyAsync(y_host, plan->y_stage, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    return DEP_OK;
+}
+
+dep_status_t dep_projection_plan_query(dep_plan_t plan, int32_t B, dep_tactic_t *out)
+{
+    if (!plan || !out || B < 1)
+        return DEP_ERR_INVALID_ARG;
+    const dep_tactic_t *t = lookup(plan, B);
+    if (!t)
+        return DEP_ERR_INTERNAL;
+    *out = *t;
+    return DEP_OK;
+}
+
+dep_status_t dep_projection_plan_table(dep_plan_t plan, dep_tactic_t *out, int32_t cap, int32_t *n)
+{
+    if (!plan || !n || cap < 0 || (cap > 0 && !out))
+        return DEP_ERR_INVALID_ARG;
+    *n = (int32_t)plan->table.size();
+    for (int32_t i = 0; i < cap && i < *n; ++i)
+        out[i] = plan->table[(size_t)i];
+    return DEP_OK;
+}
+
+dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic)
+{
+    if (!plan || !tactic || !tactic_valid(*tactic))
+        return DEP_ERR_INVALID_ARG;
+    if (!plan->host_only && (tactic_ws_floats(*tactic, plan->N, plan->K) > plan->ws_floats ||
+                             tactic_counters(*tactic, plan->N) > plan->n_counters ||
+                             tactic->max_rows > plan->stage_rows))
+        return DEP_ERR_INVALID_ARG;
+    for (auto &t : plan->table)
+        if (t.max_rows == tactic->max_rows) {
+            t = *tactic;
+            return DEP_OK;
+        }
+    plan->table.push_back(*tactic);
+    sort_table(plan->table);
+    return DEP_OK;
+}
+
+dep_status_t dep_projection_plan_workspace(dep_plan_t plan, size_t *bytes)
+{
+    if (!plan || !bytes)
+        return DEP_ERR_INVALID_ARG;
+    *bytes = plan->dev_bytes;
+    return DEP_OK;
+}
+
+dep_status_t dep_projection_plan_save(dep_plan_t plan, const char *path)
+{
+    if (!plan || !path)
+        return DEP_ERR_INVALID_ARG;
+    FILE *f = std::fopen(path, "w");
+    if (!f)
+        return DEP_ERR_IO;
+    std::string name = plan->device_name;
+    for (char &ch : name)
+        if (ch == ' ' || ch == '\t' || ch == '\n')
+            ch = '_';
+    int ok = std::fprintf(f, "dep_projection_plan 1\ndevice %s\nsms %d\nshape %lld %lld\nentries %zu\n",
+                          name.c_str(), plan->sm_count, (long long)plan->N, (long long)plan->K,
+                          plan->table.size()) > 0;
+    for (const auto &t : plan->table)
+        ok = ok && std::fprintf(f, "%d %d %d %d %d %d %d\n", t.max_rows, t.kind, t.ctas, t.tile_n,
+                                t.tile_k, t.stages, t.cols) > 0;
+    ok = (std::fclose(f) == 0) && ok;
+    return ok ? DEP_OK : DEP_ERR_IO;
+}
+
+dep_status_t dep_projection_plan_load(const char *path, int64_t N, int64_t K, dep_plan_t *out)
+{
+    if (!out)
+        return DEP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!path)
+        return DEP_ERR_INVALID_ARG;
+    FILE *f = std::fopen(path, "r");
+    if (!f)
+        return DEP_ERR_IO;
+    char name[512] = {0};
+    int version = 0, sms = 0;
+    long long fn = 0, fk = 0;
+    size_t count = 0;
+    std::vector<dep_tactic_t> table;
+    bool ok = std::fscanf(f, "dep_projection_plan %d device %511s sms %d shape %lld %lld entries %zu",
+                          &version, name, &sms, &fn, &fk, &count) == 6 &&
+              version == 1 && count >= 1 && count <= 4096;
+    for (size_t i = 0; ok && i < count; ++i) {
+        dep_tactic_t t{};
+        ok = std::fscanf(f, "%d %d %d %d %d %d %d", &t.max_rows, &t.kind, &t.ctas, &t.tile_n,
+                         &t.tile_k, &t.stages, &t.cols) == 7 &&
+             tactic_valid(t);
+        table.push_back(t);
+    }
+    std::fclose(f);
+    if (!ok)
+        return DEP_ERR_IO;
+    if (fn != N || fk != K)
+        return DEP_ERR_INVALID_ARG;
+    std::vector<int32_t> keys;
+    for (const auto &t : table)
+        keys.push_back(t.max_rows);
+    dep_plan_t p = nullptr;
+    dep_status_t st = make_plan(N, K, keys.data(), (int32_t)keys.size(), false, 0, &p);
+    if (st != DEP_OK)
+        return st;
+    if (p->sm_count != sms) {
+        dep_projection_plan_destroy(p);
+        return DEP_ERR_UNSUPPORTED;
+    }
+    p->table = table;
+    sort_table(p->table);
+    st = allocate_device(p);
+    if (st != DEP_OK) {
+        dep_projection_plan_destroy(p);
+        return st;
+    }
+    *out = p;
+    return DEP_OK;
+}
+
+void dep_projection_plan_destroy(dep_plan_t plan)
+{
+    if (!plan)
+        return;
+    if (plan->dev_block) {
+        int prev = -1;
+        cudaGetDevice(&prev);
+        cudaSetDevice(plan->device);
+        cudaDeviceSynchronize();
+        cudaFree(plan->dev_block);
+        if (prev >= 0)
+            cudaSetDevice(prev);
+        cudaGetLastError();
+    }
+    delete plan;
+}
+
+dep_status_t dep_projection_device_status(dep_plan_t plan, void *stream, int32_t *code)
+{
+    if (!plan || !code)
+        return DEP_ERR_INVALID_ARG;
+    *code = 0;
+    if (plan->host_only)
+        return DEP_ERR_UNSUPPORTED;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess ||
+        cudaMemcpy(&h, plan->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(plan->status, 0, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    *code = h;
+    return h ? DEP_ERR_TIMEOUT : DEP_OK;
+}
+
+dep_status_t dep_projection_selftest_timeout(int32_t limit_us, int32_t *code)
+{
+    if (!code || limit_us < 1 || limit_us > 10000000)
+        return DEP_ERR_INVALID_ARG;
+    *code = 0;
+    if (dep::selftest_timeout(limit_us, code) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    return DEP_OK;
+}
+
+const char *dep_status_string(dep_status_t s)
+{
+    switch (s) {
+    case DEP_OK: return "ok";
+    case DEP_ERR_INVALID_ARG: return "invalid argument";
+    case DEP_ERR_UNSUPPORTED: return "unsupported";
+    case DEP_ERR_MISALIGNED: return "misaligned pointer or K not a multiple of 8";
+    case DEP_ERR_CUDA: return "CUDA error";
+    case DEP_ERR_OOM: return "out of device memory";
+    case DEP_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    case DEP_ERR_INTERNAL: return "internal error";
+    case DEP_ERR_IO: return "plan file error";
+    }
+    return "unknown status";
+}
+
+int32_t dep_projection_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/dep_projection.h"
+
+namespace dep {
+
+// One launch's operands and the plan-owned scratch it may use.
+struct RunArgs {
+    const uint16_t *x;  // [B, K] BF16 bits, device
+    const uint16_t *W;  // [N, K]
+    uint16_t *y;        // [B, N]
+    int32_t B;
+    int64_t N, K;
+    float *ws;          // split-K partials
+    size_t ws_floats;
+    int *counters;      // per-tile arrival counters (zero between launches)
+    size_t n_counters;
+    int *status;        // device status word (0 = fine)
+    cudaStream_t stream;
+    uint64_t wait_limit_ns;
+};
+
+// Stream-K split: U work units over C blocks, block c owns [begin(c), begin(c+1)).
+__host__ __device__ inline int64_t sk_begin(int64_t c, int64_t U, int64_t C)
+{
+    return (c * U) / C;
+}
+// The block owning unit u (the c with begin(c) <= u < begin(c+1); needs U >= C).
+__host__ __device__ inline int64_t sk_owner(int64_t u, int64_t U, int64_t C)
+{
+    return ((u + 1) * C - 1) / U;
+}
+
+// ---- split-K FMA tactic (splitk_fma.cu) ----
+bool fma_valid(const dep_tactic_t &t);
+int64_t fma_units(const dep_tactic_t &t, int64_t N, int64_t K);  // stream-K work units
+size_t fma_ws_per_cta(const dep_tactic_t &t);                     // partial floats per block
+size_t fma_counters(const dep_tactic_t &t, int64_t N);
+int fma_blocks_per_sm(const dep_tactic_t &t);  // occupancy, 0 if it cannot launch
+cudaError_t fma_run(const dep_tactic_t &t, const RunArgs &a);
+cudaError_t selftest_timeout(int32_t limit_us, int32_t *code);
+
+// ---- tcgen05 tactic (tc_gemm.cu) ----
+bool tc_valid(const dep_tactic_t &t);
+int64_t tc_units(const dep_tactic_t &t, int64_t N, int64_t K);
+size_t tc_ws_per_cta(const dep_tactic_t &t);
+size_t tc_counters(const dep_tactic_t &t, int64_t N);
+int tc_blocks_per_sm(const dep_tactic_t &t);
+cudaError_t tc_run(const dep_tactic_t &t, const RunArgs &a);
+
+// ---- TMA descriptors (tma.cpp) ----
+// 2-D BF16 tensor map over a row-major [outer, inner] array with a row pitch of
+// `inner` elements; box = [box_outer rows, box_inner elements]; out-of-range
+// elements read as zero.
+CUresult encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                        uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+
+}  // namespace dep

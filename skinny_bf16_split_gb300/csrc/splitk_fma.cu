@@ -1,0 +1,392 @@
+// splitk_fma.cu -- weight-streaming warp split-K kernel on the FP32 FMA pipe.
+//
+// Computes y[B,N] = BF16(x[B,K] . W[N,K]^T) with FP32 accumulation for small
+// batches (runtime.hybrid page, HybridAttention.__init__: warp split-K for up to
+// 16 rows, the stock GEMM past that; runtime.dep page, module overview,
+// precision paragraph: FP32 accumulation, BF16 outputs, split-K order of its own).
+//
+// Design (sm_103a):
+//  * The weight is streamed exactly once.  Work units are (row tile t, k-tile kt)
+//    pairs of TN weight rows x 256 columns, ordered row tile major; the grid's
+//    persistent blocks take equal contiguous ranges of units (stream-K), so every
+//    SM streams the same number of weight bytes whatever N and K are.
+//  * One producer warp moves each unit's weight tile [TN x 256] and activation
+//    tile [BC x 256] into a shared-memory ring with 2-D TMA bulk tensor copies
+//    (completion on mbarriers; the weight with an L2 evict-first policy).
+//  * Eight compute warps own R weight rows each.  Lane l owns columns 8l..8l+7
+//    of every k-tile (one 16-byte shared load per row) and keeps one FP32 FMA
+//    chain per (row, batch row); k-tiles are visited in increasing order.
+//  * Where a block's range ends inside a row tile, the lanes' chains are summed
+//    by an xor butterfly (16, 8, 4, 2, 1) and the warp's partials go to the
+//    plan's workspace.  The last warp to arrive on the tile's counter (an integer
+//    atomic) adds the partials in increasing block order, rounds to BF16 and
+//    resets the counter.  No block waits for another and no float atomics are
+//    used, so results are identical from run to run.
+//  * Every wait is bounded in time; a warp that gives up records a code in the
+//    device status word and leaves.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dep {
+namespace {
+
+constexpr int kWarps = 8;                 // compute warps per block
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kKT = 256;                  // columns per k-tile: 32 lanes x 8
+constexpr int kRowBytes = kKT * 2;        // one tile row in shared memory
+
+template <int BC>
+struct Shape {
+    static constexpr int R = BC >= 8 ? 4 : 8;  // weight rows per compute warp
+    static constexpr int TN = kWarps * R;      // weight rows per tile
+    static constexpr int STAGE_BYTES = (TN + BC) * kRowBytes;
+};
+
+__device__ __forceinline__ void unpack8(const uint4 v, float f[8])
+{
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);              // lower address: element 2i
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);  // element 2i + 1
+    }
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float v)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+template <int BC>
+__global__ void __launch_bounds__(kThreads, 1)
+    splitk_fma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                      uint16_t *__restrict__ y, int B, int N, int K, int stages,
+                      float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ status,
+                      uint64_t limit_ns)
+{
+    constexpr int R = Shape<BC>::R, TN = Shape<BC>::TN, STAGE_BYTES = Shape<BC>::STAGE_BYTES;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * STAGE_BYTES);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + stages);
+
+    const int64_t T = (N + TN - 1) / TN, KTILES = (K + kKT - 1) / kKT, U = T * KTILES;
+    const int64_t C = gridDim.x, c = blockIdx.x;
+    const int64_t u_begin = sk_begin(c, U, C), u_end = sk_begin(c + 1, U, C);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, kWarps);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == kWarps) {  // ---------------- producer warp ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            prefetch_tmap(&tmX);
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            for (int64_t u = u_begin; u < u_end; ++u) {
+                if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, limit_ns)) {
+                    record_status(status, DEP_DEV_TIMEOUT_PRODUCER);
+                    break;
+                }
+                const uint32_t dst = smem_u32(smem + (size_t)s * STAGE_BYTES);
+                mbar_arrive_expect_tx(full0 + 8 * s, STAGE_BYTES);
+                const int t = (int)(u / KTILES), kt = (int)(u % KTILES);
+                tma_load_2d(dst, &tmW, kt * kKT, t * TN, full0 + 8 * s, pol_w);
+                tma_load_2d(dst + TN * kRowBytes, &tmX, kt * kKT, 0, full0 + 8 * s, pol_x);
+                ++issued;
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            // Drain: the block must not exit while a copy into its shared memory
+            // is in flight.  Walk back over the last `stages` fills.
+            const int64_t n = issued < stages ? issued : stages;
+            int ds = s;
+            uint32_t dph = ph;
+            for (int64_t i = 0; i < n; ++i) {
+                if (--ds < 0) {
+                    ds = stages - 1;
+                    dph ^= 1u;
+                }
+                if (!mbar_wait(full0 + 8 * ds, dph, limit_ns))
+                    record_status(status, DEP_DEV_TIMEOUT_PRODUCER);
+            }
+        }
+        return;
+    }
+
+    // ---------------- compute warps ----------------
+    float acc[R][BC];
+    int s = 0;
+    uint32_t ph = 0;
+    const int64_t first_t = u_begin / KTILES;
+    int64_t u = u_begin;
+    while (u < u_end) {
+        const int64_t t = u / KTILES;
+        const int64_t seg_end = u_end < (t + 1) * KTILES ? u_end : (t + 1) * KTILES;
+        const bool whole = (u == t * KTILES) && (seg_end == (t + 1) * KTILES);
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int b = 0; b < BC; ++b)
+                acc[i][b] = 0.0f;
+
+        for (; u < seg_end; ++u) {
+            if (!mbar_wait(full0 + 8 * s, ph, limit_ns)) {
+                record_status(status, DEP_DEV_TIMEOUT_CONSUMER);
+                return;
+            }
+            const uint8_t *st = smem + (size_t)s * STAGE_BYTES;
+            float xv[BC][8];
+#pragma unroll
+            for (int b = 0; b < BC; ++b)
+                unpack8(*reinterpret_cast<const uint4 *>(st + (TN + b) * kRowBytes + lane * 16), xv[b]);
+#pragma unroll
+            for (int i = 0; i < R; ++i) {
+                float wv[8];
+                unpack8(*reinterpret_cast<const uint4 *>(st + (warp * R + i) * kRowBytes + lane * 16), wv);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+#pragma unroll
+                    for (int b = 0; b < BC; ++b)
+                        acc[i][b] = __fmaf_rn(wv[j], xv[b][j], acc[i][b]);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(empty0 + 8 * s);
+            if (++s == stages) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+
+        // ---- segment epilogue: warp sum, then direct store or split-K fix-up ----
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int b = 0; b < BC; ++b)
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1)
+                    acc[i][b] += __shfl_xor_sync(0xFFFFFFFFu, acc[i][b], off);
+
+        // lane L keeps value (i, b) = (L / BC, L % BC)
+        float mine = 0.0f;
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int b = 0; b < BC; ++b)
+                if (i * BC + b == lane)
+                    mine = acc[i][b];
+        const bool have = lane < R * BC;
+        const int mb = lane % BC;
+        const int row = warp * R + lane / BC;  // row within the tile
+        const int64_t n = t * TN + row;
+
+        if (whole) {
+            if (have && mb < B && n < N)
+                y[(int64_t)mb * N + n] = to_bf16(mine);
+            continue;
+        }
+        const int slot = (t == first_t) ? 0 : 1;
+        if (have)
+            __stcg(&ws[((c * 2 + slot) * BC + mb) * TN + row], mine);
+        __threadfence();
+        __syncwarp();
+        int prev = 0;
+        if (lane == 0)
+            prev = atomicAdd(&counters[t * kWarps + warp], 1);
+        prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+        const int64_t c0 = sk_owner(t * KTILES, U, C), c1 = sk_owner(t * KTILES + KTILES - 1, U, C);
+        if (prev != (int)(c1 - c0))
+            continue;  // another block finishes this tile
+        __threadfence();
+        if (have) {
+            float sum = 0.0f;
+            for (int64_t cc = c0; cc <= c1; ++cc) {
+                const int sl = (t == sk_begin(cc, U, C) / KTILES) ? 0 : 1;
+                const float p = __ldcg(&ws[((cc * 2 + sl) * BC + mb) * TN + row]);
+                sum = (cc == c0) ? p : sum + p;
+            }
+            if (mb < B && n < N)
+                y[(int64_t)mb * N + n] = to_bf16(sum);
+        }
+        if (lane == 0)
+            counters[t * kWarps + warp] = 0;  // ready for the next launch
+    }
+}
+
+// One block whose wait can never be satisfied: exercises the give-up path.
+__global__ void selftest_timeout_kernel(int *status, uint64_t limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (!mbar_wait(smem_u32(&bar), 0, limit_ns) && threadIdx.x == 0)
+        record_status(status, DEP_DEV_TIMEOUT_CONSUMER);
+}
+
+template <int BC>
+size_t smem_bytes(int stages)
+{
+    return (size_t)stages * Shape<BC>::STAGE_BYTES + 2 * (size_t)stages * sizeof(uint64_t);
+}
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+template <int BC>
+cudaError_t prepare()
+{
+    static cudaError_t once = cudaFuncSetAttribute(
+        splitk_fma_kernel<BC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+    return once;
+}
+
+template <int BC>
+cudaError_t run_bc(const dep_tactic_t &t, const RunArgs &a)
+{
+    cudaError_t e = prepare<BC>();
+    if (e != cudaSuccess)
+        return e;
+    constexpr int TN = Shape<BC>::TN;
+    CUtensorMap tmW, tmX;
+    if (encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kKT, TN,
+                       CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int64_t T = (a.N + TN - 1) / TN, KT = (a.K + kKT - 1) / kKT, U = T * KT;
+    const int grid = (int)(U < t.ctas ? U : t.ctas);
+    const size_t smem = smem_bytes<BC>(t.stages);
+    for (int32_t r0 = 0; r0 < a.B; r0 += BC) {
+        const int32_t rows = a.B - r0 < BC ? a.B - r0 : BC;
+        if (encode_bf16_2d(&tmX, a.x + (size_t)r0 * a.K, (uint64_t)a.K, (uint64_t)rows, kKT, BC,
+                           CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        splitk_fma_kernel<BC><<<grid, kThreads, smem, a.stream>>>(
+            tmW, tmX, a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, a.ws, a.counters,
+            a.status, a.wait_limit_ns);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+template <int BC>
+int blocks_per_sm(int stages)
+{
+    if (prepare<BC>() != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitk_fma_kernel<BC>, kThreads,
+                                                      smem_bytes<BC>(stages)) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+size_t smem_for(const dep_tactic_t &t)
+{
+    switch (t.cols) {
+    case 1: return smem_bytes<1>(t.stages);
+    case 2: return smem_bytes<2>(t.stages);
+    case 4: return smem_bytes<4>(t.stages);
+    case 8: return smem_bytes<8>(t.stages);
+    default: return 0;
+    }
+}
+
+int tile_rows(int cols)
+{
+    switch (cols) {
+    case 1: return Shape<1>::TN;
+    case 2: return Shape<2>::TN;
+    case 4: return Shape<4>::TN;
+    case 8: return Shape<8>::TN;
+    default: return 0;
+    }
+}
+
+}  // namespace
+
+bool fma_valid(const dep_tactic_t &t)
+{
+    if (t.kind != DEP_KIND_SPLITK_FMA || t.ctas < 1 || t.tile_k != kKT)
+        return false;
+    if (tile_rows(t.cols) == 0 || t.tile_n != tile_rows(t.cols))
+        return false;
+    if (t.stages < 2 || t.stages > 16)
+        return false;
+    return smem_for(t) <= kMaxSmem;
+}
+
+int64_t fma_units(const dep_tactic_t &t, int64_t N, int64_t K)
+{
+    return ((N + t.tile_n - 1) / t.tile_n) * ((K + kKT - 1) / kKT);
+}
+
+size_t fma_ws_per_cta(const dep_tactic_t &t)
+{
+    return 2 * (size_t)t.cols * (size_t)t.tile_n;  // head and tail segment partials
+}
+
+size_t fma_counters(const dep_tactic_t &t, int64_t N)
+{
+    return (size_t)((N + t.tile_n - 1) / t.tile_n) * kWarps;
+}
+
+int fma_blocks_per_sm(const dep_tactic_t &t)
+{
+    switch (t.cols) {
+    case 1: return blocks_per_sm<1>(t.stages);
+    case 2: return blocks_per_sm<2>(t.stages);
+    case 4: return blocks_per_sm<4>(t.stages);
+    case 8: return blocks_per_sm<8>(t.stages);
+    default: return 0;
+    }
+}
+
+cudaError_t fma_run(const dep_tactic_t &t, const RunArgs &a)
+{
+    switch (t.cols) {
+    case 1: return run_bc<1>(t, a);
+    case 2: return run_bc<2>(t, a);
+    case 4: return run_bc<4>(t, a);
+    case 8: return run_bc<8>(t, a);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t selftest_timeout(int32_t limit_us, int32_t *code)
+{
+    int *d = nullptr;
+    cudaError_t e = cudaMalloc(&d, sizeof(int));
+    if (e != cudaSuccess)
+        return e;
+    e = cudaMemset(d, 0, sizeof(int));
+    if (e == cudaSuccess) {
+        selftest_timeout_kernel<<<1, 32>>>(d, (uint64_t)limit_us * 1000ull);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    int h = 0;
+    if (e == cudaSuccess)
+        e = cudaMemcpy(&h, d, sizeof(int), cudaMemcpyDeviceToHost);
+    cudaFree(d);
+    *code = h;
+    return e;
+}
+
+}  // namespace dep

@@ -18,3 +18,13 @@ def orc():
     import oracle
     oracle.lib()  # build once per session
     return oracle
+
+
+@pytest.fixture(scope="session")
+def dep():
+    """The library's Python binding, with the library built for sm_103a."""
+    from skinny_bf16_split_gb300 import build as _b
+    _b.build()
+    import skinny_bf16_split_gb300 as d
+    d.lib()
+    return d

@@ -1,0 +1,152 @@
+"""Host-side tests of the C ABI: no GPU, no compute calls.
+
+The library loads and exports every symbol the header declares; the binning
+rule matches the page's (runtime.dep page, _bins: the smallest key >= B, else
+the largest key); plan tables, validation and serialisation behave as the
+header documents.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "dep_projection.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dep_\w+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(dep):
+    names = declared_functions()
+    assert len(names) >= 15
+    for name in names:
+        assert hasattr(dep.lib(), name), name
+    assert sorted(dep.EXPORTS) == names
+
+
+def bins_rule(keys, B):
+    """The page's rule, restated: smallest key >= B, else the largest key."""
+    at_least = [k for k in keys if k >= B]
+    return min(at_least) if at_least else max(keys)
+
+
+def test_bins_rule_matches_page(dep):
+    rng = np.random.default_rng(0)
+    for _ in range(500):
+        keys = list(rng.choice(np.arange(1, 300), rng.integers(1, 10), replace=False))
+        for B in list(rng.integers(1, 400, 10)) + [1, max(keys), max(keys) + 1]:
+            i = dep.dep_bins_index(keys, int(B))
+            assert keys[i] == bins_rule(keys, int(B))
+    assert dep.dep_bins_index([], 3) == -1
+
+
+def test_default_table_follows_split_rule(dep):
+    """Default table: one entry per requested batch, split-K kinds for small
+    batches (runtime.hybrid page, HybridAttention.__init__)."""
+    plan = dep.dep_projection_plan_host(7168, 12288, [16, 1, 4, 2, 8, 4], 152)
+    try:
+        table = dep.dep_projection_plan_table(plan)
+        assert [t.max_rows for t in table] == [1, 2, 4, 8, 16]
+        for t in table:
+            assert t.ctas >= 152 and t.stages >= 2
+            assert t.kind in (dep.DEP_KIND_SPLITK_FMA, dep.DEP_KIND_TC)
+            if t.max_rows <= 4:
+                assert t.kind == dep.DEP_KIND_SPLITK_FMA
+        for B, key in [(1, 1), (3, 4), (5, 8), (16, 16), (17, 16), (1000, 16)]:
+            assert dep.dep_projection_plan_query(plan, B).max_rows == key
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+def test_default_batches_when_none_given(dep):
+    plan = dep.dep_projection_plan_host(14560, 7168, [], 152)
+    try:
+        assert [t.max_rows for t in dep.dep_projection_plan_table(plan)] == [1, 2, 4, 8, 16, 32, 64, 128, 256]
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("N,K,batches,sms,status", [
+    (0, 64, [1], 152, "DEP_ERR_INVALID_ARG"),
+    (64, 0, [1], 152, "DEP_ERR_INVALID_ARG"),
+    (64, 12, [1], 152, "DEP_ERR_MISALIGNED"),
+    (64, 100, [1], 152, "DEP_ERR_MISALIGNED"),
+    (64, 64, [0], 152, "DEP_ERR_INVALID_ARG"),
+    (64, 64, [-3], 152, "DEP_ERR_INVALID_ARG"),
+    (64, 64, [1], 0, "DEP_ERR_INVALID_ARG"),
+])
+def test_plan_argument_errors(dep, N, K, batches, sms, status):
+    with pytest.raises(dep.DepError) as e:
+        dep.dep_projection_plan_host(N, K, batches, sms)
+    assert e.value.status == getattr(dep, status)
+
+
+def test_host_plan_cannot_run(dep):
+    plan = dep.dep_projection_plan_host(64, 64, [1], 152)
+    try:
+        with pytest.raises(dep.DepError) as e:
+            dep.dep_projection_run(plan, 16, 16, 16, 1, 0)
+        assert e.value.status == dep.DEP_ERR_UNSUPPORTED
+        with pytest.raises(dep.DepError) as e:
+            dep.dep_projection_run(plan, 16, 16, 16, -1, 0)
+        assert e.value.status == dep.DEP_ERR_INVALID_ARG
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+def test_plan_set_validates_and_inserts(dep):
+    plan = dep.dep_projection_plan_host(7168, 12288, [1, 16], 152)
+    try:
+        t = dep.dep_projection_plan_query(plan, 1)
+        t.max_rows, t.cols, t.tile_n, t.stages = 3, 4, 64, 3
+        dep.dep_projection_plan_set(plan, t)
+        assert [x.max_rows for x in dep.dep_projection_plan_table(plan)] == [1, 3, 16]
+        assert dep.dep_projection_plan_query(plan, 2).cols == 4
+        bad = dep.dep_tactic_t(**{**t.as_dict(), "cols": 3})
+        with pytest.raises(dep.DepError):
+            dep.dep_projection_plan_set(plan, bad)
+        bad = dep.dep_tactic_t(**{**t.as_dict(), "kind": 9})
+        with pytest.raises(dep.DepError):
+            dep.dep_projection_plan_set(plan, bad)
+        bad = dep.dep_tactic_t(**{**t.as_dict(), "stages": 40})
+        with pytest.raises(dep.DepError):
+            dep.dep_projection_plan_set(plan, bad)
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+def test_plan_save_format(dep, tmp_path):
+    plan = dep.dep_projection_plan_host(49376, 7168, [1, 4, 8, 16], 152)
+    try:
+        path = str(tmp_path / "plan.txt")
+        dep.dep_projection_plan_save(plan, path)
+        lines = open(path).read().split("\n")
+        assert lines[0] == "dep_projection_plan 1"
+        assert lines[2] == "sms 152" and lines[3] == "shape 49376 7168" and lines[4] == "entries 4"
+        rows = [list(map(int, l.split())) for l in lines[5:9]]
+        table = dep.dep_projection_plan_table(plan)
+        assert rows == [[t.max_rows, t.kind, t.ctas, t.tile_n, t.tile_k, t.stages, t.cols] for t in table]
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+def test_plan_load_rejects_bad_files(dep, tmp_path):
+    p = tmp_path / "bad.txt"
+    p.write_text("not a plan\n")
+    with pytest.raises(dep.DepError) as e:
+        dep.dep_projection_plan_load(str(p), 64, 64)
+    assert e.value.status == dep.DEP_ERR_IO
+    with pytest.raises(dep.DepError) as e:
+        dep.dep_projection_plan_load(str(tmp_path / "missing.txt"), 64, 64)
+    assert e.value.status == dep.DEP_ERR_IO
+
+
+def test_status_strings(dep):
+    for s in range(0, 9):
+        assert dep.dep_status_string(s)
+    assert dep.dep_status_string(1234) == "unknown status"

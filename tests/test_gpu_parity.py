@@ -1,0 +1,286 @@
+"""GPU parity of the decode projection against the CPU oracle and the FP32 mirror.
+
+Every case calls the CUDA path through the C ABI (the ctypes binding) and
+compares element by element: against the exact oracle within the acceptance
+tolerance |y - y_ref| <= 2^-7 |y_ref| + 1e-3 rms(y_ref), and -- for the split-K
+FMA tactic, whose summation order is fixed and restated in oracle/mirror.c --
+against the FP32 mirror bit for bit.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from gpu_util import empty_out, to_dev, to_host  # noqa: E402
+from helpers import exact_bf16, within_tolerance  # noqa: E402
+from skinny_bf16_split_gb300 import synth  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+
+def fma_tactic(dep, cols, ctas, stages=None, max_rows=None):
+    tn = 32 if cols >= 8 else 64
+    return dep.dep_tactic_t(max_rows=max_rows or cols, kind=dep.DEP_KIND_SPLITK_FMA, ctas=ctas,
+                            tile_n=tn, tile_k=256, stages=stages or (6 if cols >= 8 else 4),
+                            cols=cols)
+
+
+@pytest.fixture(scope="module")
+def plan_cache(dep):
+    plans = {}
+    yield plans
+    for p in plans.values():
+        dep.dep_projection_plan_destroy(p)
+
+
+def get_plan(dep, cache, N, K, batches=(1, 2, 4, 8, 16, 32, 64, 128, 256)):
+    key = (N, K, tuple(batches))
+    if key not in cache:
+        cache[key] = dep.dep_projection_plan(N, K, list(batches))
+    return cache[key]
+
+
+def run(dep, plan, x, W, N, tactic=None):
+    xd, Wd = to_dev(x), to_dev(W)
+    y = empty_out(x.shape[0], N)
+    if tactic is None:
+        dep.dep_projection_run(plan, xd, Wd, y, x.shape[0])
+    else:
+        dep.dep_projection_run_tactic(plan, tactic, xd, Wd, y, x.shape[0])
+    torch.cuda.synchronize()
+    return to_host(y)
+
+
+def test_bounded_wait_gives_up_and_reports(dep):
+    """A wait that can never be satisfied returns by itself with its code."""
+    assert dep.dep_projection_selftest_timeout(2000) == dep.DEP_DEV_TIMEOUT_CONSUMER
+    # the context is still usable afterwards
+    a = torch.ones(4, device="cuda")
+    assert float(a.sum()) == 4.0
+
+
+# shapes spanning several tiles plus ragged tails in N (tile 32/64) and K (tile 256)
+SHAPES = [(333, 3000), (64, 256), (97, 264), (1, 8), (1000, 1032)]
+
+
+@pytest.mark.parametrize("N,K", SHAPES)
+@pytest.mark.parametrize("cols", [1, 2, 4, 8])
+@pytest.mark.parametrize("ctas", [1, 7, 152, 1000])
+def test_fma_bitexact_vs_mirror(dep, orc, plan_cache, N, K, cols, ctas):
+    B = {1: 1, 2: 2, 4: 3, 8: 8}[cols]
+    x = synth.normal_bf16(N + cols, 2, (B, K))
+    W = synth.normal_bf16(N + ctas, 1, (N, K), sigma=0.02)
+    t = fma_tactic(dep, cols, ctas)
+    y = run(dep, get_plan(dep, plan_cache, N, K), x, W, N, t)
+    T = -(-N // t.tile_n) * -(-K // 256)
+    want = orc.mirror_fma(x, W, min(ctas, T), t.tile_n)
+    np.testing.assert_array_equal(y, want)
+    ok, worst, idx = within_tolerance(y, orc.linear(x, W))
+    assert ok, (worst, idx)
+
+
+@pytest.mark.parametrize("B", list(range(1, 18)) + [31, 33, 64, 100, 256, 300])
+def test_default_plan_any_batch(dep, orc, plan_cache, B):
+    """Any B >= 1 works through the binning rule (wide batches run in passes)."""
+    N, K = 200, 1280
+    x = synth.normal_bf16(B, 2, (B, K))
+    W = synth.normal_bf16(77, 1, (N, K), sigma=0.02)
+    plan = get_plan(dep, plan_cache, N, K)
+    y = run(dep, plan, x, W, N)
+    ok, worst, idx = within_tolerance(y, orc.linear(x, W))
+    assert ok, (worst, idx)
+    t = dep.dep_projection_plan_query(plan, B)
+    if t.kind == dep.DEP_KIND_SPLITK_FMA:
+        T = -(-N // t.tile_n) * -(-K // 256)
+        np.testing.assert_array_equal(y, orc.mirror_fma(x, W, min(t.ctas, T), t.tile_n))
+
+
+def test_small_integers_exact(dep, orc, plan_cache):
+    """Small-integer inputs: all partial sums are exact in FP32, so the GPU must
+    equal the exact oracle bit for bit whatever its order."""
+    rng = np.random.default_rng(5)
+    B, N, K = 16, 300, 2048
+    xi, wi = rng.integers(-8, 9, (B, K)), rng.integers(-8, 9, (N, K))
+    x = np.vectorize(exact_bf16)(xi).astype(np.uint16)
+    W = np.vectorize(exact_bf16)(wi).astype(np.uint16)
+    want = orc.linear(x, W)
+    np.testing.assert_array_equal(want, synth.bf16_from_f64((xi @ wi.T).astype(np.float64)))
+    np.testing.assert_array_equal(run(dep, get_plan(dep, plan_cache, N, K), x, W, N), want)
+
+
+def test_closed_forms(dep, orc, plan_cache):
+    """Identity-like W returns x; all-ones x returns BF16 row sums (oracle)."""
+    N, K = 128, 512
+    x = synth.normal_bf16(1, 2, (4, K))
+    W = np.zeros((N, K), dtype=np.uint16)
+    W[np.arange(N), np.arange(N)] = 0x3F80
+    y = run(dep, get_plan(dep, plan_cache, N, K), x, W, N)
+    xz = x[:, :N].copy()
+    xz[synth.bf16_to_f32(xz) == 0] = 0
+    np.testing.assert_array_equal(y, xz)
+    W = synth.normal_bf16(2, 1, (N, K), sigma=0.02)
+    ones = np.full((2, K), 0x3F80, dtype=np.uint16)
+    ok, worst, idx = within_tolerance(run(dep, get_plan(dep, plan_cache, N, K), ones, W, N),
+                                      orc.linear(ones, W))
+    assert ok, (worst, idx)
+
+
+def test_invariants_bitwise(dep, plan_cache):
+    """Negating x negates y and scaling x by 2^3 scales y: bit for bit, since
+    every FP32 step commutes with both."""
+    N, K = 500, 4096
+    x = synth.normal_bf16(3, 2, (4, K))
+    W = synth.normal_bf16(3, 1, (N, K), sigma=0.02)
+    plan = get_plan(dep, plan_cache, N, K)
+    y = run(dep, plan, x, W, N)
+    yn = run(dep, plan, x ^ np.uint16(0x8000), W, N)
+    nz = synth.bf16_to_f32(y) != 0
+    np.testing.assert_array_equal(yn[nz], y[nz] ^ np.uint16(0x8000))
+    f = synth.bf16_to_f32(x)
+    x8 = np.where(f != 0, x + np.uint16(3 << 7), x).astype(np.uint16)
+    y8 = run(dep, plan, x8, W, N)
+    np.testing.assert_array_equal(y8[nz], (y[nz] + np.uint16(3 << 7)).astype(np.uint16))
+
+
+def test_row_permutation_within_tiles(dep, plan_cache):
+    """An output's summation order depends only on its row tile and k, so
+    permuting W's rows inside aligned blocks of 32 (a whole number of rows of
+    every tile size) permutes y's columns bit for bit."""
+    N, K = 256, 2048
+    x = synth.normal_bf16(4, 2, (2, K))
+    W = synth.normal_bf16(4, 1, (N, K), sigma=0.02)
+    plan = get_plan(dep, plan_cache, N, K)
+    y = run(dep, plan, x, W, N)
+    rng = np.random.default_rng(0)
+    perm = np.concatenate([32 * j + rng.permutation(32) for j in range(N // 32)])
+    np.testing.assert_array_equal(run(dep, plan, x, W[perm], N), y[:, perm])
+
+
+def test_determinism_repeated_and_concurrent(dep, plan_cache):
+    """The same call gives the same bits every time, also with other streams busy."""
+    N, K, B = 7168, 4096, 4
+    x, W = to_dev(synth.normal_bf16(8, 2, (B, K))), to_dev(synth.normal_bf16(8, 1, (N, K), 0.02))
+    plan = get_plan(dep, plan_cache, N, K)
+    ref = empty_out(B, N)
+    dep.dep_projection_run(plan, x, W, ref, B)
+    torch.cuda.synchronize()
+    other = torch.cuda.Stream()
+    big = torch.randn(4096, 4096, device="cuda")
+    for i in range(30):
+        y = empty_out(B, N)
+        if i % 3 == 0:
+            with torch.cuda.stream(other):
+                big = big @ big * 1e-3
+        dep.dep_projection_run(plan, x, W, y, B)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), i
+
+
+def test_cuda_graph_capture_and_replay(dep, plan_cache):
+    """run() allocates nothing and synchronises nothing: it captures into a CUDA
+    graph, and replays give the eager result (counters reset themselves)."""
+    N, K, B = 1000, 3000, 4
+    x, W = to_dev(synth.normal_bf16(9, 2, (B, K))), to_dev(synth.normal_bf16(9, 1, (N, K), 0.02))
+    plan = get_plan(dep, plan_cache, N, K)
+    eager = empty_out(B, N)
+    dep.dep_projection_run(plan, x, W, eager, B)
+    torch.cuda.synchronize()
+    y = empty_out(B, N)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dep.dep_projection_run(plan, x, W, y, B, s)
+    for _ in range(5):
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), eager.view(torch.int16))
+
+
+def test_zero_batch_and_guard_bands(dep, plan_cache):
+    """B == 0 writes nothing; a normal call writes exactly y and nothing around it."""
+    N, K, B = 777, 1024, 3
+    plan = get_plan(dep, plan_cache, N, K)
+    x, W = to_dev(synth.normal_bf16(1, 2, (B, K))), to_dev(synth.normal_bf16(1, 1, (N, K), 0.02))
+    pad = 4096
+    buf = torch.full((pad + B * N + pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = buf[pad:pad + B * N].view(B, N)
+    dep.dep_projection_run(plan, x, W, y, 0)
+    torch.cuda.synchronize()
+    assert bool((buf == 7.0).all())
+    dep.dep_projection_run(plan, x, W, y, B)
+    torch.cuda.synchronize()
+    assert bool((buf[:pad] == 7.0).all()) and bool((buf[pad + B * N:] == 7.0).all())
+    assert not bool((y == 7.0).all())
+
+
+def test_argument_errors_on_device(dep, plan_cache):
+    N, K = 64, 64
+    plan = get_plan(dep, plan_cache, N, K)
+    x = torch.zeros(2, K, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(N, K, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(2, N, dtype=torch.bfloat16, device="cuda")
+    cases = [
+        (lambda: dep.dep_projection_run(plan, x, W, y, -1), dep.DEP_ERR_INVALID_ARG),
+        (lambda: dep.dep_projection_run(plan, 0, W, y, 2), dep.DEP_ERR_INVALID_ARG),
+        (lambda: dep.dep_projection_run(plan, x.data_ptr() + 2, W, y, 2), dep.DEP_ERR_MISALIGNED),
+        (lambda: dep.dep_projection_run(plan, x, W, W.data_ptr(), 2), dep.DEP_ERR_INVALID_ARG),
+        (lambda: dep.dep_projection_run(plan, x, W, x.data_ptr(), 1), dep.DEP_ERR_INVALID_ARG),
+    ]
+    for fn, status in cases:
+        with pytest.raises(dep.DepError) as e:
+            fn()
+        assert e.value.status == status
+    assert dep.dep_projection_device_status(plan) == 0
+    # a grid whose split-K partials exceed the plan's workspace is refused
+    N, K = 7168, 12288
+    big = get_plan(dep, plan_cache, N, K, (1, 2, 4, 8, 16))
+    x = torch.zeros(2, K, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(N, K, dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(2, N, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(dep.DepError) as e:
+        dep.dep_projection_run_tactic(big, fma_tactic(dep, 8, 10 ** 6), x, W, y, 2)
+    assert e.value.status == dep.DEP_ERR_INVALID_ARG
+
+
+def test_run_host_end_to_end(dep, orc, plan_cache):
+    N, K, B = 640, 2048, 5
+    plan = get_plan(dep, plan_cache, N, K)
+    x = synth.normal_bf16(2, 2, (B, K))
+    W = synth.normal_bf16(2, 1, (N, K), sigma=0.02)
+    xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((B, N), dtype=torch.bfloat16).pin_memory()
+    Wd = to_dev(W)
+    dep.dep_projection_run_host(plan, xh, Wd, yh, B)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(yh.view(torch.int16).numpy().view(np.uint16),
+                                  run(dep, plan, x, W, N))
+
+
+def test_plan_save_load_roundtrip(dep, plan_cache, tmp_path):
+    N, K = 7168, 12288
+    plan = get_plan(dep, plan_cache, N, K, (1, 2, 4, 8, 16))
+    path = str(tmp_path / "plan.txt")
+    dep.dep_projection_plan_save(plan, path)
+    p2 = dep.dep_projection_plan_load(path, N, K)
+    try:
+        assert [t.as_dict() for t in dep.dep_projection_plan_table(p2)] == \
+               [t.as_dict() for t in dep.dep_projection_plan_table(plan)]
+        with pytest.raises(dep.DepError) as e:
+            dep.dep_projection_plan_load(path, N, K + 8)
+        assert e.value.status == dep.DEP_ERR_INVALID_ARG
+    finally:
+        dep.dep_projection_plan_destroy(p2)
+
+
+def test_stock_gemm_within_tolerance_of_oracle(orc):
+    """Context: torch.mm (the stock path the pages fall back to) sits within the
+    same tolerance of the oracle."""
+    N, K, B = 512, 7168, 16
+    x = synth.normal_bf16(6, 2, (B, K))
+    W = synth.normal_bf16(6, 1, (N, K), sigma=0.02)
+    y = to_host(torch.mm(to_dev(x), to_dev(W).t()))
+    ok, worst, idx = within_tolerance(y, orc.linear(x, W))
+    assert ok, (worst, idx)
