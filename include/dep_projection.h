@@ -136,6 +136,31 @@ dep_status_t dep_projection_run_tactic(dep_plan_t plan, const dep_tactic_t *tact
 dep_status_t dep_projection_run_host(dep_plan_t plan, const void *x_host, const void *W,
                                      void *y_host, int32_t B, void *stream);
 
+/*
+ * No counterpart in the pages: an addition of this library for callers that
+ * must not allocate device memory -- code running inside a device-memory
+ * allocator or pool (allocating there would re-enter it), hosts that reserve
+ * all device memory up front and allow no other allocation, and latency-bound
+ * paths that cannot afford cudaMalloc's implicit synchronisation.  They cannot
+ * build a plan, since a plan allocates its workspace.
+ *
+ * y[B,N] = BF16(x[B,K] . W[N,K]^T) with the split-K FMA kernel, no plan, and no
+ * allocation: the kernel's scratch (status word, tile counters, split-K
+ * partials) is one 1 MiB array compiled into the library, which every GPU that
+ * loads the library holds until the process exits.  Limits: N <= 262144 rows
+ * (the counters) and at most 383 SMs (the partials); larger shapes return
+ * DEP_ERR_UNSUPPORTED.  Same layouts, alignment and argument errors as
+ * dep_projection_run; B == 0 does nothing.  The first call on a device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call clears the
+ * counters and status word on `stream` before its kernel.  All calls share the
+ * one array: calls that overlap on the GPU (other streams, other threads) race
+ * and give wrong results.  Give-ups of the kernel's bounded waits are not
+ * reported by this entry point.
+ */
+dep_status_t dep_projection_run_static(const void *x, const void *W, void *y, int64_t N,
+                                       int64_t K, int32_t B, void *stream);
+
 /* The tactic the plan uses for a batch of B >= 1 rows. */
 dep_status_t dep_projection_plan_query(dep_plan_t plan, int32_t B, dep_tactic_t *out);
 

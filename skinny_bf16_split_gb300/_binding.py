@@ -42,7 +42,7 @@ EXPORTS = (
     "dep_projection_plan_table", "dep_projection_plan_set", "dep_projection_plan_workspace",
     "dep_projection_plan_save", "dep_projection_plan_load", "dep_projection_plan_destroy",
     "dep_projection_device_status", "dep_projection_selftest_timeout", "dep_bins_index",
-    "dep_status_string", "dep_projection_version",
+    "dep_status_string", "dep_projection_version", "dep_projection_run_static",
 )
 
 
@@ -96,6 +96,7 @@ def lib():
         "dep_bins_index": ([P(i32), i32, i32], i32),
         "dep_status_string": ([i32], ctypes.c_char_p),
         "dep_projection_version": ([], i32),
+        "dep_projection_run_static": ([vp, vp, vp, i64, i64, i32, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -238,6 +239,18 @@ def dep_projection_selftest_timeout(limit_us: int) -> int:
     _check(lib().dep_projection_selftest_timeout(limit_us, ctypes.byref(code)),
            "dep_projection_selftest_timeout")
     return code.value
+
+
+def dep_projection_run_static(x, W, y, N: int | None = None, K: int | None = None,
+                              B: int | None = None, stream=None) -> None:
+    """The no-allocation entry point (see include/dep_projection.h): for callers
+    that must not allocate device memory, so cannot hold a plan."""
+    if N is None:
+        N, K = W.shape
+    if B is None:
+        B = x.shape[0]
+    _check(lib().dep_projection_run_static(_ptr(x), _ptr(W), _ptr(y), N, K, B, _stream(stream)),
+           "dep_projection_run_static")
 
 
 class Projection:

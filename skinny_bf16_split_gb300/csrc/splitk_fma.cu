@@ -390,3 +390,145 @@ cudaError_t selftest_timeout(int32_t limit_us, int32_t *code)
 }
 
 }  // namespace dep
+
+// ---------------------------------------------------------------------------
+// dep_projection_run_static: the split-K FMA kernel with its scratch in a fixed
+// array compiled into this library, for callers that must not allocate.
+//
+// Who cannot allocate: code that runs inside a device-memory allocator or pool
+// (allocating there would re-enter the allocator), hosts that reserve all device
+// memory up front and forbid any other allocation, and latency-critical paths
+// where cudaMalloc's implicit synchronisation is not acceptable.  Such callers
+// cannot build a plan, because a plan allocates its workspace.
+//
+// The scratch (status word, tile counters, split-K partials) lives in one
+// file-scope __device__ array of kStaticScratchBytes.  Every GPU that loads this
+// library holds it until the process exits.  Host code cannot use the array's
+// name as a device address (it is a host-side stand-in), so the first call on a
+// device looks the address up with cudaGetSymbolAddress while that device is
+// current and keeps it; that first call should therefore come before any stream
+// capture.  All calls share the array and it keeps the last call's contents:
+// each call clears the counters and the status word (they must start at zero)
+// on its stream; the partials are always written before they are read.  Calls
+// that overlap on the GPU race on the array.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace dep {
+namespace {
+
+constexpr size_t kStaticScratchBytes = 1u << 20;        // 1 MiB in total
+constexpr size_t kStaticStatusBytes = 256;              // status word (padded)
+constexpr size_t kStaticCounterBytes = 256u * 1024u;    // 65536 tile counters
+constexpr size_t kStaticPartialBytes = kStaticScratchBytes - kStaticStatusBytes - kStaticCounterBytes;
+constexpr int kStaticMaxDevices = 64;
+constexpr int64_t kStaticMaxRows = 262144;  // weight rows: 32-row tiles x 8 counters fit the counter area
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+struct StaticDevice {
+    bool ready;
+    unsigned char *scratch;  // device address of g_static_scratch on this device
+    int sm_count;
+};
+std::mutex g_static_mutex;
+StaticDevice g_static_devices[kStaticMaxDevices];
+
+// Once per device, with that device current.
+cudaError_t static_device(int dev, StaticDevice *out)
+{
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    StaticDevice &d = g_static_devices[dev];
+    if (!d.ready) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess)
+            return e;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return e;
+        d.scratch = static_cast<unsigned char *>(p);
+        d.sm_count = sms;
+        d.ready = true;
+    }
+    *out = d;
+    return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace dep
+
+extern "C" dep_status_t dep_projection_run_static(const void *x, const void *W, void *y, int64_t N,
+                                                  int64_t K, int32_t B, void *stream)
+{
+    using namespace dep;
+    if (B < 0 || N < 1 || K < 8)
+        return DEP_ERR_INVALID_ARG;
+    if (K % 8)
+        return DEP_ERR_MISALIGNED;
+    if (N > kStaticMaxRows || K > INT32_MAX)
+        return DEP_ERR_UNSUPPORTED;  // beyond the fixed scratch array's stated limit
+    if (B == 0)
+        return DEP_OK;
+    if (!x || !W || !y)
+        return DEP_ERR_INVALID_ARG;
+    const uintptr_t px = reinterpret_cast<uintptr_t>(x), pw = reinterpret_cast<uintptr_t>(W),
+                    py = reinterpret_cast<uintptr_t>(y);
+    if ((px | pw | py) & 15u)
+        return DEP_ERR_MISALIGNED;
+    const size_t xb = (size_t)B * K * 2, wb = (size_t)N * K * 2, yb = (size_t)B * N * 2;
+    if ((py < px + xb && px < py + yb) || (py < pw + wb && pw < py + yb))
+        return DEP_ERR_INVALID_ARG;
+
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kStaticMaxDevices) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    StaticDevice sd;
+    if (static_device(dev, &sd) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+
+    dep_tactic_t t{};
+    t.max_rows = B;
+    t.kind = DEP_KIND_SPLITK_FMA;
+    t.cols = B <= 1 ? 1 : B <= 2 ? 2 : B <= 4 ? 4 : 8;
+    t.tile_n = tile_rows(t.cols);
+    t.tile_k = kKT;
+    t.stages = t.cols >= 8 ? 6 : 4;
+    t.ctas = sd.sm_count;
+    const int64_t U = fma_units(t, N, K);
+    const int64_t grid = U < t.ctas ? U : t.ctas;
+    const size_t counters = fma_counters(t, N);
+    if (counters * sizeof(int) > kStaticCounterBytes ||
+        (size_t)grid * fma_ws_per_cta(t) * sizeof(float) > kStaticPartialBytes)
+        return DEP_ERR_UNSUPPORTED;  // larger than the fixed scratch array
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(sd.scratch, 0, kStaticStatusBytes + counters * sizeof(int), s) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    RunArgs a;
+    a.x = static_cast<const uint16_t *>(x);
+    a.W = static_cast<const uint16_t *>(W);
+    a.y = static_cast<uint16_t *>(y);
+    a.B = B;
+    a.N = N;
+    a.K = K;
+    a.status = reinterpret_cast<int *>(sd.scratch);
+    a.counters = reinterpret_cast<int *>(sd.scratch + kStaticStatusBytes);
+    a.n_counters = kStaticCounterBytes / sizeof(int);
+    a.ws = reinterpret_cast<float *>(sd.scratch + kStaticStatusBytes + kStaticCounterBytes);
+    a.ws_floats = kStaticPartialBytes / sizeof(float);
+    a.stream = s;
+    a.wait_limit_ns = 1000000000ull;
+    if (fma_run(t, a) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    return DEP_OK;
+}
