@@ -100,23 +100,60 @@ size_t tactic_counters(const dep_tactic_t &t, int64_t N)
     return t.kind == DEP_KIND_SPLITK_FMA ? dep::fma_counters(t, N) : dep::tc_counters(t, N);
 }
 
-// The fixed rule: warp split-K on the FMA pipe for small batches; the
-// tensor-core kernel past them (runtime.hybrid page, HybridAttention.__init__:
-// warp split-K up to 16 rows, the GEMM path past it).
-dep_tactic_t default_tactic(int32_t rows, int sm_count, bool host_only)
+constexpr int32_t kFmaMaxRows = 4;  // default split point between the two kernels
+
+dep_tactic_t fma_tactic(int32_t rows, int32_t cols, int32_t stages, int sm_count, bool host_only)
 {
     dep_tactic_t t{};
     t.max_rows = rows;
-    t.tile_k = 256;
     t.kind = DEP_KIND_SPLITK_FMA;
-    t.cols = std::min<int32_t>(8, pow2_at_least(rows));
-    t.tile_n = t.cols >= 8 ? 32 : 64;
-    t.stages = t.cols >= 8 ? 6 : 4;
+    t.tile_k = 256;
+    t.cols = cols;
+    t.tile_n = cols >= 8 ? 32 : 64;
+    t.stages = stages;
     int per_sm = host_only ? 1 : dep::fma_blocks_per_sm(t);
-    if (per_sm < 1)
-        per_sm = 1;
-    t.ctas = sm_count * per_sm;
+    t.ctas = sm_count * (per_sm < 1 ? 1 : per_sm);
     return t;
+}
+
+dep_tactic_t tc_tactic(int32_t rows, int32_t cols, int32_t stages, int32_t ctas)
+{
+    dep_tactic_t t{};
+    t.max_rows = rows;
+    t.kind = DEP_KIND_TC;
+    t.tile_n = 128;
+    t.tile_k = 64;
+    t.cols = cols;
+    t.stages = stages;
+    t.ctas = ctas;
+    return t;
+}
+
+// Deepest pipeline of the tensor-core kernel that fits in shared memory.
+int32_t tc_default_stages(int32_t cols)
+{
+    for (int32_t st : {8, 6, 4, 3, 2})
+        if (dep::tc_valid(tc_tactic(1, cols, st, 1)))
+            return st;
+    return 2;
+}
+
+// The fixed rule: warp split-K on the FMA pipe for small batches; the
+// tensor-core kernel past them (runtime.hybrid page, HybridAttention.__init__:
+// warp split-K up to 16 rows, the GEMM path past it; the split point moves to
+// where the FMA pipe stops keeping up with HBM on this GPU).  The tensor-core
+// kernel runs one block per 128-row tile when the tiles nearly fill the GPU,
+// and the even stream-K split otherwise.
+dep_tactic_t default_tactic(int32_t rows, int64_t N, int sm_count, bool host_only)
+{
+    if (rows <= kFmaMaxRows) {
+        const int32_t cols = pow2_at_least(rows);
+        return fma_tactic(rows, cols, 4, sm_count, host_only);
+    }
+    const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
+    const int64_t tiles = (N + 127) / 128;
+    const int32_t ctas = (tiles <= sm_count && 4 * tiles >= 3 * (int64_t)sm_count) ? (int32_t)tiles : sm_count;
+    return tc_tactic(rows, cols, tc_default_stages(cols), ctas);
 }
 
 void sort_table(std::vector<dep_tactic_t> &table)
@@ -136,15 +173,17 @@ const dep_tactic_t *lookup(const dep_plan_s *p, int32_t B)
 }
 
 // Allocate (or re-allocate) the plan's device block for its current table.
-dep_status_t allocate_device(dep_plan_s *p, size_t extra_ws_floats = 0)
+dep_status_t allocate_device(dep_plan_s *p, size_t extra_ws_floats = 0, size_t extra_counters = 0)
 {
-    // Room for the table's tactics, and for any tactic of the same footprint
-    // per block on up to four blocks per SM (tests and tuning use other grids).
-    size_t ws = extra_ws_floats, cnt = 256;
+    // Room for the table's tactics, for any tactic of the same per-block
+    // footprint on up to one block per SM, and for FMA-sized footprints on up to
+    // four blocks per SM (explicit tactics of tests and tuning use other grids).
+    size_t ws = std::max(extra_ws_floats, (size_t)4 * (size_t)p->sm_count * 512);
+    size_t cnt = std::max<size_t>(256, extra_counters);
     int32_t rows = 1;
     for (const auto &t : p->table) {
         ws = std::max(ws, tactic_ws_floats(t, p->N, p->K));
-        ws = std::max(ws, (size_t)4 * (size_t)p->sm_count * ws_per_cta(t));
+        ws = std::max(ws, (size_t)p->sm_count * ws_per_cta(t));
         cnt = std::max(cnt, tactic_counters(t, p->N));
         rows = std::max(rows, t.max_rows);
     }
@@ -245,7 +284,7 @@ dep_status_t make_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_b
         }
     }
     for (int32_t b : bs)
-        p->table.push_back(default_tactic(b, p->sm_count, host_only));
+        p->table.push_back(default_tactic(b, N, p->sm_count, host_only));
     sort_table(p->table);
     if (!host_only) {
         st = allocate_device(p);
@@ -309,6 +348,136 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
     return DEP_OK;
 }
 
+// ---- tuning (DEP_PLAN_TUNE) ----
+
+__global__ void fill_bf16_kernel(uint16_t *p, size_t n, uint64_t seed)
+{
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        uint64_t z = seed + 0x9E3779B97F4A7C15ull * (i + 1);
+        z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+        z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+        z ^= z >> 31;
+        // random sign and fraction, magnitude in [2^-8, 2): ordinary finite values
+        p[i] = (uint16_t)(((z >> 16) & 0x8000u) | ((119u + (uint32_t)(z % 9u)) << 7) | ((z >> 32) & 0x7Fu));
+    }
+}
+
+std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int sm_count)
+{
+    std::vector<dep_tactic_t> c;
+    if (rows <= 8) {
+        const int32_t cols = pow2_at_least(rows);
+        for (int32_t st : {3, 4, 6})
+            c.push_back(fma_tactic(rows, cols, st, sm_count, false));
+    }
+    const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
+    const int64_t tiles = (N + 127) / 128;
+    for (int32_t st : {4, 6, 8}) {
+        c.push_back(tc_tactic(rows, cols, st, sm_count));
+        if (tiles < sm_count)
+            c.push_back(tc_tactic(rows, cols, st, (int32_t)tiles));
+    }
+    std::vector<dep_tactic_t> ok;
+    for (const auto &t : c)
+        if (tactic_valid(t))
+            ok.push_back(t);
+    return ok;
+}
+
+// Time every candidate of every table entry on scratch data of the plan's shape
+// (enough distinct weight copies that no launch reads its weight from L2) and
+// keep the fastest.  Median of timed launches, CUDA events on a private stream.
+dep_status_t tune_plan(dep_plan_s *p)
+{
+    std::vector<std::vector<dep_tactic_t>> cands;
+    size_t ws_need = 0, cnt_need = 0;
+    int32_t rows_max = 1;
+    for (const auto &t : p->table) {
+        cands.push_back(candidates(t.max_rows, p->N, p->sm_count));
+        for (const auto &c : cands.back()) {
+            ws_need = std::max(ws_need, tactic_ws_floats(c, p->N, p->K));
+            cnt_need = std::max(cnt_need, tactic_counters(c, p->N));
+        }
+        rows_max = std::max(rows_max, t.max_rows);
+    }
+    dep_status_t st = allocate_device(p, ws_need, cnt_need);
+    if (st != DEP_OK)
+        return st;
+    int l2 = 0;
+    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, p->device);
+    const size_t wbytes = (size_t)p->N * p->K * 2;
+    size_t copies = std::max<size_t>(2, (2 * (size_t)l2 + wbytes - 1) / wbytes);
+    copies = std::min<size_t>(copies, 64);
+    const size_t xbytes = (size_t)rows_max * p->K * 2, ybytes = (size_t)rows_max * p->N * 2;
+    char *scratch = nullptr;
+    if (cudaMalloc(&scratch, copies * wbytes + xbytes + ybytes + 512) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_OOM;
+    }
+    uint16_t *Wc = reinterpret_cast<uint16_t *>(scratch);
+    uint16_t *xs = reinterpret_cast<uint16_t *>(scratch + ((copies * wbytes + 255) & ~(size_t)255));
+    uint16_t *ys = reinterpret_cast<uint16_t *>(reinterpret_cast<char *>(xs) + ((xbytes + 255) & ~(size_t)255));
+    cudaStream_t s = nullptr;
+    cudaEvent_t e0 = nullptr, e1 = nullptr;
+    bool ok = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreate(&e0) == cudaSuccess && cudaEventCreate(&e1) == cudaSuccess;
+    if (ok) {
+        fill_bf16_kernel<<<1024, 256, 0, s>>>(Wc, copies * wbytes / 2, 12345);
+        fill_bf16_kernel<<<64, 256, 0, s>>>(xs, xbytes / 2, 777);
+        ok = cudaGetLastError() == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess;
+    }
+    for (size_t i = 0; ok && i < p->table.size(); ++i) {
+        const int32_t B = p->table[i].max_rows;
+        float best = 1e30f;
+        dep_tactic_t best_t = p->table[i];
+        size_t turn = 0;
+        for (const auto &c : cands[i]) {
+            std::vector<float> ms;
+            for (int rep = 0; rep < 12 && ok; ++rep) {
+                const uint16_t *W = Wc + (turn++ % copies) * (wbytes / 2);
+                ok = cudaEventRecord(e0, s) == cudaSuccess &&
+                     run_impl(p, &c, xs, W, ys, B, s) == DEP_OK && cudaEventRecord(e1, s) == cudaSuccess &&
+                     cudaEventSynchronize(e1) == cudaSuccess;
+                float t = 0;
+                if (ok && rep >= 2 && cudaEventElapsedTime(&t, e0, e1) == cudaSuccess)
+                    ms.push_back(t);
+            }
+            if (!ok || ms.empty())
+                break;
+            std::sort(ms.begin(), ms.end());
+            const float med = ms[ms.size() / 2];
+            if (p->log)
+                std::fprintf(stderr, "[dep] tune N=%lld K=%lld B=%d kind=%d cols=%d stages=%d ctas=%d: %.2f us\n",
+                             (long long)p->N, (long long)p->K, B, c.kind, c.cols, c.stages, c.ctas, med * 1e3f);
+            if (med < best) {
+                best = med;
+                best_t = c;
+            }
+        }
+        best_t.max_rows = B;
+        p->table[i] = best_t;
+    }
+    if (e0)
+        cudaEventDestroy(e0);
+    if (e1)
+        cudaEventDestroy(e1);
+    if (s) {
+        cudaStreamSynchronize(s);
+        cudaStreamDestroy(s);
+    }
+    cudaFree(scratch);
+    if (!ok) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    int32_t code = 0;
+    if (cudaMemcpy(&code, p->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    return code ? DEP_ERR_TIMEOUT : DEP_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -338,7 +507,12 @@ dep_status_t dep_projection_plan(int64_t N, int64_t K, const int32_t *batches, i
     dep_status_t st = make_plan(N, K, batches, n_batches, false, 0, out);
     if (st != DEP_OK || !(flags & DEP_PLAN_TUNE))
         return st;
-    return DEP_OK;  // tuning is added with the tuner
+    st = tune_plan(*out);
+    if (st != DEP_OK) {
+        dep_projection_plan_destroy(*out);
+        *out = nullptr;
+    }
+    return st;
 }
 
 dep_status_t dep_projection_plan_host(int64_t N, int64_t K, const int32_t *batches,

@@ -212,11 +212,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             continue;  // another block finishes this tile
         __threadfence();
         if (have) {
+            // Sum the segments in increasing block order; up to 4 loads in flight.
             float sum = 0.0f;
-            for (int64_t cc = c0; cc <= c1; ++cc) {
-                const int sl = (t == sk_begin(cc, U, C) / KTILES) ? 0 : 1;
-                const float p = __ldcg(&ws[((cc * 2 + sl) * BC + mb) * TN + row]);
-                sum = (cc == c0) ? p : sum + p;
+            for (int64_t g0 = c0; g0 <= c1; g0 += 4) {
+                float p[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int64_t cc = g0 + i;
+                    const int sl = (t == sk_begin(cc, U, C) / KTILES) ? 0 : 1;
+                    p[i] = cc <= c1 ? __ldcg(&ws[((cc * 2 + sl) * BC + mb) * TN + row]) : 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (g0 + i <= c1)
+                        sum = (g0 + i == c0) ? p[i] : sum + p[i];
             }
             if (mb < B && n < N)
                 y[(int64_t)mb * N + n] = to_bf16(sum);

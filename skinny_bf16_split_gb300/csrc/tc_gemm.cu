@@ -1,11 +1,421 @@
-// tc_gemm.cu -- tcgen05 tensor-core tactic (not yet implemented: rejected as invalid).
+// tc_gemm.cu -- tcgen05 tensor-core tactic for the decode projection.
+//
+// Computes y[B,N] = BF16(x[B,K] . W[N,K]^T), BF16 products accumulated in FP32,
+// for the batches where the FMA pipe would be the bottleneck (runtime.hybrid
+// page, HybridAttention.__init__: past the split-K rows the projection runs the
+// stock FP32-accumulated BF16 GEMM; runtime.dep page, DepProjection).
+//
+// Design (sm_103a, one CTA per SM, no clusters, no multicast):
+//  * Swap-AB: the MMA's M side is 128 weight rows, its N side the batch padded
+//    to NT (16..256), so one weight tile feeds one MMA and a tiny batch wastes
+//    only tensor throughput, never weight bytes.  D[128 x NT] lives in TMEM.
+//  * Work units are (128-row tile, 64-column k-tile) pairs; the persistent
+//    blocks take equal contiguous ranges (stream-K), exactly as the FMA tactic.
+//  * Warp 0: TMA producer.  Weight tile [128 x 64] and activation tile [NT x 64]
+//    land in a shared-memory ring in the 128-byte swizzle layout.
+//  * Warp 1: allocates TMEM (two accumulators of NT columns), one thread issues
+//    tcgen05.mma (4 per stage, K = 16 each) and releases each stage with
+//    tcgen05.commit; at the end of a segment it commits the accumulator.
+//  * Warps 2-5: epilogue.  Each owns the 32 TMEM lanes (= weight rows) of its
+//    quadrant, reads its accumulator with tcgen05.ld, frees it for the MMA of
+//    the next-but-one segment, and either stores BF16 y (segment = whole tile)
+//    or writes FP32 partials for the split-K fix-up: the last warp to arrive on
+//    the tile's counter adds the partials in increasing block order.  No float
+//    atomics and no inter-block waits: results are identical from run to run.
+//  * Every wait is bounded in time; on a give-up the block records a code,
+//    lets every role finish, waits for its MMAs and copies, and frees TMEM.
+#include <cuda_bf16.h>
+
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dep {
-bool tc_valid(const dep_tactic_t &) { return false; }
-int64_t tc_units(const dep_tactic_t &, int64_t, int64_t) { return 1; }
-size_t tc_ws_per_cta(const dep_tactic_t &) { return 0; }
-size_t tc_counters(const dep_tactic_t &, int64_t) { return 0; }
-int tc_blocks_per_sm(const dep_tactic_t &) { return 0; }
-cudaError_t tc_run(const dep_tactic_t &, const RunArgs &) { return cudaErrorNotSupported; }
+namespace {
+
+constexpr int kBM = 128;          // weight rows per tile (MMA M)
+constexpr int kBK = 64;           // columns per stage: one 128-byte swizzle row
+constexpr int kUmmaK = 16;        // K of one kind::f16 MMA
+constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA/TMEM, warps 2-5 epilogue
+constexpr int kEpiWarps = 4;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB weight tile per stage
+
+template <int NT>
+struct TcShape {
+    static constexpr int B_BYTES = NT * kBK * 2;
+    static constexpr int STAGE = kABytes + B_BYTES;  // a multiple of 1024
+    static constexpr uint32_t TMEM_COLS = 2 * NT < 32 ? 32 : 2 * NT;
+};
+
+__device__ __forceinline__ uint16_t to_bf16(float v)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                   uint16_t *__restrict__ y, int B, int N, int K, int stages, float *__restrict__ ws,
+                   int *__restrict__ counters, int *__restrict__ status, uint64_t limit_ns)
+{
+    using S = TcShape<NT>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles need 1 KB alignment
+    uint8_t *smem = smem_raw + (base - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * S::STAGE);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8 * stages;
+    const uint32_t accf0 = empty0 + 8 * stages;  // accumulator ready, 2 buffers
+    const uint32_t acce0 = accf0 + 16;           // accumulator drained, 2 buffers
+    const uint32_t done = acce0 + 16;            // all MMAs complete
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 5);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int64_t T = (N + kBM - 1) / kBM, KTILES = (K + kBK - 1) / kBK, U = T * KTILES;
+    const int64_t C = gridDim.x, c = blockIdx.x;
+    const int64_t u_begin = sk_begin(c, U, C), u_end = sk_begin(c + 1, U, C);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, kEpiWarps);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tc::alloc(smem_u32(tmem_slot), S::TMEM_COLS);
+        tc::relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            prefetch_tmap(&tmX);
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            int s = 0;
+            uint32_t ph = 0;
+            int64_t issued = 0;
+            for (int64_t u = u_begin; u < u_end; ++u) {
+                if (*abort_flag)
+                    break;
+                if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, limit_ns)) {
+                    record_status(status, DEP_DEV_TIMEOUT_PRODUCER);
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint32_t a = base + (uint32_t)(s * S::STAGE);
+                mbar_arrive_expect_tx(full0 + 8 * s, S::STAGE);
+                const int t = (int)(u / KTILES), kt = (int)(u % KTILES);
+                tma_load_2d(a, &tmW, kt * kBK, t * kBM, full0 + 8 * s, pol_w);
+                tma_load_2d(a + kABytes, &tmX, kt * kBK, 0, full0 + 8 * s, pol_x);
+                ++issued;
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            const int64_t n = issued < stages ? issued : stages;  // drain copies in flight
+            int ds = s;
+            uint32_t dph = ph;
+            for (int64_t i = 0; i < n; ++i) {
+                if (--ds < 0) {
+                    ds = stages - 1;
+                    dph ^= 1u;
+                }
+                if (!mbar_wait(full0 + 8 * ds, dph, limit_ns))
+                    record_status(status, DEP_DEV_TIMEOUT_PRODUCER);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, NT);
+            int s = 0;
+            uint32_t ph = 0, acce_ph = 0;
+            int buf = 0;
+            int64_t u = u_begin;
+            bool ok = true;
+            while (u < u_end && ok) {
+                const int64_t t = u / KTILES;
+                const int64_t seg_end = u_end < (t + 1) * KTILES ? u_end : (t + 1) * KTILES;
+                if (!mbar_wait(acce0 + 8 * buf, ((acce_ph >> buf) & 1u) ^ 1u, limit_ns)) {
+                    record_status(status, DEP_DEV_TIMEOUT_MMA);
+                    *abort_flag = 1;
+                    break;
+                }
+                acce_ph ^= 1u << buf;
+                tc::fence_after();
+                const uint32_t d = tmem + (uint32_t)(buf * NT);
+                uint32_t accumulate = 0;
+                for (; u < seg_end; ++u) {
+                    if (*abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    if (!mbar_wait(full0 + 8 * s, ph, limit_ns)) {
+                        record_status(status, DEP_DEV_TIMEOUT_MMA);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint32_t a = base + (uint32_t)(s * S::STAGE);
+                    const uint64_t ad = tc::desc_sw128(a), bd = tc::desc_sw128(a + kABytes);
+#pragma unroll
+                    for (int j = 0; j < kBK / kUmmaK; ++j) {
+                        // advance along K inside the 128-byte swizzle row: 32 bytes per step
+                        const uint64_t off = (uint64_t)((j * kUmmaK * 2) >> 4);
+                        tc::mma_bf16(d, ad + off, bd + off, idesc, accumulate);
+                        accumulate = 1;
+                    }
+                    tc::commit(empty0 + 8 * s);  // the stage is free once these MMAs finish
+                    if (++s == stages) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!ok)
+                    break;
+                tc::commit(accf0 + 8 * buf);  // the accumulator is final
+                buf ^= 1;
+            }
+            tc::commit(done);  // TMEM is freed at the end: wait for every MMA
+            if (!mbar_wait(done, 0, limit_ns))
+                record_status(status, DEP_DEV_TIMEOUT_MMA);
+        }
+    } else {
+        // ---------------- epilogue warps ----------------
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int row = 32 * q + lane;
+        const int64_t first_t = u_begin / KTILES;
+        uint32_t accf_ph = 0;
+        int buf = 0;
+        int64_t u = u_begin;
+        while (u < u_end) {
+            const int64_t t = u / KTILES;
+            const int64_t seg_end = u_end < (t + 1) * KTILES ? u_end : (t + 1) * KTILES;
+            const bool whole = (u == t * KTILES) && (seg_end == (t + 1) * KTILES);
+            u = seg_end;
+            if (!mbar_wait(accf0 + 8 * buf, (accf_ph >> buf) & 1u, limit_ns)) {
+                record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
+                *abort_flag = 1;
+                break;
+            }
+            accf_ph ^= 1u << buf;
+            tc::fence_after();
+            const int64_t n = t * kBM + row;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NT);
+            const int slot = (t == first_t) ? 0 : 1;
+            float *part = ws + ((c * 2 + slot) * NT) * kBM + row;
+#pragma unroll 1
+            for (int c0 = 0; c0 < NT; c0 += 16) {
+                uint32_t v[16];
+                tc::ld16(taddr + (uint32_t)c0, v);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int b = c0 + j;
+                    if (b < B) {
+                        const float f = __uint_as_float(v[j]);
+                        if (whole) {
+                            if (n < N)
+                                y[(int64_t)b * N + n] = to_bf16(f);
+                        } else {
+                            __stcg(part + (int64_t)b * kBM, f);
+                        }
+                    }
+                }
+            }
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acce0 + 8 * buf);
+            buf ^= 1;
+            if (whole)
+                continue;
+            __threadfence();
+            __syncwarp();
+            int prev = 0;
+            if (lane == 0)
+                prev = atomicAdd(&counters[t * kEpiWarps + q], 1);
+            prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+            const int64_t c_first = sk_owner(t * KTILES, U, C);
+            const int64_t c_last = sk_owner(t * KTILES + KTILES - 1, U, C);
+            if (prev != (int)(c_last - c_first))
+                continue;  // another block finishes this tile
+            __threadfence();
+            if (n < N) {
+                // Sum the segments in increasing block order.  The loads of up to
+                // 4 segments x 8 batch columns are issued together, then added.
+                for (int b0 = 0; b0 < B; b0 += 8) {
+                    float sum[8];
+                    for (int64_t g0 = c_first; g0 <= c_last; g0 += 4) {
+                        float p[4][8];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int64_t cc = g0 + i;
+                            const int sl = (t == sk_begin(cc, U, C) / KTILES) ? 0 : 1;
+                            const float *src = ws + ((cc * 2 + sl) * NT + b0) * kBM + row;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                p[i][j] = (cc <= c_last && b0 + j < B) ? __ldcg(src + (int64_t)j * kBM) : 0.0f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (g0 + i <= c_last)
+                                    sum[j] = (g0 + i == c_first) ? p[i][j] : sum[j] + p[i][j];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if (b0 + j < B)
+                            y[(int64_t)(b0 + j) * N + n] = to_bf16(sum[j]);
+                }
+            }
+            if (lane == 0)
+                counters[t * kEpiWarps + q] = 0;  // ready for the next launch
+        }
+    }
+
+    __syncwarp();
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after();
+        tc::dealloc(tmem, S::TMEM_COLS);
+    }
+}
+
+constexpr size_t kMaxSmem = 227 * 1024;
+
+template <int NT>
+size_t smem_bytes(int stages)
+{
+    return 1024 + (size_t)stages * TcShape<NT>::STAGE + (size_t)(2 * stages + 5) * 8 + 16;
+}
+
+template <int NT>
+cudaError_t prepare()
+{
+    static cudaError_t once = cudaFuncSetAttribute(
+        tc_gemm_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+    return once;
+}
+
+template <int NT>
+cudaError_t run_nt(const dep_tactic_t &t, const RunArgs &a)
+{
+    cudaError_t e = prepare<NT>();
+    if (e != cudaSuccess)
+        return e;
+    CUtensorMap tmW, tmX;
+    if (encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, kBM,
+                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int64_t T = (a.N + kBM - 1) / kBM, KT = (a.K + kBK - 1) / kBK, U = T * KT;
+    const int grid = (int)(U < t.ctas ? U : t.ctas);
+    const size_t smem = smem_bytes<NT>(t.stages);
+    for (int32_t r0 = 0; r0 < a.B; r0 += NT) {
+        const int32_t rows = a.B - r0 < NT ? a.B - r0 : NT;
+        if (encode_bf16_2d(&tmX, a.x + (size_t)r0 * a.K, (uint64_t)a.K, (uint64_t)rows, kBK, NT,
+                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        tc_gemm_kernel<NT><<<grid, kThreads, smem, a.stream>>>(tmW, tmX, a.y + (size_t)r0 * a.N, rows,
+                                                                (int)a.N, (int)a.K, t.stages, a.ws,
+                                                                a.counters, a.status, a.wait_limit_ns);
+        e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+template <int NT>
+int blocks_per_sm(int stages)
+{
+    if (prepare<NT>() != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_gemm_kernel<NT>, kThreads,
+                                                      smem_bytes<NT>(stages)) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+size_t smem_for(const dep_tactic_t &t)
+{
+    switch (t.cols) {
+    case 16: return smem_bytes<16>(t.stages);
+    case 32: return smem_bytes<32>(t.stages);
+    case 64: return smem_bytes<64>(t.stages);
+    case 128: return smem_bytes<128>(t.stages);
+    case 256: return smem_bytes<256>(t.stages);
+    default: return 0;
+    }
+}
+
+}  // namespace
+
+bool tc_valid(const dep_tactic_t &t)
+{
+    if (t.kind != DEP_KIND_TC || t.ctas < 1 || t.tile_n != kBM || t.tile_k != kBK)
+        return false;
+    if (t.stages < 2 || t.stages > 16)
+        return false;
+    const size_t smem = smem_for(t);
+    return smem != 0 && smem <= kMaxSmem;
+}
+
+int64_t tc_units(const dep_tactic_t &, int64_t N, int64_t K)
+{
+    return ((N + kBM - 1) / kBM) * ((K + kBK - 1) / kBK);
+}
+
+size_t tc_ws_per_cta(const dep_tactic_t &t)
+{
+    return 2 * (size_t)t.cols * kBM;  // head and tail segment partials
+}
+
+size_t tc_counters(const dep_tactic_t &, int64_t N)
+{
+    return (size_t)((N + kBM - 1) / kBM) * kEpiWarps;
+}
+
+int tc_blocks_per_sm(const dep_tactic_t &t)
+{
+    switch (t.cols) {
+    case 16: return blocks_per_sm<16>(t.stages);
+    case 32: return blocks_per_sm<32>(t.stages);
+    case 64: return blocks_per_sm<64>(t.stages);
+    case 128: return blocks_per_sm<128>(t.stages);
+    case 256: return blocks_per_sm<256>(t.stages);
+    default: return 0;
+    }
+}
+
+cudaError_t tc_run(const dep_tactic_t &t, const RunArgs &a)
+{
+    switch (t.cols) {
+    case 16: return run_nt<16>(t, a);
+    case 32: return run_nt<32>(t, a);
+    case 64: return run_nt<64>(t, a);
+    case 128: return run_nt<128>(t, a);
+    case 256: return run_nt<256>(t, a);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace dep

@@ -284,3 +284,108 @@ def test_stock_gemm_within_tolerance_of_oracle(orc):
     y = to_host(torch.mm(to_dev(x), to_dev(W).t()))
     ok, worst, idx = within_tolerance(y, orc.linear(x, W))
     assert ok, (worst, idx)
+
+
+# ---------------- tensor-core (tcgen05) tactic ----------------
+
+def tc_tactic(dep, NT, ctas, stages=4):
+    return dep.dep_tactic_t(max_rows=NT, kind=dep.DEP_KIND_TC, ctas=ctas, tile_n=128, tile_k=64,
+                            stages=stages, cols=NT)
+
+
+SMS = None
+
+
+def sm_count():
+    global SMS
+    if SMS is None:
+        SMS = torch.cuda.get_device_properties(0).multi_processor_count
+    return SMS
+
+
+@pytest.mark.parametrize("N,K", [(128, 64), (333, 1000), (97, 264), (1000, 3000)])
+@pytest.mark.parametrize("NT", [16, 32, 64, 128, 256])
+def test_tc_parity_vs_oracle(dep, orc, plan_cache, N, K, NT):
+    """tcgen05 kernel, every MMA width, partial and full batches, stream-K grids
+    of 1, 7 and all SMs (split tiles, ragged N and K tails)."""
+    plan = get_plan(dep, plan_cache, N, K, (256,))
+    W = synth.normal_bf16(N + NT, 1, (N, K), sigma=0.02)
+    for B in sorted({1, min(NT, 5), NT}):
+        x = synth.normal_bf16(B + NT, 2, (B, K))
+        ref = orc.linear(x, W)
+        for ctas in (1, 7, sm_count()):
+            y = run(dep, plan, x, W, N, tc_tactic(dep, NT, ctas, 4 if NT < 256 else 3))
+            ok, worst, idx = within_tolerance(y, ref)
+            assert ok, (B, ctas, worst, idx)
+    assert dep.dep_projection_device_status(plan) == 0
+
+
+@pytest.mark.parametrize("B", [5, 16, 64])
+def test_tc_determinism_and_graph_replay(dep, plan_cache, B):
+    """The tensor-core kernel's split-K fix-up is order-fixed: repeated runs and
+    CUDA-graph replays give identical bits."""
+    N, K = 7168, 4096
+    x, W = to_dev(synth.normal_bf16(B, 2, (B, K))), to_dev(synth.normal_bf16(5, 1, (N, K), 0.02))
+    plan = get_plan(dep, plan_cache, N, K)
+    assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC
+    ref = empty_out(B, N)
+    dep.dep_projection_run(plan, x, W, ref, B)
+    torch.cuda.synchronize()
+    for _ in range(10):
+        y = empty_out(B, N)
+        dep.dep_projection_run(plan, x, W, y, B)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+    y = empty_out(B, N)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dep.dep_projection_run(plan, x, W, y, B, s)
+    for _ in range(3):
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+
+
+def test_tc_small_integers_exact(dep, orc, plan_cache):
+    """Small-integer inputs give exact FP32 sums: the tensor-core path must equal
+    the exact oracle bit for bit."""
+    rng = np.random.default_rng(9)
+    B, N, K = 24, 300, 2048
+    xi, wi = rng.integers(-8, 9, (B, K)), rng.integers(-8, 9, (N, K))
+    x = np.vectorize(exact_bf16)(xi).astype(np.uint16)
+    W = np.vectorize(exact_bf16)(wi).astype(np.uint16)
+    plan = get_plan(dep, plan_cache, N, K)
+    assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC
+    np.testing.assert_array_equal(run(dep, plan, x, W, N), orc.linear(x, W))
+
+
+def test_tc_negation_symmetric(dep, plan_cache):
+    """Negating x negates every product, and every FP32 step of the fix-up is
+    sign-symmetric: y(-x) = -y(x) bit for bit on the tensor-core path too."""
+    N, K, B = 500, 4096, 16
+    x = synth.normal_bf16(13, 2, (B, K))
+    W = synth.normal_bf16(13, 1, (N, K), sigma=0.02)
+    plan = get_plan(dep, plan_cache, N, K)
+    y = run(dep, plan, x, W, N)
+    yn = run(dep, plan, x ^ np.uint16(0x8000), W, N)
+    nz = synth.bf16_to_f32(y) != 0
+    np.testing.assert_array_equal(yn[nz], y[nz] ^ np.uint16(0x8000))
+
+
+def test_tuned_plan_is_valid_and_correct(dep, orc):
+    """DEP_PLAN_TUNE measures candidates and keeps one per batch; the result is
+    a valid table whose runs match the oracle."""
+    N, K = 1000, 2048
+    plan = dep.dep_projection_plan(N, K, [1, 8, 32], dep.DEP_PLAN_TUNE)
+    try:
+        table = dep.dep_projection_plan_table(plan)
+        assert [t.max_rows for t in table] == [1, 8, 32]
+        for B in (1, 8, 32):
+            x = synth.normal_bf16(B, 2, (B, K))
+            W = synth.normal_bf16(3, 1, (N, K), sigma=0.02)
+            ok, worst, idx = within_tolerance(run(dep, plan, x, W, N), orc.linear(x, W))
+            assert ok, (B, worst, idx)
+    finally:
+        dep.dep_projection_plan_destroy(plan)
