@@ -60,6 +60,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--plan", default="default", choices=("default", "tune"))
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay (programmatic dependent launch) measurement")
+    ap.add_argument("--report", action="store_true",
+                    help="measure every workload; one JSON line each (per-config report)")
     return ap.parse_args()
 
 
@@ -371,6 +375,9 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, dep, calls, plans, xs_host, W_dev, device, world)
+    graph = None
+    if not args.no_graph:
+        graph = run_graph_pdl(args, dep, calls, x_dev, W_dev, y_dev, device, world, flags)
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -385,6 +392,7 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(args.workload, calls),
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "graph_pdl": graph,
             "gpu_launches": launches_per_step * args.steps, "per_call": per_call,
             "plan": args.plan, "kernel_sources": source_hash(),
             "device": torch.cuda.get_device_name(device),
@@ -393,6 +401,62 @@ def run_ours(args):
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def run_graph_pdl(args, dep, calls, x_dev, W_dev, y_dev, device, world, flags):
+    """One step captured as a CUDA graph on plans with programmatic dependent
+    launch (each kernel streams its first weight tiles while the previous one
+    finishes), replayed K times; events around all replays."""
+    import torch
+    keys = {}
+    for c in calls:
+        keys.setdefault((c.N, c.K), set()).add(c.B)
+    plans = {k: dep.dep_projection_plan(k[0], k[1], sorted(v), flags | dep.DEP_PLAN_PDL)
+             for k, v in keys.items()}
+    lib = dep.lib()
+    stream = torch.cuda.Stream()
+    run_args = [(plans[(c.N, c.K)], x_dev[i].data_ptr(), W_dev[c.weight_key].data_ptr(),
+                 y_dev[i].data_ptr(), c.B) for i, c in enumerate(calls)]
+
+    def step(sptr):
+        for p, x, W, y, B in run_args:
+            st = lib.dep_projection_run(p, x, W, y, B, sptr)
+            if st:
+                raise dep.DepError(st, "dep_projection_run")
+
+    with torch.cuda.stream(stream):
+        step(stream.cuda_stream)  # eager warm-up (kernel attributes, descriptors)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(stream.cuda_stream)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    cur = torch.cuda.current_stream()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(cur)
+    for _ in range(args.steps):
+        graph.replay()
+    t1.record(cur)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    for p in plans.values():
+        code = dep.dep_projection_device_status(p)
+        if code:
+            raise RuntimeError(f"a kernel reported device status {code}")
+        dep.dep_projection_plan_destroy(p)
+    bytes_per_step = sum(c.algorithmic_bytes for c in calls)
+    return {"value": bytes_per_step * args.steps * world / (ms * 1e-3) / 1e9, "unit": UNIT,
+            "ms_per_step": ms / args.steps,
+            "how": "one step captured as a CUDA graph, kernels chained by programmatic dependent "
+                   "launch (DEP_PLAN_PDL), K replays timed by events"}
 
 
 def run_e2e(args, dep, calls, plans, xs_host, W_dev, device, world):
@@ -442,6 +506,11 @@ def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.report:
+        for name in synth.WORKLOADS:
+            args.workload = name
+            run_ours(args)
+        return 0
     return run_ours(args)
 
 

@@ -82,12 +82,19 @@ typedef struct {
 /* Plan flags. */
 #define DEP_PLAN_DEFAULT 0u /* fixed rule: FMA split-K for small batches, TC past them */
 #define DEP_PLAN_TUNE 1u    /* time candidate tactics per batch on scratch data; keep the fastest */
+/* Programmatic dependent launch: each run may start while the preceding kernel
+ * in its stream finishes, streaming its first weight tiles early and waiting for
+ * that kernel before it reads x or writes y.  The caller promises that no work
+ * enqueued before a run on the same stream writes W (decode weights are
+ * read-only).  Consecutive runs then overlap one kernel's tail with the next
+ * one's ramp-up, also inside CUDA graphs. */
+#define DEP_PLAN_PDL 2u
 
 /*
  * Build a plan for weights of shape [N,K] on the current CUDA device.
  *   batches/n_batches: the batch sizes the caller will run (the table's keys);
  *                      n_batches == 0 takes 1,2,4,8,16,32,64,128,256.
- *   flags:             DEP_PLAN_DEFAULT or DEP_PLAN_TUNE.
+ *   flags:             DEP_PLAN_DEFAULT, or DEP_PLAN_TUNE and/or DEP_PLAN_PDL.
  * Allocates the plan's workspace, counters and status word on the device.
  * Errors: INVALID_ARG (N < 1, K < 8, batch < 1, null out), MISALIGNED (K % 8),
  * OOM, CUDA.  On error *out is set to NULL.

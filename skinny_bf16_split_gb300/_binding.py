@@ -29,6 +29,7 @@ DEP_KIND_SPLITK_FMA = 1
 DEP_KIND_TC = 2
 DEP_PLAN_DEFAULT = 0
 DEP_PLAN_TUNE = 1
+DEP_PLAN_PDL = 2
 
 DEP_DEV_TIMEOUT_PRODUCER = 1
 DEP_DEV_TIMEOUT_CONSUMER = 2

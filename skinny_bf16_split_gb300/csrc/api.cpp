@@ -38,6 +38,7 @@ struct dep_plan_s {
     uint64_t wait_limit_ns = 1000000000ull;  // 1 s per wait
     bool fault_launch = false;
     bool log = false;
+    bool pdl = false;  // DEP_PLAN_PDL
 };
 
 namespace {
@@ -340,6 +341,7 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
     a.status = p->status;
     a.stream = static_cast<cudaStream_t>(stream);
     a.wait_limit_ns = p->wait_limit_ns;
+    a.pdl = p->pdl;
     cudaError_t e = t->kind == DEP_KIND_SPLITK_FMA ? dep::fma_run(*t, a) : dep::tc_run(*t, a);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -499,13 +501,16 @@ int32_t dep_bins_index(const int32_t *keys, int32_t n_keys, int32_t B)
 dep_status_t dep_projection_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_batches,
                                  uint32_t flags, dep_plan_t *out)
 {
-    if (flags & ~(DEP_PLAN_DEFAULT | DEP_PLAN_TUNE)) {
+    if (flags & ~(DEP_PLAN_DEFAULT | DEP_PLAN_TUNE | DEP_PLAN_PDL)) {
         if (out)
             *out = nullptr;
         return DEP_ERR_INVALID_ARG;
     }
     dep_status_t st = make_plan(N, K, batches, n_batches, false, 0, out);
-    if (st != DEP_OK || !(flags & DEP_PLAN_TUNE))
+    if (st != DEP_OK)
+        return st;
+    (*out)->pdl = (flags & DEP_PLAN_PDL) != 0;
+    if (!(flags & DEP_PLAN_TUNE))
         return st;
     st = tune_plan(*out);
     if (st != DEP_OK) {

@@ -24,7 +24,29 @@ struct RunArgs {
     int *status;        // device status word (0 = fine)
     cudaStream_t stream;
     uint64_t wait_limit_ns;
+    // Programmatic dependent launch: the kernel may start while the preceding
+    // grid in the stream finishes; it streams its first weight stages before
+    // waiting for that grid (the weight must not be written by preceding work).
+    bool pdl = false;
 };
+
+// Launch with the programmatic-stream-serialisation attribute when `pdl` is set.
+template <typename Kernel, typename... Args>
+cudaError_t launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                   Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 // Stream-K split: U work units over C blocks, block c owns [begin(c), begin(c+1)).
 __host__ __device__ inline int64_t sk_begin(int64_t c, int64_t U, int64_t C)

@@ -99,6 +99,20 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     return p;
 }
 
+// ---- programmatic dependent launch ----
+// Let the next grid in the stream be scheduled once every block of this grid has
+// issued this (no-op when the launch did not allow it).
+__device__ __forceinline__ void griddep_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the preceding grid in the stream has completed and its memory is
+// visible (returns at once when there is no programmatic dependency).
+__device__ __forceinline__ void griddep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Record the first nonzero code in the device status word.
 __device__ __forceinline__ void record_status(int *status, int code)
 {

@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(empty0 + 8 * s, kWarps);
         }
         fence_mbar_init();
+        griddep_launch_dependents();
     }
     __syncthreads();
 
@@ -90,10 +91,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmX);
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-            int s = 0;
-            uint32_t ph = 0;
-            int64_t issued = 0;
-            for (int64_t u = u_begin; u < u_end; ++u) {
+            // The weight is not written by preceding work: fill the ring with its
+            // first tiles, then wait for the preceding grid before reading x.
+            const int64_t pre = (u_end - u_begin) < stages ? (u_end - u_begin) : stages;
+            for (int64_t i = 0; i < pre; ++i) {
+                const int64_t u = u_begin + i;
+                mbar_arrive_expect_tx(full0 + 8 * (int)i, STAGE_BYTES);
+                tma_load_2d(smem_u32(smem + (size_t)i * STAGE_BYTES), &tmW, (int)(u % KTILES) * kKT,
+                            (int)(u / KTILES) * TN, full0 + 8 * (int)i, pol_w);
+            }
+            griddep_wait();
+            for (int64_t i = 0; i < pre; ++i) {
+                const int64_t u = u_begin + i;
+                tma_load_2d(smem_u32(smem + (size_t)i * STAGE_BYTES) + TN * kRowBytes, &tmX,
+                            (int)(u % KTILES) * kKT, 0, full0 + 8 * (int)i, pol_x);
+            }
+            int s = (int)(pre % stages);
+            uint32_t ph = pre == stages ? 1u : 0u;
+            int64_t issued = pre;
+            for (int64_t u = u_begin + pre; u < u_end; ++u) {
                 if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, limit_ns)) {
                     record_status(status, DEP_DEV_TIMEOUT_PRODUCER);
                     break;
@@ -127,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ---------------- compute warps ----------------
+    griddep_wait();  // workspace, counters and y may still be in use by the preceding grid
     float acc[R][BC];
     int s = 0;
     uint32_t ph = 0;
@@ -283,10 +300,9 @@ cudaError_t run_bc(const dep_tactic_t &t, const RunArgs &a)
         if (encode_bf16_2d(&tmX, a.x + (size_t)r0 * a.K, (uint64_t)a.K, (uint64_t)rows, kKT, BC,
                            CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        splitk_fma_kernel<BC><<<grid, kThreads, smem, a.stream>>>(
-            tmW, tmX, a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, a.ws, a.counters,
-            a.status, a.wait_limit_ns);
-        e = cudaGetLastError();
+        e = launch(splitk_fma_kernel<BC>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
+                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, a.ws, a.counters, a.status,
+                   a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }

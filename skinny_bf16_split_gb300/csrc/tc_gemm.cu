@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(done, 1);
         *abort_flag = 0;
         fence_mbar_init();
+        griddep_launch_dependents();
     }
     if (warp == 1) {
         tc::alloc(smem_u32(tmem_slot), S::TMEM_COLS);
@@ -104,10 +105,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmW);
             prefetch_tmap(&tmX);
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-            int s = 0;
-            uint32_t ph = 0;
-            int64_t issued = 0;
-            for (int64_t u = u_begin; u < u_end; ++u) {
+            // The weight is not written by preceding work: fill the ring with its
+            // first tiles, then wait for the preceding grid before reading x.
+            const int64_t pre = (u_end - u_begin) < stages ? (u_end - u_begin) : stages;
+            for (int64_t i = 0; i < pre; ++i) {
+                const int64_t u = u_begin + i;
+                mbar_arrive_expect_tx(full0 + 8 * (int)i, S::STAGE);
+                tma_load_2d(base + (uint32_t)(i * S::STAGE), &tmW, (int)(u % KTILES) * kBK,
+                            (int)(u / KTILES) * kBM, full0 + 8 * (int)i, pol_w);
+            }
+            griddep_wait();
+            for (int64_t i = 0; i < pre; ++i) {
+                const int64_t u = u_begin + i;
+                tma_load_2d(base + (uint32_t)(i * S::STAGE) + kABytes, &tmX, (int)(u % KTILES) * kBK, 0,
+                            full0 + 8 * (int)i, pol_x);
+            }
+            int s = (int)(pre % stages);
+            uint32_t ph = pre == stages ? 1u : 0u;
+            int64_t issued = pre;
+            for (int64_t u = u_begin + pre; u < u_end; ++u) {
                 if (*abort_flag)
                     break;
                 if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, limit_ns)) {
@@ -197,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue warps ----------------
+        griddep_wait();  // workspace, counters and y may still be in use by the preceding grid
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const int row = 32 * q + lane;
         const int64_t first_t = u_begin / KTILES;
@@ -333,10 +350,9 @@ cudaError_t run_nt(const dep_tactic_t &t, const RunArgs &a)
         if (encode_bf16_2d(&tmX, a.x + (size_t)r0 * a.K, (uint64_t)a.K, (uint64_t)rows, kBK, NT,
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        tc_gemm_kernel<NT><<<grid, kThreads, smem, a.stream>>>(tmW, tmX, a.y + (size_t)r0 * a.N, rows,
-                                                                (int)a.N, (int)a.K, t.stages, a.ws,
-                                                                a.counters, a.status, a.wait_limit_ns);
-        e = cudaGetLastError();
+        e = launch(tc_gemm_kernel<NT>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
+                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, a.ws, a.counters, a.status,
+                   a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }

@@ -389,3 +389,50 @@ def test_tuned_plan_is_valid_and_correct(dep, orc):
             assert ok, (B, worst, idx)
     finally:
         dep.dep_projection_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("B", [2, 8, 40])
+def test_pdl_chain_respects_data_dependencies(dep, B):
+    """With DEP_PLAN_PDL each kernel streams its first weight tiles before the
+    preceding kernel finishes, but reads x only after it: a chain where every
+    call's output is the next call's input (kernels back to back, outputs
+    allocated beforehand) gives exactly the bits of the same chain without
+    overlap -- eagerly and replayed from a CUDA graph."""
+    N = K = 2048
+    Ws = [to_dev(synth.normal_bf16(20 + i, 1, (N, K), sigma=0.02)) for i in range(6)]
+    x0 = to_dev(synth.normal_bf16(20, 2, (B, K)))
+    plain = dep.dep_projection_plan(N, K, [B])
+    pdl = dep.dep_projection_plan(N, K, [B], dep.DEP_PLAN_PDL)
+    try:
+        def chain(plan, outs, stream=None):
+            x = x0
+            for W, y in zip(Ws, outs):
+                dep.dep_projection_run(plan, x, W, y, B, stream)
+                x = y
+
+        ref = [empty_out(B, N) for _ in Ws]
+        chain(plain, ref)
+        got = [empty_out(B, N) for _ in Ws]
+        torch.cuda.synchronize()
+        chain(pdl, got)
+        torch.cuda.synchronize()
+        for r, g in zip(ref, got):
+            assert torch.equal(r.view(torch.int16), g.view(torch.int16))
+        outs = [empty_out(B, N) for _ in Ws]
+        s = torch.cuda.Stream()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            chain(pdl, outs, s)
+        for _ in range(3):
+            for o in outs:
+                o.fill_(float("nan"))
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            for r, g in zip(ref, outs):
+                assert torch.equal(r.view(torch.int16), g.view(torch.int16))
+        assert dep.dep_projection_device_status(pdl) == 0
+    finally:
+        dep.dep_projection_plan_destroy(plain)
+        dep.dep_projection_plan_destroy(pdl)
