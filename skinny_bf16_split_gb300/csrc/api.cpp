@@ -103,14 +103,15 @@ size_t tactic_counters(const dep_tactic_t &t, int64_t N)
 
 constexpr int32_t kFmaMaxRows = 4;  // default split point between the two kernels
 
-dep_tactic_t fma_tactic(int32_t rows, int32_t cols, int32_t stages, int sm_count, bool host_only)
+dep_tactic_t fma_tactic(int32_t rows, int32_t cols, int32_t stages, int sm_count, bool host_only,
+                        int32_t tile_n = 32)
 {
     dep_tactic_t t{};
     t.max_rows = rows;
     t.kind = DEP_KIND_SPLITK_FMA;
     t.tile_k = 256;
     t.cols = cols;
-    t.tile_n = cols >= 8 ? 32 : 64;
+    t.tile_n = tile_n;
     t.stages = stages;
     int per_sm = host_only ? 1 : dep::fma_blocks_per_sm(t);
     t.ctas = sm_count * (per_sm < 1 ? 1 : per_sm);
@@ -148,8 +149,11 @@ int32_t tc_default_stages(int32_t cols)
 dep_tactic_t default_tactic(int32_t rows, int64_t N, int sm_count, bool host_only)
 {
     if (rows <= kFmaMaxRows) {
+        // One x row: 32-row tiles, 8 stages (the first data arrives sooner).  Two
+        // or four x rows: 64-row tiles reuse each x value over 8 rows per warp.
         const int32_t cols = pow2_at_least(rows);
-        return fma_tactic(rows, cols, 4, sm_count, host_only);
+        return cols == 1 ? fma_tactic(rows, cols, 8, sm_count, host_only, 32)
+                         : fma_tactic(rows, cols, 4, sm_count, host_only, 64);
     }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128;
@@ -369,12 +373,13 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int sm_count)
     std::vector<dep_tactic_t> c;
     if (rows <= 8) {
         const int32_t cols = pow2_at_least(rows);
-        for (int32_t st : {3, 4, 6})
-            c.push_back(fma_tactic(rows, cols, st, sm_count, false));
+        for (int32_t tn : {32, 64})
+            for (int32_t st : {4, 6, 8})
+                c.push_back(fma_tactic(rows, cols, st, sm_count, false, tn));
     }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128;
-    for (int32_t st : {4, 6, 8}) {
+    for (int32_t st : {4, 6, 8, 10, 12}) {
         c.push_back(tc_tactic(rows, cols, st, sm_count));
         if (tiles < sm_count)
             c.push_back(tc_tactic(rows, cols, st, (int32_t)tiles));

@@ -37,11 +37,14 @@ constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kKT = 256;                  // columns per k-tile: 32 lanes x 8
 constexpr int kRowBytes = kKT * 2;        // one tile row in shared memory
 
-template <int BC>
+// BC rows of x per pass, TN weight rows per tile (R = TN / 8 per compute warp).
+template <int BC_, int TN_>
 struct Shape {
-    static constexpr int R = BC >= 8 ? 4 : 8;  // weight rows per compute warp
-    static constexpr int TN = kWarps * R;      // weight rows per tile
+    static constexpr int BC = BC_;
+    static constexpr int TN = TN_;
+    static constexpr int R = TN / kWarps;  // weight rows per compute warp
     static constexpr int STAGE_BYTES = (TN + BC) * kRowBytes;
+    static_assert(R * BC <= 32, "one lane per (row, batch row) value in the epilogue");
 };
 
 __device__ __forceinline__ void unpack8(const uint4 v, float f[8])
@@ -59,14 +62,14 @@ __device__ __forceinline__ uint16_t to_bf16(float v)
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-template <int BC>
+template <int BC, int TN_>
 __global__ void __launch_bounds__(kThreads, 1)
     splitk_fma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       uint16_t *__restrict__ y, int B, int N, int K, int stages,
                       float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ status,
                       uint64_t limit_ns)
 {
-    constexpr int R = Shape<BC>::R, TN = Shape<BC>::TN, STAGE_BYTES = Shape<BC>::STAGE_BYTES;
+    constexpr int R = Shape<BC, TN_>::R, TN = TN_, STAGE_BYTES = Shape<BC, TN_>::STAGE_BYTES;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * STAGE_BYTES);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + stages);
@@ -265,42 +268,58 @@ __global__ void selftest_timeout_kernel(int *status, uint64_t limit_ns)
         record_status(status, DEP_DEV_TIMEOUT_CONSUMER);
 }
 
-template <int BC>
+template <class S>
 size_t smem_bytes(int stages)
 {
-    return (size_t)stages * Shape<BC>::STAGE_BYTES + 2 * (size_t)stages * sizeof(uint64_t);
+    return (size_t)stages * S::STAGE_BYTES + 2 * (size_t)stages * sizeof(uint64_t);
 }
 
 constexpr size_t kMaxSmem = 227 * 1024;
 
-template <int BC>
+template <class S>
 cudaError_t prepare()
 {
     static cudaError_t once = cudaFuncSetAttribute(
-        splitk_fma_kernel<BC>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
+        splitk_fma_kernel<S::BC, S::TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
     return once;
 }
 
-template <int BC>
-cudaError_t run_bc(const dep_tactic_t &t, const RunArgs &a)
+// Call f with the Shape of (cols, tile rows); false if this build has no such kernel.
+template <typename F>
+bool with_shape(int cols, int tile_n, F &&f)
 {
-    cudaError_t e = prepare<BC>();
+    switch (cols * 1000 + tile_n) {
+    case 1032: f(Shape<1, 32>{}); return true;
+    case 1064: f(Shape<1, 64>{}); return true;
+    case 2032: f(Shape<2, 32>{}); return true;
+    case 2064: f(Shape<2, 64>{}); return true;
+    case 4032: f(Shape<4, 32>{}); return true;
+    case 4064: f(Shape<4, 64>{}); return true;
+    case 8032: f(Shape<8, 32>{}); return true;
+    default: return false;
+    }
+}
+
+template <class S>
+cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
+{
+    constexpr int BC = S::BC, TN = S::TN;
+    cudaError_t e = prepare<S>();
     if (e != cudaSuccess)
         return e;
-    constexpr int TN = Shape<BC>::TN;
     CUtensorMap tmW, tmX;
     if (encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kKT, TN,
                        CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const int64_t T = (a.N + TN - 1) / TN, KT = (a.K + kKT - 1) / kKT, U = T * KT;
     const int grid = (int)(U < t.ctas ? U : t.ctas);
-    const size_t smem = smem_bytes<BC>(t.stages);
+    const size_t smem = smem_bytes<S>(t.stages);
     for (int32_t r0 = 0; r0 < a.B; r0 += BC) {
         const int32_t rows = a.B - r0 < BC ? a.B - r0 : BC;
         if (encode_bf16_2d(&tmX, a.x + (size_t)r0 * a.K, (uint64_t)a.K, (uint64_t)rows, kKT, BC,
                            CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        e = launch(splitk_fma_kernel<BC>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
+        e = launch(splitk_fma_kernel<BC, TN>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
                    a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, a.ws, a.counters, a.status,
                    a.wait_limit_ns);
         if (e != cudaSuccess)
@@ -309,38 +328,11 @@ cudaError_t run_bc(const dep_tactic_t &t, const RunArgs &a)
     return cudaSuccess;
 }
 
-template <int BC>
-int blocks_per_sm(int stages)
-{
-    if (prepare<BC>() != cudaSuccess)
-        return 0;
-    int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitk_fma_kernel<BC>, kThreads,
-                                                      smem_bytes<BC>(stages)) != cudaSuccess)
-        return 0;
-    return n;
-}
-
-size_t smem_for(const dep_tactic_t &t)
-{
-    switch (t.cols) {
-    case 1: return smem_bytes<1>(t.stages);
-    case 2: return smem_bytes<2>(t.stages);
-    case 4: return smem_bytes<4>(t.stages);
-    case 8: return smem_bytes<8>(t.stages);
-    default: return 0;
-    }
-}
-
+// Default tile height for a column count: 32 rows (one 16-byte load per lane
+// per row; smaller boxes bring the first data in sooner).
 int tile_rows(int cols)
 {
-    switch (cols) {
-    case 1: return Shape<1>::TN;
-    case 2: return Shape<2>::TN;
-    case 4: return Shape<4>::TN;
-    case 8: return Shape<8>::TN;
-    default: return 0;
-    }
+    return (cols == 1 || cols == 2 || cols == 4 || cols == 8) ? 32 : 0;
 }
 
 }  // namespace
@@ -349,11 +341,12 @@ bool fma_valid(const dep_tactic_t &t)
 {
     if (t.kind != DEP_KIND_SPLITK_FMA || t.ctas < 1 || t.tile_k != kKT)
         return false;
-    if (tile_rows(t.cols) == 0 || t.tile_n != tile_rows(t.cols))
-        return false;
     if (t.stages < 2 || t.stages > 16)
         return false;
-    return smem_for(t) <= kMaxSmem;
+    size_t smem = 0;
+    if (!with_shape(t.cols, t.tile_n, [&](auto sh) { smem = smem_bytes<decltype(sh)>(t.stages); }))
+        return false;
+    return smem <= kMaxSmem;
 }
 
 int64_t fma_units(const dep_tactic_t &t, int64_t N, int64_t K)
@@ -373,24 +366,22 @@ size_t fma_counters(const dep_tactic_t &t, int64_t N)
 
 int fma_blocks_per_sm(const dep_tactic_t &t)
 {
-    switch (t.cols) {
-    case 1: return blocks_per_sm<1>(t.stages);
-    case 2: return blocks_per_sm<2>(t.stages);
-    case 4: return blocks_per_sm<4>(t.stages);
-    case 8: return blocks_per_sm<8>(t.stages);
-    default: return 0;
-    }
+    int n = 0;
+    with_shape(t.cols, t.tile_n, [&](auto sh) {
+        using S = decltype(sh);
+        if (prepare<S>() != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitk_fma_kernel<S::BC, S::TN>, kThreads,
+                                                          smem_bytes<S>(t.stages)) != cudaSuccess)
+            n = 0;
+    });
+    return n;
 }
 
 cudaError_t fma_run(const dep_tactic_t &t, const RunArgs &a)
 {
-    switch (t.cols) {
-    case 1: return run_bc<1>(t, a);
-    case 2: return run_bc<2>(t, a);
-    case 4: return run_bc<4>(t, a);
-    case 8: return run_bc<8>(t, a);
-    default: return cudaErrorInvalidValue;
-    }
+    cudaError_t e = cudaErrorInvalidValue;
+    with_shape(t.cols, t.tile_n, [&](auto sh) { e = run_shape<decltype(sh)>(t, a); });
+    return e;
 }
 
 cudaError_t selftest_timeout(int32_t limit_us, int32_t *code)

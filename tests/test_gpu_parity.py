@@ -20,10 +20,9 @@ from skinny_bf16_split_gb300 import synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 
-def fma_tactic(dep, cols, ctas, stages=None, max_rows=None):
-    tn = 32 if cols >= 8 else 64
+def fma_tactic(dep, cols, ctas, stages=None, max_rows=None, tile_n=32):
     return dep.dep_tactic_t(max_rows=max_rows or cols, kind=dep.DEP_KIND_SPLITK_FMA, ctas=ctas,
-                            tile_n=tn, tile_k=256, stages=stages or (6 if cols >= 8 else 4),
+                            tile_n=tile_n, tile_k=256, stages=stages or (6 if cols >= 8 else 4),
                             cols=cols)
 
 
@@ -66,13 +65,13 @@ SHAPES = [(333, 3000), (64, 256), (97, 264), (1, 8), (1000, 1032)]
 
 
 @pytest.mark.parametrize("N,K", SHAPES)
-@pytest.mark.parametrize("cols", [1, 2, 4, 8])
+@pytest.mark.parametrize("cols,tile_n", [(1, 32), (1, 64), (2, 32), (2, 64), (4, 32), (4, 64), (8, 32)])
 @pytest.mark.parametrize("ctas", [1, 7, 152, 1000])
-def test_fma_bitexact_vs_mirror(dep, orc, plan_cache, N, K, cols, ctas):
+def test_fma_bitexact_vs_mirror(dep, orc, plan_cache, N, K, cols, tile_n, ctas):
     B = {1: 1, 2: 2, 4: 3, 8: 8}[cols]
     x = synth.normal_bf16(N + cols, 2, (B, K))
     W = synth.normal_bf16(N + ctas, 1, (N, K), sigma=0.02)
-    t = fma_tactic(dep, cols, ctas)
+    t = fma_tactic(dep, cols, ctas, tile_n=tile_n)
     y = run(dep, get_plan(dep, plan_cache, N, K), x, W, N, t)
     T = -(-N // t.tile_n) * -(-K // 256)
     want = orc.mirror_fma(x, W, min(ctas, T), t.tile_n)
