@@ -44,7 +44,13 @@ WORKLOAD_TEXT = {
     "dsa_wide": "wide DSA input projection: x[B,7168] . W[14560,7168]^T, B in {32,64,128,256}, seeds 0..3",
     "chain": "8-layer decode chain: per layer x[16,7168] . W_dsa[14560,7168]^T then "
              "x'[16,12288] . W_o[7168,12288]^T, 16 distinct weights, seed 7",
+    "dsa_verify": "verify-step batches on the DSA input projection: x[B,7168] . W[14560,7168]^T, "
+                  "B = requests x q in {3,6,12,24,48}, seeds 0..4, tuned plan",
+    "tp_sharded": "TP-G shards at B=16: DSA input projection rows 14560/G x 7168 and o_proj "
+                  "7168 x 12288/G for G in {2,4,8}, seeds 0..5",
 }
+# Workloads whose plan is tuned by default (the verify-step tables are measured).
+TUNED_BY_DEFAULT = {"dsa_verify"}
 KERNEL_SOURCES = ["splitk_fma.cu", "tc_gemm.cu", "ptx.cuh", "internal.h"]
 
 
@@ -290,7 +296,8 @@ def run_ours(args):
     plans = {}
     for c in calls:
         plans.setdefault((c.N, c.K), set()).add(c.B)
-    flags = dep.DEP_PLAN_TUNE if args.plan == "tune" else dep.DEP_PLAN_DEFAULT
+    tuned = args.plan == "tune" or args.workload in TUNED_BY_DEFAULT
+    flags = dep.DEP_PLAN_TUNE if tuned else dep.DEP_PLAN_DEFAULT
     plans = {k: dep.dep_projection_plan(k[0], k[1], sorted(v), flags) for k, v in plans.items()}
     tactics = [dep.dep_projection_plan_query(plans[(c.N, c.K)], c.B) for c in calls]
     launches_per_step = sum(-(-c.B // t.cols) for c, t in zip(calls, tactics))
@@ -366,8 +373,11 @@ def run_ours(args):
                 "share_of_timed_region": d["ms"] / (call_ms.sum() or 1.0)}
     per_call = []
     for i, (c, t) in enumerate(zip(calls, tactics)):
-        us = float(np.median(call_ms[:, i])) * 1e3
-        per_call.append({"call": c.name, "N": c.N, "K": c.K, "B": c.B, "us_median": us,
+        # Event timestamps tick in about 2 us steps: the mean over the timed
+        # steps resolves a call's time, a single pair (or the median) does not.
+        us = float(np.mean(call_ms[:, i])) * 1e3
+        per_call.append({"call": c.name, "N": c.N, "K": c.K, "B": c.B, "us_mean": us,
+                         "us_median": float(np.median(call_ms[:, i])) * 1e3,
                          "gbs": c.algorithmic_bytes / (us * 1e-6) / 1e9,
                          "frac_of_peak": c.algorithmic_bytes / (us * 1e-6) / 1e9 / peak,
                          "kernel": kernel_name(t), "tactic": t.as_dict()})
@@ -394,7 +404,7 @@ def run_ours(args):
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "graph_pdl": graph,
             "gpu_launches": launches_per_step * args.steps, "per_call": per_call,
-            "plan": args.plan, "kernel_sources": source_hash(),
+            "plan": "tune" if tuned else "default", "kernel_sources": source_hash(),
             "device": torch.cuda.get_device_name(device),
         }
         print(json.dumps(line), flush=True)

@@ -118,13 +118,13 @@ dep_tactic_t fma_tactic(int32_t rows, int32_t cols, int32_t stages, int sm_count
     return t;
 }
 
-dep_tactic_t tc_tactic(int32_t rows, int32_t cols, int32_t stages, int32_t ctas)
+dep_tactic_t tc_tactic(int32_t rows, int32_t cols, int32_t stages, int32_t ctas, int32_t tile_k = 64)
 {
     dep_tactic_t t{};
     t.max_rows = rows;
     t.kind = DEP_KIND_TC;
     t.tile_n = 128;
-    t.tile_k = 64;
+    t.tile_k = tile_k;
     t.cols = cols;
     t.stages = stages;
     t.ctas = ctas;
@@ -149,15 +149,24 @@ int32_t tc_default_stages(int32_t cols)
 dep_tactic_t default_tactic(int32_t rows, int64_t N, int sm_count, bool host_only)
 {
     if (rows <= kFmaMaxRows) {
-        // One x row: 32-row tiles, 8 stages (the first data arrives sooner).  Two
-        // or four x rows: 64-row tiles reuse each x value over 8 rows per warp.
+        // 64-row tiles (each x value reused over 8 rows per warp), 4 stages of
+        // 32-34 KB; 6 stages for four x rows.  Measured on GB300 against 32-row
+        // tiles with up to 8 stages: equal or faster on all three weights.
         const int32_t cols = pow2_at_least(rows);
-        return cols == 1 ? fma_tactic(rows, cols, 8, sm_count, host_only, 32)
-                         : fma_tactic(rows, cols, 4, sm_count, host_only, 64);
+        return fma_tactic(rows, cols, cols >= 4 ? 6 : 4, sm_count, host_only, 64);
     }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128;
     const int32_t ctas = (tiles <= sm_count && 4 * tiles >= 3 * (int64_t)sm_count) ? (int32_t)tiles : sm_count;
+    // Widest stage (most contiguous bytes per weight row) that still leaves a
+    // ring of at least three stages; 64-column stages for the widest batches.
+    for (int32_t tk : {256, 128}) {
+        for (int32_t st : {6, 5, 4, 3}) {
+            const dep_tactic_t t = tc_tactic(rows, cols, st, ctas, tk);
+            if (dep::tc_valid(t))
+                return t;
+        }
+    }
     return tc_tactic(rows, cols, tc_default_stages(cols), ctas);
 }
 
@@ -379,11 +388,12 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int sm_count)
     }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128;
-    for (int32_t st : {4, 6, 8, 10, 12}) {
-        c.push_back(tc_tactic(rows, cols, st, sm_count));
-        if (tiles < sm_count)
-            c.push_back(tc_tactic(rows, cols, st, (int32_t)tiles));
-    }
+    for (int32_t tk : {64, 128, 256})
+        for (int32_t st : {2, 3, 4, 6, 8, 10, 12}) {
+            c.push_back(tc_tactic(rows, cols, st, sm_count, tk));
+            if (tiles < sm_count)
+                c.push_back(tc_tactic(rows, cols, st, (int32_t)tiles, tk));
+        }
     std::vector<dep_tactic_t> ok;
     for (const auto &t : c)
         if (tactic_valid(t))
@@ -439,20 +449,25 @@ dep_status_t tune_plan(dep_plan_s *p)
         dep_tactic_t best_t = p->table[i];
         size_t turn = 0;
         for (const auto &c : cands[i]) {
+            // Event timestamps are coarse (about 2 us on GB300): time batches of
+            // 8 back-to-back launches between one pair of events; keep the best
+            // of 3 batches, after 2 warm-up launches.
+            for (int w = 0; w < 2 && ok; ++w)
+                ok = run_impl(p, &c, xs, Wc + (turn++ % copies) * (wbytes / 2), ys, B, s) == DEP_OK;
             std::vector<float> ms;
-            for (int rep = 0; rep < 12 && ok; ++rep) {
-                const uint16_t *W = Wc + (turn++ % copies) * (wbytes / 2);
-                ok = cudaEventRecord(e0, s) == cudaSuccess &&
-                     run_impl(p, &c, xs, W, ys, B, s) == DEP_OK && cudaEventRecord(e1, s) == cudaSuccess &&
-                     cudaEventSynchronize(e1) == cudaSuccess;
+            for (int rep = 0; rep < 3 && ok; ++rep) {
+                ok = cudaEventRecord(e0, s) == cudaSuccess;
+                for (int l = 0; l < 8 && ok; ++l)
+                    ok = run_impl(p, &c, xs, Wc + (turn++ % copies) * (wbytes / 2), ys, B, s) == DEP_OK;
+                ok = ok && cudaEventRecord(e1, s) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess;
                 float t = 0;
-                if (ok && rep >= 2 && cudaEventElapsedTime(&t, e0, e1) == cudaSuccess)
-                    ms.push_back(t);
+                if (ok && cudaEventElapsedTime(&t, e0, e1) == cudaSuccess)
+                    ms.push_back(t / 8);
             }
             if (!ok || ms.empty())
                 break;
             std::sort(ms.begin(), ms.end());
-            const float med = ms[ms.size() / 2];
+            const float med = ms[0];
             if (p->log)
                 std::fprintf(stderr, "[dep] tune N=%lld K=%lld B=%d kind=%d cols=%d stages=%d ctas=%d: %.2f us\n",
                              (long long)p->N, (long long)p->K, B, c.kind, c.cols, c.stages, c.ctas, med * 1e3f);

@@ -59,6 +59,56 @@ __host__ __device__ inline int64_t sk_owner(int64_t u, int64_t U, int64_t C)
     return ((u + 1) * C - 1) / U;
 }
 
+// Order in which a block visits its units: the segment of its last tile first,
+// then the segment of its first tile, then the whole tiles in between.  Both
+// split tiles a block shares with its neighbours are thus finished (and their
+// split-K fix-up done) early, and the block ends on a whole tile whenever its
+// range holds one.  Units inside a segment keep increasing k order, so the
+// arithmetic of every output does not depend on this order.
+struct SegOrder {
+    int64_t u_begin, u_end, ktiles, t_first, t_last, m;
+    __host__ __device__ SegOrder(int64_t ub, int64_t ue, int64_t kt)
+        : u_begin(ub), u_end(ue), ktiles(kt), t_first(ub / kt), t_last(ue > ub ? (ue - 1) / kt : ub / kt),
+          m(ue > ub ? t_last - t_first + 1 : 0)
+    {
+    }
+    __host__ __device__ int64_t tile(int64_t i) const
+    {
+        return m >= 2 ? (i == 0 ? t_last : t_first + i - 1) : t_first;
+    }
+    __host__ __device__ int64_t seg_begin(int64_t t) const
+    {
+        return u_begin > t * ktiles ? u_begin : t * ktiles;
+    }
+    __host__ __device__ int64_t seg_end(int64_t t) const
+    {
+        return u_end < (t + 1) * ktiles ? u_end : (t + 1) * ktiles;
+    }
+};
+
+// Walks a block's units in SegOrder.
+struct UnitCursor {
+    SegOrder o;
+    int64_t i, u, end;
+    __host__ __device__ explicit UnitCursor(const SegOrder &order) : o(order), i(0), u(0), end(0)
+    {
+        if (o.m > 0) {
+            u = o.seg_begin(o.tile(0));
+            end = o.seg_end(o.tile(0));
+        }
+    }
+    __host__ __device__ bool done() const { return i >= o.m; }
+    __host__ __device__ void next()
+    {
+        if (++u < end)
+            return;
+        if (++i < o.m) {
+            u = o.seg_begin(o.tile(i));
+            end = o.seg_end(o.tile(i));
+        }
+    }
+};
+
 // ---- split-K FMA tactic (splitk_fma.cu) ----
 bool fma_valid(const dep_tactic_t &t);
 int64_t fma_units(const dep_tactic_t &t, int64_t N, int64_t K);  // stream-K work units

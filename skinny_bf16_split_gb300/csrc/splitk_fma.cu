@@ -96,23 +96,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
             // The weight is not written by preceding work: fill the ring with its
             // first tiles, then wait for the preceding grid before reading x.
+            const SegOrder order(u_begin, u_end, KTILES);
             const int64_t pre = (u_end - u_begin) < stages ? (u_end - u_begin) : stages;
-            for (int64_t i = 0; i < pre; ++i) {
-                const int64_t u = u_begin + i;
+            UnitCursor cur(order);
+            for (int64_t i = 0; i < pre; ++i, cur.next()) {
+                const int64_t u = cur.u;
                 mbar_arrive_expect_tx(full0 + 8 * (int)i, STAGE_BYTES);
                 tma_load_2d(smem_u32(smem + (size_t)i * STAGE_BYTES), &tmW, (int)(u % KTILES) * kKT,
                             (int)(u / KTILES) * TN, full0 + 8 * (int)i, pol_w);
             }
             griddep_wait();
-            for (int64_t i = 0; i < pre; ++i) {
-                const int64_t u = u_begin + i;
+            UnitCursor cx(order);
+            for (int64_t i = 0; i < pre; ++i, cx.next()) {
+                const int64_t u = cx.u;
                 tma_load_2d(smem_u32(smem + (size_t)i * STAGE_BYTES) + TN * kRowBytes, &tmX,
                             (int)(u % KTILES) * kKT, 0, full0 + 8 * (int)i, pol_x);
             }
             int s = (int)(pre % stages);
             uint32_t ph = pre == stages ? 1u : 0u;
             int64_t issued = pre;
-            for (int64_t u = u_begin + pre; u < u_end; ++u) {
+            for (; !cur.done(); cur.next()) {
+                const int64_t u = cur.u;
                 if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, limit_ns)) {
                     record_status(status, DEP_DEV_TIMEOUT_PRODUCER);
                     break;
@@ -151,18 +155,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     const int64_t first_t = u_begin / KTILES;
-    int64_t u = u_begin;
-    while (u < u_end) {
-        const int64_t t = u / KTILES;
-        const int64_t seg_end = u_end < (t + 1) * KTILES ? u_end : (t + 1) * KTILES;
-        const bool whole = (u == t * KTILES) && (seg_end == (t + 1) * KTILES);
+    const SegOrder order(u_begin, u_end, KTILES);
+    for (int64_t seg = 0; seg < order.m; ++seg) {
+        const int64_t t = order.tile(seg);
+        const int64_t seg_u0 = order.seg_begin(t), seg_end = order.seg_end(t);
+        const bool whole = (seg_u0 == t * KTILES) && (seg_end == (t + 1) * KTILES);
 #pragma unroll
         for (int i = 0; i < R; ++i)
 #pragma unroll
             for (int b = 0; b < BC; ++b)
                 acc[i][b] = 0.0f;
 
-        for (; u < seg_end; ++u) {
+        for (int64_t u = seg_u0; u < seg_end; ++u) {
             if (!mbar_wait(full0 + 8 * s, ph, limit_ns)) {
                 record_status(status, DEP_DEV_TIMEOUT_CONSUMER);
                 return;

@@ -9,12 +9,14 @@
 //  * Swap-AB: the MMA's M side is 128 weight rows, its N side the batch padded
 //    to NT (16..256), so one weight tile feeds one MMA and a tiny batch wastes
 //    only tensor throughput, never weight bytes.  D[128 x NT] lives in TMEM.
-//  * Work units are (128-row tile, 64-column k-tile) pairs; the persistent
-//    blocks take equal contiguous ranges (stream-K), exactly as the FMA tactic.
-//  * Warp 0: TMA producer.  Weight tile [128 x 64] and activation tile [NT x 64]
-//    land in a shared-memory ring in the 128-byte swizzle layout.
+//  * Work units are (128-row tile, tile_k-column k-tile) pairs, tile_k = 64, 128
+//    or 256; the persistent blocks take equal contiguous ranges (stream-K),
+//    exactly as the FMA tactic.
+//  * Warp 0: TMA producer.  Per stage, tile_k / 64 weight slices [128 x 64] and
+//    activation slices [NT x 64] land in a shared-memory ring in the 128-byte
+//    swizzle layout (wider stages give each weight row longer contiguous reads).
 //  * Warp 1: allocates TMEM (two accumulators of NT columns), one thread issues
-//    tcgen05.mma (4 per stage, K = 16 each) and releases each stage with
+//    tcgen05.mma (4 per 64-column slice, K = 16 each) and releases each stage with
 //    tcgen05.commit; at the end of a segment it commits the accumulator.
 //  * Warps 2-5: epilogue.  Each owns the 32 TMEM lanes (= weight rows) of its
 //    quadrant, reads its accumulator with tcgen05.ld, frees it for the MMA of
@@ -39,10 +41,12 @@ constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA/TMEM, warps 2-5 epil
 constexpr int kEpiWarps = 4;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB weight tile per stage
 
+// A stage holds `atoms` consecutive 64-column slices of one unit: the weight
+// slices [128 x 64] first (16 KB each), then the activation slices [NT x 64].
 template <int NT>
 struct TcShape {
-    static constexpr int B_BYTES = NT * kBK * 2;
-    static constexpr int STAGE = kABytes + B_BYTES;  // a multiple of 1024
+    static constexpr int B_BYTES = NT * kBK * 2;     // one activation slice (a multiple of 1024)
+    static constexpr int ATOM = kABytes + B_BYTES;   // bytes per 64-column slice pair
     static constexpr uint32_t TMEM_COLS = 2 * NT < 32 ? 32 : 2 * NT;
 };
 
@@ -54,15 +58,18 @@ __device__ __forceinline__ uint16_t to_bf16(float v)
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   uint16_t *__restrict__ y, int B, int N, int K, int stages, float *__restrict__ ws,
-                   int *__restrict__ counters, int *__restrict__ status, uint64_t limit_ns)
+                   uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms,
+                   float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ status,
+                   uint64_t limit_ns)
 {
     using S = TcShape<NT>;
+    const int STAGE = atoms * S::ATOM;   // bytes per stage
+    const int KG = atoms * kBK;          // columns per unit
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles need 1 KB alignment
     uint8_t *smem = smem_raw + (base - raw);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * S::STAGE);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * STAGE);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * stages;
     const uint32_t accf0 = empty0 + 8 * stages;  // accumulator ready, 2 buffers
@@ -71,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 5);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    const int64_t T = (N + kBM - 1) / kBM, KTILES = (K + kBK - 1) / kBK, U = T * KTILES;
+    const int64_t T = (N + kBM - 1) / kBM, KTILES = (K + KG - 1) / KG, U = T * KTILES;
     const int64_t C = gridDim.x, c = blockIdx.x;
     const int64_t u_begin = sk_begin(c, U, C), u_end = sk_begin(c + 1, U, C);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,23 +114,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
             // The weight is not written by preceding work: fill the ring with its
             // first tiles, then wait for the preceding grid before reading x.
+            const SegOrder order(u_begin, u_end, KTILES);
             const int64_t pre = (u_end - u_begin) < stages ? (u_end - u_begin) : stages;
-            for (int64_t i = 0; i < pre; ++i) {
-                const int64_t u = u_begin + i;
-                mbar_arrive_expect_tx(full0 + 8 * (int)i, S::STAGE);
-                tma_load_2d(base + (uint32_t)(i * S::STAGE), &tmW, (int)(u % KTILES) * kBK,
-                            (int)(u / KTILES) * kBM, full0 + 8 * (int)i, pol_w);
+            UnitCursor cur(order);
+            for (int64_t i = 0; i < pre; ++i, cur.next()) {
+                const int64_t u = cur.u;
+                const uint32_t st = base + (uint32_t)(i * STAGE);
+                mbar_arrive_expect_tx(full0 + 8 * (int)i, STAGE);
+                for (int a = 0; a < atoms; ++a)
+                    tma_load_2d(st + (uint32_t)(a * kABytes), &tmW, (int)(u % KTILES) * KG + a * kBK,
+                                (int)(u / KTILES) * kBM, full0 + 8 * (int)i, pol_w);
             }
             griddep_wait();
-            for (int64_t i = 0; i < pre; ++i) {
-                const int64_t u = u_begin + i;
-                tma_load_2d(base + (uint32_t)(i * S::STAGE) + kABytes, &tmX, (int)(u % KTILES) * kBK, 0,
-                            full0 + 8 * (int)i, pol_x);
+            UnitCursor cx(order);
+            for (int64_t i = 0; i < pre; ++i, cx.next()) {
+                const int64_t u = cx.u;
+                const uint32_t xs = base + (uint32_t)(i * STAGE) + (uint32_t)(atoms * kABytes);
+                for (int a = 0; a < atoms; ++a)
+                    tma_load_2d(xs + (uint32_t)(a * S::B_BYTES), &tmX, (int)(u % KTILES) * KG + a * kBK, 0,
+                                full0 + 8 * (int)i, pol_x);
             }
             int s = (int)(pre % stages);
             uint32_t ph = pre == stages ? 1u : 0u;
             int64_t issued = pre;
-            for (int64_t u = u_begin + pre; u < u_end; ++u) {
+            for (; !cur.done(); cur.next()) {
+                const int64_t u = cur.u;
                 if (*abort_flag)
                     break;
                 if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, limit_ns)) {
@@ -131,11 +146,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *abort_flag = 1;
                     break;
                 }
-                const uint32_t a = base + (uint32_t)(s * S::STAGE);
-                mbar_arrive_expect_tx(full0 + 8 * s, S::STAGE);
-                const int t = (int)(u / KTILES), kt = (int)(u % KTILES);
-                tma_load_2d(a, &tmW, kt * kBK, t * kBM, full0 + 8 * s, pol_w);
-                tma_load_2d(a + kABytes, &tmX, kt * kBK, 0, full0 + 8 * s, pol_x);
+                const uint32_t st = base + (uint32_t)(s * STAGE);
+                mbar_arrive_expect_tx(full0 + 8 * s, STAGE);
+                const int t = (int)(u / KTILES), kg = (int)(u % KTILES);
+                for (int a = 0; a < atoms; ++a)
+                    tma_load_2d(st + (uint32_t)(a * kABytes), &tmW, kg * KG + a * kBK, t * kBM, full0 + 8 * s,
+                                pol_w);
+                for (int a = 0; a < atoms; ++a)
+                    tma_load_2d(st + (uint32_t)(atoms * kABytes + a * S::B_BYTES), &tmX, kg * KG + a * kBK, 0,
+                                full0 + 8 * s, pol_x);
                 ++issued;
                 if (++s == stages) {
                     s = 0;
@@ -161,11 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             int s = 0;
             uint32_t ph = 0, acce_ph = 0;
             int buf = 0;
-            int64_t u = u_begin;
+            const SegOrder order(u_begin, u_end, KTILES);
             bool ok = true;
-            while (u < u_end && ok) {
-                const int64_t t = u / KTILES;
-                const int64_t seg_end = u_end < (t + 1) * KTILES ? u_end : (t + 1) * KTILES;
+            for (int64_t seg = 0; seg < order.m && ok; ++seg) {
+                const int64_t t = order.tile(seg);
+                const int64_t seg_end = order.seg_end(t);
+                int64_t u = order.seg_begin(t);
                 if (!mbar_wait(acce0 + 8 * buf, ((acce_ph >> buf) & 1u) ^ 1u, limit_ns)) {
                     record_status(status, DEP_DEV_TIMEOUT_MMA);
                     *abort_flag = 1;
@@ -187,14 +207,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t a = base + (uint32_t)(s * S::STAGE);
-                    const uint64_t ad = tc::desc_sw128(a), bd = tc::desc_sw128(a + kABytes);
+                    const uint32_t st = base + (uint32_t)(s * STAGE);
+                    for (int a = 0; a < atoms; ++a) {
+                        const uint64_t ad = tc::desc_sw128(st + (uint32_t)(a * kABytes));
+                        const uint64_t bd = tc::desc_sw128(st + (uint32_t)(atoms * kABytes + a * S::B_BYTES));
 #pragma unroll
-                    for (int j = 0; j < kBK / kUmmaK; ++j) {
-                        // advance along K inside the 128-byte swizzle row: 32 bytes per step
-                        const uint64_t off = (uint64_t)((j * kUmmaK * 2) >> 4);
-                        tc::mma_bf16(d, ad + off, bd + off, idesc, accumulate);
-                        accumulate = 1;
+                        for (int j = 0; j < kBK / kUmmaK; ++j) {
+                            // advance along K inside the 128-byte swizzle row: 32 bytes per step
+                            const uint64_t off = (uint64_t)((j * kUmmaK * 2) >> 4);
+                            tc::mma_bf16(d, ad + off, bd + off, idesc, accumulate);
+                            accumulate = 1;
+                        }
                     }
                     tc::commit(empty0 + 8 * s);  // the stage is free once these MMAs finish
                     if (++s == stages) {
@@ -219,12 +242,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t first_t = u_begin / KTILES;
         uint32_t accf_ph = 0;
         int buf = 0;
-        int64_t u = u_begin;
-        while (u < u_end) {
-            const int64_t t = u / KTILES;
-            const int64_t seg_end = u_end < (t + 1) * KTILES ? u_end : (t + 1) * KTILES;
-            const bool whole = (u == t * KTILES) && (seg_end == (t + 1) * KTILES);
-            u = seg_end;
+        const SegOrder order(u_begin, u_end, KTILES);
+        for (int64_t seg = 0; seg < order.m; ++seg) {
+            const int64_t t = order.tile(seg);
+            const bool whole = (order.seg_begin(t) == t * KTILES) && (order.seg_end(t) == (t + 1) * KTILES);
             if (!mbar_wait(accf0 + 8 * buf, (accf_ph >> buf) & 1u, limit_ns)) {
                 record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
                 *abort_flag = 1;
@@ -275,29 +296,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             __threadfence();
             if (n < N) {
                 // Sum the segments in increasing block order.  The loads of up to
-                // 4 segments x 8 batch columns are issued together, then added.
-                for (int b0 = 0; b0 < B; b0 += 8) {
-                    float sum[8];
+                // 4 segments x 16 batch columns are issued together, then added.
+                for (int b0 = 0; b0 < B; b0 += 16) {
+                    float sum[16];
                     for (int64_t g0 = c_first; g0 <= c_last; g0 += 4) {
-                        float p[4][8];
+                        float p[4][16];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const int64_t cc = g0 + i;
                             const int sl = (t == sk_begin(cc, U, C) / KTILES) ? 0 : 1;
                             const float *src = ws + ((cc * 2 + sl) * NT + b0) * kBM + row;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
+                            for (int j = 0; j < 16; ++j)
                                 p[i][j] = (cc <= c_last && b0 + j < B) ? __ldcg(src + (int64_t)j * kBM) : 0.0f;
                         }
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
 #pragma unroll
-                            for (int j = 0; j < 8; ++j)
+                            for (int j = 0; j < 16; ++j)
                                 if (g0 + i <= c_last)
                                     sum[j] = (g0 + i == c_first) ? p[i][j] : sum[j] + p[i][j];
                     }
 #pragma unroll
-                    for (int j = 0; j < 8; ++j)
+                    for (int j = 0; j < 16; ++j)
                         if (b0 + j < B)
                             y[(int64_t)(b0 + j) * N + n] = to_bf16(sum[j]);
                 }
@@ -319,9 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr size_t kMaxSmem = 227 * 1024;
 
 template <int NT>
-size_t smem_bytes(int stages)
+size_t smem_bytes(int stages, int atoms)
 {
-    return 1024 + (size_t)stages * TcShape<NT>::STAGE + (size_t)(2 * stages + 5) * 8 + 16;
+    return 1024 + (size_t)stages * atoms * TcShape<NT>::ATOM + (size_t)(2 * stages + 5) * 8 + 16;
 }
 
 template <int NT>
@@ -342,17 +363,18 @@ cudaError_t run_nt(const dep_tactic_t &t, const RunArgs &a)
     if (encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, kBM,
                        CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    const int64_t T = (a.N + kBM - 1) / kBM, KT = (a.K + kBK - 1) / kBK, U = T * KT;
+    const int atoms = t.tile_k / kBK;
+    const int64_t T = (a.N + kBM - 1) / kBM, KT = (a.K + t.tile_k - 1) / t.tile_k, U = T * KT;
     const int grid = (int)(U < t.ctas ? U : t.ctas);
-    const size_t smem = smem_bytes<NT>(t.stages);
+    const size_t smem = smem_bytes<NT>(t.stages, atoms);
     for (int32_t r0 = 0; r0 < a.B; r0 += NT) {
         const int32_t rows = a.B - r0 < NT ? a.B - r0 : NT;
         if (encode_bf16_2d(&tmX, a.x + (size_t)r0 * a.K, (uint64_t)a.K, (uint64_t)rows, kBK, NT,
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
         e = launch(tc_gemm_kernel<NT>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
-                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, a.ws, a.counters, a.status,
-                   a.wait_limit_ns);
+                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, a.ws, a.counters,
+                   a.status, a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }
@@ -360,25 +382,26 @@ cudaError_t run_nt(const dep_tactic_t &t, const RunArgs &a)
 }
 
 template <int NT>
-int blocks_per_sm(int stages)
+int blocks_per_sm(int stages, int atoms)
 {
     if (prepare<NT>() != cudaSuccess)
         return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_gemm_kernel<NT>, kThreads,
-                                                      smem_bytes<NT>(stages)) != cudaSuccess)
+                                                      smem_bytes<NT>(stages, atoms)) != cudaSuccess)
         return 0;
     return n;
 }
 
 size_t smem_for(const dep_tactic_t &t)
 {
+    const int atoms = t.tile_k / kBK;
     switch (t.cols) {
-    case 16: return smem_bytes<16>(t.stages);
-    case 32: return smem_bytes<32>(t.stages);
-    case 64: return smem_bytes<64>(t.stages);
-    case 128: return smem_bytes<128>(t.stages);
-    case 256: return smem_bytes<256>(t.stages);
+    case 16: return smem_bytes<16>(t.stages, atoms);
+    case 32: return smem_bytes<32>(t.stages, atoms);
+    case 64: return smem_bytes<64>(t.stages, atoms);
+    case 128: return smem_bytes<128>(t.stages, atoms);
+    case 256: return smem_bytes<256>(t.stages, atoms);
     default: return 0;
     }
 }
@@ -387,17 +410,19 @@ size_t smem_for(const dep_tactic_t &t)
 
 bool tc_valid(const dep_tactic_t &t)
 {
-    if (t.kind != DEP_KIND_TC || t.ctas < 1 || t.tile_n != kBM || t.tile_k != kBK)
+    if (t.kind != DEP_KIND_TC || t.ctas < 1 || t.tile_n != kBM)
         return false;
+    if (t.tile_k != kBK && t.tile_k != 2 * kBK && t.tile_k != 4 * kBK)
+        return false;  // 1, 2 or 4 slices of 64 columns per stage
     if (t.stages < 2 || t.stages > 16)
         return false;
     const size_t smem = smem_for(t);
     return smem != 0 && smem <= kMaxSmem;
 }
 
-int64_t tc_units(const dep_tactic_t &, int64_t N, int64_t K)
+int64_t tc_units(const dep_tactic_t &t, int64_t N, int64_t K)
 {
-    return ((N + kBM - 1) / kBM) * ((K + kBK - 1) / kBK);
+    return ((N + kBM - 1) / kBM) * ((K + t.tile_k - 1) / t.tile_k);
 }
 
 size_t tc_ws_per_cta(const dep_tactic_t &t)
@@ -412,12 +437,13 @@ size_t tc_counters(const dep_tactic_t &, int64_t N)
 
 int tc_blocks_per_sm(const dep_tactic_t &t)
 {
+    const int atoms = t.tile_k / kBK;
     switch (t.cols) {
-    case 16: return blocks_per_sm<16>(t.stages);
-    case 32: return blocks_per_sm<32>(t.stages);
-    case 64: return blocks_per_sm<64>(t.stages);
-    case 128: return blocks_per_sm<128>(t.stages);
-    case 256: return blocks_per_sm<256>(t.stages);
+    case 16: return blocks_per_sm<16>(t.stages, atoms);
+    case 32: return blocks_per_sm<32>(t.stages, atoms);
+    case 64: return blocks_per_sm<64>(t.stages, atoms);
+    case 128: return blocks_per_sm<128>(t.stages, atoms);
+    case 256: return blocks_per_sm<256>(t.stages, atoms);
     default: return 0;
     }
 }

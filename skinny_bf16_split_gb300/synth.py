@@ -191,6 +191,18 @@ def workload(name: str) -> list[Call]:
         return [Call(f"kda_b{b}", *KDA, B=b, seed=s) for s, b in enumerate((1, 4, 8, 16))]
     if name == "dsa_wide":
         return [Call(f"dsa_b{b}", *DSA, B=b, seed=s) for s, b in enumerate((32, 64, 128, 256))]
+    if name == "dsa_verify":
+        # speculative verify steps: B = requests x q tokens (q = 2..4)
+        return [Call(f"dsa_verify_b{b}", *DSA, B=b, seed=s) for s, b in enumerate((3, 6, 12, 24, 48))]
+    if name == "tp_sharded":
+        # one rank's share of a TP-G hybrid step: input projection rows N/G,
+        # o_proj reduction K/G (the all-reduce of the partials is a separate step)
+        calls = []
+        for s, g in enumerate((2, 4, 8)):
+            calls.append(Call(f"dsa_tp{g}", DSA[0] // g, DSA[1], B=16, seed=s))
+        for s, g in enumerate((2, 4, 8)):
+            calls.append(Call(f"oproj_tp{g}", OPROJ[0], OPROJ[1] // g, B=16, seed=3 + s))
+        return calls
     if name == "chain":
         calls = []
         for layer in range(8):
@@ -202,4 +214,4 @@ def workload(name: str) -> list[Call]:
     raise KeyError(f"unknown workload {name!r}")
 
 
-WORKLOADS = ("dsa_b1", "oproj_sweep", "kda_sweep", "dsa_wide", "chain")
+WORKLOADS = ("dsa_b1", "oproj_sweep", "kda_sweep", "dsa_wide", "chain", "dsa_verify", "tp_sharded")

@@ -2,8 +2,11 @@
 
 Workloads (skinny_bf16_split_gb300.synth): the DSA packed input projection at
 B = 1 (unit-RMS rows), the o_proj sweep, the KDA packed input projection sweep,
-the wide-batch DSA projection, and the 8-layer decode chain -- the weights the
-runtime.dep page lists (DSA 14560 x 7168, o_proj 7168 x 12288, KDA 49376 x 7168).
+the wide-batch DSA projection, the 8-layer decode chain -- the weights the
+runtime.dep page lists (DSA 14560 x 7168, o_proj 7168 x 12288, KDA 49376 x 7168)
+-- plus verify-step batches B = requests x q (runtime.dep page, DepKda: verify
+keys (B // q, q)) and TP-G shards of the same weights (runtime.hybrid page,
+HybridAttention.__init__: projection_policies(tp, pitch, ...), o_proj 12288 // tp).
 
 Each call runs through the default plan for its shape and batch set (as the
 benchmark does) and is checked against the exact oracle on sampled weight rows:
@@ -58,7 +61,9 @@ def test_workload_full_size(dep, orc, weights, workload):
     batches = {}
     for c in calls:
         batches.setdefault((c.N, c.K), set()).add(c.B)
-    plans = {k: dep.dep_projection_plan(k[0], k[1], sorted(v)) for k, v in batches.items()}
+    from bench import TUNED_BY_DEFAULT  # the launch configuration the bench times
+    flags = dep.DEP_PLAN_TUNE if workload in TUNED_BY_DEFAULT else dep.DEP_PLAN_DEFAULT
+    plans = {k: dep.dep_projection_plan(k[0], k[1], sorted(v), flags) for k, v in batches.items()}
     try:
         for i, c in enumerate(calls):
             W = weights(c)

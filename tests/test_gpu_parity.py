@@ -287,8 +287,8 @@ def test_stock_gemm_within_tolerance_of_oracle(orc):
 
 # ---------------- tensor-core (tcgen05) tactic ----------------
 
-def tc_tactic(dep, NT, ctas, stages=4):
-    return dep.dep_tactic_t(max_rows=NT, kind=dep.DEP_KIND_TC, ctas=ctas, tile_n=128, tile_k=64,
+def tc_tactic(dep, NT, ctas, stages=4, tile_k=64):
+    return dep.dep_tactic_t(max_rows=NT, kind=dep.DEP_KIND_TC, ctas=ctas, tile_n=128, tile_k=tile_k,
                             stages=stages, cols=NT)
 
 
@@ -303,17 +303,20 @@ def sm_count():
 
 
 @pytest.mark.parametrize("N,K", [(128, 64), (333, 1000), (97, 264), (1000, 3000)])
-@pytest.mark.parametrize("NT", [16, 32, 64, 128, 256])
-def test_tc_parity_vs_oracle(dep, orc, plan_cache, N, K, NT):
-    """tcgen05 kernel, every MMA width, partial and full batches, stream-K grids
-    of 1, 7 and all SMs (split tiles, ragged N and K tails)."""
+@pytest.mark.parametrize("NT,tile_k", [(16, 64), (16, 128), (16, 256), (32, 64), (32, 256), (64, 64),
+                                       (64, 128), (128, 64), (128, 128), (256, 64)])
+def test_tc_parity_vs_oracle(dep, orc, plan_cache, N, K, NT, tile_k):
+    """tcgen05 kernel, every MMA width, 1, 2 or 4 slices of 64 columns per stage,
+    partial and full batches, stream-K grids of 1, 7 and all SMs (split tiles,
+    ragged N and K tails)."""
     plan = get_plan(dep, plan_cache, N, K, (256,))
     W = synth.normal_bf16(N + NT, 1, (N, K), sigma=0.02)
+    stages = {64: 4 if NT < 256 else 3, 128: 2 if NT >= 128 else 3, 256: 2}[tile_k]
     for B in sorted({1, min(NT, 5), NT}):
         x = synth.normal_bf16(B + NT, 2, (B, K))
         ref = orc.linear(x, W)
         for ctas in (1, 7, sm_count()):
-            y = run(dep, plan, x, W, N, tc_tactic(dep, NT, ctas, 4 if NT < 256 else 3))
+            y = run(dep, plan, x, W, N, tc_tactic(dep, NT, ctas, stages, tile_k))
             ok, worst, idx = within_tolerance(y, ref)
             assert ok, (B, ctas, worst, idx)
     assert dep.dep_projection_device_status(plan) == 0
