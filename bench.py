@@ -51,7 +51,7 @@ WORKLOAD_TEXT = {
 }
 # Workloads whose plan is tuned by default (the verify-step tables are measured).
 TUNED_BY_DEFAULT = {"dsa_verify"}
-KERNEL_SOURCES = ["splitk_fma.cu", "tc_gemm.cu", "ptx.cuh", "internal.h"]
+KERNEL_SOURCES = ["splitk_fma.cu", "tc_gemm.cu", "rows_gemv.cu", "ptx.cuh", "internal.h"]
 
 
 def parse_args():
@@ -263,6 +263,8 @@ def kernel_name(t) -> str:
     import skinny_bf16_split_gb300 as dep
     if t.kind == dep.DEP_KIND_SPLITK_FMA:
         return f"splitk_fma_c{t.cols}"
+    if t.kind == dep.DEP_KIND_ROWS:
+        return f"rows_gemv_c{t.cols}"
     return f"tc_gemm_n{t.cols}"
 
 

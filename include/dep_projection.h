@@ -67,6 +67,8 @@ typedef enum {
 /* Tactic kinds. */
 #define DEP_KIND_SPLITK_FMA 1 /* warp split-K on the FP32 FMA pipe, TMA-staged W */
 #define DEP_KIND_TC 2         /* tcgen05 MMA, TMEM accumulators, TMA-staged W and x */
+#define DEP_KIND_ROWS 3       /* warp split-K over whole weight rows, dynamic tiles, no
+                                 cross-block fix-up; x resident in shared memory */
 
 /* One table entry: the tactic that serves batches of up to max_rows rows. */
 typedef struct {
@@ -76,7 +78,7 @@ typedef struct {
     int32_t tile_n;   /* weight rows per tile */
     int32_t tile_k;   /* reduction columns per pipeline stage */
     int32_t stages;   /* pipeline depth (shared-memory stages) */
-    int32_t cols;     /* batch rows per pass (FMA: x rows held; TC: MMA N) */
+    int32_t cols;     /* batch rows per pass (FMA/ROWS: x rows held; TC: MMA N) */
 } dep_tactic_t;
 
 /* Plan flags. */

@@ -27,6 +27,7 @@ DEP_ERR_IO = 8
 
 DEP_KIND_SPLITK_FMA = 1
 DEP_KIND_TC = 2
+DEP_KIND_ROWS = 3
 DEP_PLAN_DEFAULT = 0
 DEP_PLAN_TUNE = 1
 DEP_PLAN_PDL = 2

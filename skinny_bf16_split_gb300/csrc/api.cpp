@@ -75,18 +75,26 @@ bool tactic_valid(const dep_tactic_t &t)
         return dep::fma_valid(t);
     if (t.kind == DEP_KIND_TC)
         return dep::tc_valid(t);
+    if (t.kind == DEP_KIND_ROWS)
+        return dep::rows_valid(t);
     return false;
 }
 
 size_t ws_per_cta(const dep_tactic_t &t)
 {
-    return t.kind == DEP_KIND_SPLITK_FMA ? dep::fma_ws_per_cta(t) : dep::tc_ws_per_cta(t);
+    switch (t.kind) {
+    case DEP_KIND_SPLITK_FMA: return dep::fma_ws_per_cta(t);
+    case DEP_KIND_TC: return dep::tc_ws_per_cta(t);
+    default: return 0;  // the whole-row tactic has no split-K partials
+    }
 }
 
-// Blocks a launch really uses: never more than the stream-K work units.
+// Blocks a launch really uses: never more than the work units (stream-K) or tiles.
 int64_t effective_ctas(const dep_tactic_t &t, int64_t N, int64_t K)
 {
-    const int64_t U = t.kind == DEP_KIND_SPLITK_FMA ? dep::fma_units(t, N, K) : dep::tc_units(t, N, K);
+    const int64_t U = t.kind == DEP_KIND_SPLITK_FMA ? dep::fma_units(t, N, K)
+                      : t.kind == DEP_KIND_TC       ? dep::tc_units(t, N, K)
+                                                    : dep::rows_tiles(t, N);
     return U < t.ctas ? U : t.ctas;
 }
 
@@ -98,7 +106,11 @@ size_t tactic_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K)
 
 size_t tactic_counters(const dep_tactic_t &t, int64_t N)
 {
-    return t.kind == DEP_KIND_SPLITK_FMA ? dep::fma_counters(t, N) : dep::tc_counters(t, N);
+    switch (t.kind) {
+    case DEP_KIND_SPLITK_FMA: return dep::fma_counters(t, N);
+    case DEP_KIND_TC: return dep::tc_counters(t, N);
+    default: return 2;  // tile dispenser and finish count (the last two counters)
+    }
 }
 
 constexpr int32_t kFmaMaxRows = 4;  // default split point between the two kernels
@@ -115,6 +127,19 @@ dep_tactic_t fma_tactic(int32_t rows, int32_t cols, int32_t stages, int sm_count
     t.stages = stages;
     int per_sm = host_only ? 1 : dep::fma_blocks_per_sm(t);
     t.ctas = sm_count * (per_sm < 1 ? 1 : per_sm);
+    return t;
+}
+
+dep_tactic_t rows_tactic(int32_t rows, int32_t cols, int32_t tile_n, int32_t tile_k, int32_t stages, int32_t ctas)
+{
+    dep_tactic_t t{};
+    t.max_rows = rows;
+    t.kind = DEP_KIND_ROWS;
+    t.cols = cols;
+    t.tile_n = tile_n;
+    t.tile_k = tile_k;
+    t.stages = stages;
+    t.ctas = ctas;
     return t;
 }
 
@@ -146,8 +171,18 @@ int32_t tc_default_stages(int32_t cols)
 // where the FMA pipe stops keeping up with HBM on this GPU).  The tensor-core
 // kernel runs one block per 128-row tile when the tiles nearly fill the GPU,
 // and the even stream-K split otherwise.
-dep_tactic_t default_tactic(int32_t rows, int64_t N, int sm_count, bool host_only)
+dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count, bool host_only)
 {
+    if (rows <= 2) {
+        // Whole rows, no cross-block split: 16-row tiles, 4 stages of 1024
+        // columns, handed out dynamically (measured on GB300: 5-8 % faster than
+        // the stream-K FMA kernel at one x row, on all three weights).  Falls
+        // back to the FMA kernel where x does not fit in shared memory.
+        const int32_t cols = pow2_at_least(rows);
+        const dep_tactic_t t = rows_tactic(rows, cols, 16, 1024, 4, sm_count);
+        if (dep::rows_fits(t, K))
+            return t;
+    }
     if (rows <= kFmaMaxRows) {
         // 64-row tiles (each x value reused over 8 rows per warp), 4 stages of
         // 32-34 KB; 6 stages for four x rows.  Measured on GB300 against 32-row
@@ -298,7 +333,7 @@ dep_status_t make_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_b
         }
     }
     for (int32_t b : bs)
-        p->table.push_back(default_tactic(b, N, p->sm_count, host_only));
+        p->table.push_back(default_tactic(b, N, K, p->sm_count, host_only));
     sort_table(p->table);
     if (!host_only) {
         st = allocate_device(p);
@@ -355,7 +390,11 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
     a.stream = static_cast<cudaStream_t>(stream);
     a.wait_limit_ns = p->wait_limit_ns;
     a.pdl = p->pdl;
-    cudaError_t e = t->kind == DEP_KIND_SPLITK_FMA ? dep::fma_run(*t, a) : dep::tc_run(*t, a);
+    if (t->kind == DEP_KIND_ROWS && !dep::rows_fits(*t, p->K))
+        return DEP_ERR_UNSUPPORTED;  // x and the ring do not fit in shared memory for this K
+    cudaError_t e = t->kind == DEP_KIND_SPLITK_FMA ? dep::fma_run(*t, a)
+                    : t->kind == DEP_KIND_TC       ? dep::tc_run(*t, a)
+                                                   : dep::rows_run(*t, a);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return DEP_ERR_CUDA;
@@ -377,7 +416,7 @@ __global__ void fill_bf16_kernel(uint16_t *p, size_t n, uint64_t seed)
     }
 }
 
-std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int sm_count)
+std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_count)
 {
     std::vector<dep_tactic_t> c;
     if (rows <= 8) {
@@ -385,6 +424,13 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int sm_count)
         for (int32_t tn : {32, 64})
             for (int32_t st : {4, 6, 8})
                 c.push_back(fma_tactic(rows, cols, st, sm_count, false, tn));
+    }
+    if (rows <= 4) {
+        const int32_t cols = pow2_at_least(rows);
+        for (int32_t tn : {8, 16})
+            for (int32_t kc : {1024, 2048, 4096})
+                for (int32_t st : {2, 3, 4, 6})
+                    c.push_back(rows_tactic(rows, cols, tn, kc, st, sm_count));
     }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128;
@@ -396,7 +442,7 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int sm_count)
         }
     std::vector<dep_tactic_t> ok;
     for (const auto &t : c)
-        if (tactic_valid(t))
+        if (tactic_valid(t) && (t.kind != DEP_KIND_ROWS || dep::rows_fits(t, K)))
             ok.push_back(t);
     return ok;
 }
@@ -410,7 +456,7 @@ dep_status_t tune_plan(dep_plan_s *p)
     size_t ws_need = 0, cnt_need = 0;
     int32_t rows_max = 1;
     for (const auto &t : p->table) {
-        cands.push_back(candidates(t.max_rows, p->N, p->sm_count));
+        cands.push_back(candidates(t.max_rows, p->N, p->K, p->sm_count));
         for (const auto &c : cands.back()) {
             ws_need = std::max(ws_need, tactic_ws_floats(c, p->N, p->K));
             cnt_need = std::max(cnt_need, tactic_counters(c, p->N));

@@ -126,6 +126,13 @@ size_t tc_counters(const dep_tactic_t &t, int64_t N);
 int tc_blocks_per_sm(const dep_tactic_t &t);
 cudaError_t tc_run(const dep_tactic_t &t, const RunArgs &a);
 
+// ---- whole-row tactic (rows_gemv.cu) ----
+bool rows_valid(const dep_tactic_t &t);
+bool rows_fits(const dep_tactic_t &t, int64_t K);  // x and the ring fit in shared memory
+int64_t rows_tiles(const dep_tactic_t &t, int64_t N);
+int rows_blocks_per_sm(const dep_tactic_t &t, int64_t K);
+cudaError_t rows_run(const dep_tactic_t &t, const RunArgs &a);  // uses the last 2 counters
+
 // ---- TMA descriptors (tma.cpp) ----
 // 2-D BF16 tensor map over a row-major [outer, inner] array with a row pitch of
 // `inner` elements; box = [box_outer rows, box_inner elements]; out-of-range

@@ -54,9 +54,11 @@ def test_default_table_follows_split_rule(dep):
         assert [t.max_rows for t in table] == [1, 2, 4, 8, 16]
         for t in table:
             assert t.ctas >= 152 and t.stages >= 2
-            assert t.kind in (dep.DEP_KIND_SPLITK_FMA, dep.DEP_KIND_TC)
-            if t.max_rows <= 4:
-                assert t.kind == dep.DEP_KIND_SPLITK_FMA
+            assert t.kind in (dep.DEP_KIND_SPLITK_FMA, dep.DEP_KIND_TC, dep.DEP_KIND_ROWS)
+            if t.max_rows <= 4:  # small batches: warp split-K on the FMA pipe
+                assert t.kind in (dep.DEP_KIND_SPLITK_FMA, dep.DEP_KIND_ROWS)
+            else:
+                assert t.kind == dep.DEP_KIND_TC
         for B, key in [(1, 1), (3, 4), (5, 8), (16, 16), (17, 16), (1000, 16)]:
             assert dep.dep_projection_plan_query(plan, B).max_rows == key
     finally:
@@ -102,8 +104,8 @@ def test_host_plan_cannot_run(dep):
 def test_plan_set_validates_and_inserts(dep):
     plan = dep.dep_projection_plan_host(7168, 12288, [1, 16], 152)
     try:
-        t = dep.dep_projection_plan_query(plan, 1)
-        t.max_rows, t.cols, t.tile_n, t.stages = 3, 4, 64, 3
+        t = dep.dep_tactic_t(max_rows=3, kind=dep.DEP_KIND_SPLITK_FMA, ctas=152, tile_n=64, tile_k=256,
+                             stages=3, cols=4)
         dep.dep_projection_plan_set(plan, t)
         assert [x.max_rows for x in dep.dep_projection_plan_table(plan)] == [1, 3, 16]
         assert dep.dep_projection_plan_query(plan, 2).cols == 4

@@ -438,3 +438,104 @@ def test_pdl_chain_respects_data_dependencies(dep, B):
     finally:
         dep.dep_projection_plan_destroy(plain)
         dep.dep_projection_plan_destroy(pdl)
+
+
+def test_host_fault_injection(dep, monkeypatch):
+    """Failures are made on the host (no GPU fault): a forced allocation failure
+    gives DEP_ERR_OOM and no plan; a forced launch failure gives DEP_ERR_CUDA
+    and launches nothing; clearing the switch restores normal runs."""
+    monkeypatch.setenv("DEP_FAULT", "alloc")
+    with pytest.raises(dep.DepError) as e:
+        dep.dep_projection_plan(256, 512, [1, 16])
+    assert e.value.status == dep.DEP_ERR_OOM
+    monkeypatch.setenv("DEP_FAULT", "launch")
+    plan = dep.dep_projection_plan(256, 512, [1, 16])
+    try:
+        x = torch.ones(4, 512, dtype=torch.bfloat16, device="cuda")
+        W = torch.ones(256, 512, dtype=torch.bfloat16, device="cuda")
+        y = torch.full((4, 256), 7.0, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(dep.DepError) as e:
+            dep.dep_projection_run(plan, x, W, y, 4)
+        assert e.value.status == dep.DEP_ERR_CUDA
+        torch.cuda.synchronize()
+        assert bool((y == 7.0).all())
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+    monkeypatch.delenv("DEP_FAULT")
+    plan = dep.dep_projection_plan(256, 512, [1, 16])
+    try:
+        dep.dep_projection_run(plan, x, W, y, 4)
+        torch.cuda.synchronize()
+        assert bool((y == 512.0).all())
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+def test_plan_file_for_another_gpu_is_refused(dep, tmp_path):
+    """A table tuned on a GPU with another SM count is not applied here."""
+    path = tmp_path / "other.txt"
+    path.write_text("dep_projection_plan 1\ndevice other\nsms 999\nshape 256 512\nentries 1\n"
+                    "1 1 999 64 256 4 1\n")
+    with pytest.raises(dep.DepError) as e:
+        dep.dep_projection_plan_load(str(path), 256, 512)
+    assert e.value.status == dep.DEP_ERR_UNSUPPORTED
+
+
+# ---------------- whole-row tactic (no cross-block split) ----------------
+
+def rows_tactic(dep, cols, tile_n, tile_k, stages, ctas):
+    return dep.dep_tactic_t(max_rows=cols, kind=dep.DEP_KIND_ROWS, ctas=ctas, tile_n=tile_n,
+                            tile_k=tile_k, stages=stages, cols=cols)
+
+
+def rows_fits(cols, tile_n, tile_k, stages, K):
+    """Shared memory of the whole-row kernel: x (padded to 256 columns) + ring + barriers."""
+    kpad = -(-K // 256) * 256
+    return cols * kpad * 2 + stages * tile_n * tile_k * 2 + (3 * stages + 1) * 8 <= 227 * 1024
+
+
+@pytest.mark.parametrize("N,K", [(333, 3000), (64, 256), (97, 264), (1, 8), (1000, 1032), (130, 4104)])
+@pytest.mark.parametrize("cols,tile_n", [(1, 8), (1, 16), (2, 8), (2, 16), (4, 8), (4, 16)])
+@pytest.mark.parametrize("tile_k,stages", [(1024, 2), (2048, 3), (4096, 2)])
+def test_rows_bitexact_vs_mirror(dep, orc, plan_cache, N, K, cols, tile_n, tile_k, stages):
+    """Every output is summed by one warp over all of K, whatever block takes its
+    tile: the result equals the mirror's order for a tile owned whole (a grid of
+    one block), bit for bit, for grids of 1, 7 and 152 blocks and more blocks
+    than tiles."""
+    if not rows_fits(cols, tile_n, tile_k, stages, K):
+        pytest.skip("ring and x exceed shared memory")
+    B = {1: 1, 2: 2, 4: 3}[cols]
+    x = synth.normal_bf16(N + cols + tile_n, 2, (B, K))
+    W = synth.normal_bf16(N + tile_k, 1, (N, K), sigma=0.02)
+    plan = get_plan(dep, plan_cache, N, K)
+    want = orc.mirror_fma(x, W, 1, 64)
+    for ctas in (1, 7, 152, 1000):
+        y = run(dep, plan, x, W, N, rows_tactic(dep, cols, tile_n, tile_k, stages, ctas))
+        np.testing.assert_array_equal(y, want)
+    assert dep.dep_projection_device_status(plan) == 0
+
+
+def test_rows_wide_batch_and_oracle(dep, orc, plan_cache):
+    """B larger than the tactic's x rows runs in passes; within tolerance of the oracle."""
+    N, K, B = 777, 2048, 11
+    x = synth.normal_bf16(31, 2, (B, K))
+    W = synth.normal_bf16(31, 1, (N, K), sigma=0.02)
+    y = run(dep, get_plan(dep, plan_cache, N, K), x, W, N, rows_tactic(dep, 4, 16, 2048, 3, 152))
+    np.testing.assert_array_equal(y, orc.mirror_fma(x, W, 1, 64))
+    ok, worst, idx = within_tolerance(y, orc.linear(x, W))
+    assert ok, (worst, idx)
+
+
+def test_rows_refuses_when_x_does_not_fit(dep):
+    """x stays in shared memory: a K too long for it is refused, not run."""
+    N, K = 8, 65536
+    plan = dep.dep_projection_plan(N, K, [4])
+    try:
+        x = torch.zeros(4, K, dtype=torch.bfloat16, device="cuda")
+        W = torch.zeros(N, K, dtype=torch.bfloat16, device="cuda")
+        y = torch.zeros(4, N, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(dep.DepError) as e:
+            dep.dep_projection_run_tactic(plan, rows_tactic(dep, 4, 8, 2048, 2, 152), x, W, y, 4)
+        assert e.value.status == dep.DEP_ERR_UNSUPPORTED
+    finally:
+        dep.dep_projection_plan_destroy(plan)
