@@ -47,11 +47,13 @@ WORKLOAD_TEXT = {
     "dsa_verify": "verify-step batches on the DSA input projection: x[B,7168] . W[14560,7168]^T, "
                   "B = requests x q in {3,6,12,24,48}, seeds 0..4, tuned plan",
     "tp_sharded": "TP-G shards at B=16: DSA input projection rows 14560/G x 7168 and o_proj "
-                  "7168 x 12288/G for G in {2,4,8}, seeds 0..5",
+                  "7168 x 12288/G for G in {2,4,8}, seeds 0..5, tuned plan",
 }
 # Workloads whose plan is tuned by default (the verify-step tables are measured).
-TUNED_BY_DEFAULT = {"dsa_verify"}
-KERNEL_SOURCES = ["splitk_fma.cu", "tc_gemm.cu", "rows_gemv.cu", "ptx.cuh", "internal.h"]
+TUNED_BY_DEFAULT = {"dsa_verify", "tp_sharded"}
+# Sources each kernel family is built from (a traffic record is stale once they change).
+KERNEL_SOURCES = {"splitk_fma": ["splitk_fma.cu"], "tc_gemm": ["tc_gemm.cu"], "rows_gemv": ["rows_gemv.cu"]}
+SHARED_SOURCES = ["ptx.cuh", "internal.h"]
 
 
 def parse_args():
@@ -78,13 +80,20 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
-def source_hash() -> str:
+def source_hash(family: str | None = None) -> str:
+    """Hash of a kernel family's sources (all families when None)."""
+    names = ([n for v in KERNEL_SOURCES.values() for n in v] if family is None
+             else KERNEL_SOURCES[family]) + SHARED_SOURCES
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in names:
         p = os.path.join(ROOT, "skinny_bf16_split_gb300", "csrc", name)
         if os.path.exists(p):
             h.update(open(p, "rb").read())
     return h.hexdigest()[:16]
+
+
+def kernel_family(kernel: str) -> str:
+    return next(f for f in KERNEL_SOURCES if kernel.startswith(f))
 
 
 def read_peaks():
@@ -105,7 +114,7 @@ def read_traffic(kernel: str, workload: str):
         fields = dict(line.split(":", 1) for line in open(path) if ":" in line)
     except OSError:
         return None
-    if fields.get("source_sha", "").strip() != source_hash():
+    if fields.get("source_sha", "").strip() != source_hash(kernel_family(kernel)):
         return None
     try:
         return float(fields["dram_bytes_per_launch"])

@@ -434,12 +434,16 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
     }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128;
+    // Grids: every SM (stream-K), and for weights with fewer 128-row tiles than
+    // SMs also one, two and four blocks per tile (less splitting, fewer partials).
+    std::vector<int32_t> grids{sm_count};
+    for (int64_t per : {1, 2, 4})
+        if (per * tiles < sm_count)
+            grids.push_back((int32_t)(per * tiles));
     for (int32_t tk : {64, 128, 256})
-        for (int32_t st : {2, 3, 4, 6, 8, 10, 12}) {
-            c.push_back(tc_tactic(rows, cols, st, sm_count, tk));
-            if (tiles < sm_count)
-                c.push_back(tc_tactic(rows, cols, st, (int32_t)tiles, tk));
-        }
+        for (int32_t st : {2, 3, 4, 6, 8, 10, 12})
+            for (int32_t g : grids)
+                c.push_back(tc_tactic(rows, cols, st, g, tk));
     std::vector<dep_tactic_t> ok;
     for (const auto &t : c)
         if (tactic_valid(t) && (t.kind != DEP_KIND_ROWS || dep::rows_fits(t, K)))
