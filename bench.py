@@ -80,6 +80,25 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def reduce_max(value: float) -> float:
+    """The largest `value` over all ranks (the value itself when not distributed).
+    Works on the NCCL (CUDA tensor) and gloo (CPU tensor) backends."""
+    import torch
+    import torch.distributed as tdist
+    if not (tdist.is_available() and tdist.is_initialized()) or tdist.get_world_size() == 1:
+        return float(value)
+    device = "cuda" if tdist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, elapsed_ms: float) -> float:
+    """Throughput of the whole job: the bytes every rank moved over the slowest
+    rank's time (each rank runs the same workload: weak scaling)."""
+    return bytes_per_step * steps * world / (elapsed_ms * 1e-3) / 1e9
+
+
 def source_hash(family: str | None = None) -> str:
     """Hash of a kernel family's sources (all families when None)."""
     names = ([n for v in KERNEL_SOURCES.values() for n in v] if family is None
@@ -357,12 +376,8 @@ def run_ours(args):
         code = dep.dep_projection_device_status(p)
         if code:
             raise RuntimeError(f"a kernel reported device status {code}")
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-
-    value = bytes_per_step * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    elapsed_ms = reduce_max(elapsed_ms)
+    value = whole_job_gbs(bytes_per_step, args.steps, world, elapsed_ms)
     peak, peak_src = read_peaks()
 
     # per-kernel totals over the timed region; the dominant kernel's roofline
@@ -463,18 +478,14 @@ def run_graph_pdl(args, dep, calls, x_dev, W_dev, y_dev, device, world, flags):
         graph.replay()
     t1.record(cur)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(t0.elapsed_time(t1))
     for p in plans.values():
         code = dep.dep_projection_device_status(p)
         if code:
             raise RuntimeError(f"a kernel reported device status {code}")
         dep.dep_projection_plan_destroy(p)
     bytes_per_step = sum(c.algorithmic_bytes for c in calls)
-    return {"value": bytes_per_step * args.steps * world / (ms * 1e-3) / 1e9, "unit": UNIT,
+    return {"value": whole_job_gbs(bytes_per_step, args.steps, world, ms), "unit": UNIT,
             "ms_per_step": ms / args.steps,
             "how": "one step captured as a CUDA graph, kernels chained by programmatic dependent "
                    "launch (DEP_PLAN_PDL), K replays timed by events"}
@@ -511,13 +522,9 @@ def run_e2e(args, dep, calls, plans, xs_host, W_dev, device, world):
         step()
     t_end.record(stream)
     torch.cuda.synchronize()
-    ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(t_start.elapsed_time(t_end))
     bytes_per_step = sum(c.algorithmic_bytes for c in calls)
-    return {"value": bytes_per_step * steps * world / (ms * 1e-3) / 1e9, "unit": UNIT,
+    return {"value": whole_job_gbs(bytes_per_step, steps, world, ms), "unit": UNIT,
             "h2d_bytes_per_step": sum(2 * c.B * c.K for c in calls),
             "d2h_bytes_per_step": sum(2 * c.B * c.N for c in calls),
             "ms_per_step": ms / steps, "api": "dep_projection_run_host"}

@@ -331,6 +331,12 @@ dep_status_t make_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_b
             delete p;
             return DEP_ERR_UNSUPPORTED;
         }
+        if (dep::fma_prepare_device() != cudaSuccess || dep::tc_prepare_device() != cudaSuccess ||
+            dep::rows_prepare_device() != cudaSuccess) {
+            cudaGetLastError();
+            delete p;
+            return DEP_ERR_CUDA;
+        }
     }
     for (int32_t b : bs)
         p->table.push_back(default_tactic(b, N, K, p->sm_count, host_only));

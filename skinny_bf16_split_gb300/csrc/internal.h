@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/dep_projection.h"
 
 namespace dep {
@@ -29,6 +31,35 @@ struct RunArgs {
     // waiting for that grid (the weight must not be written by preceding work).
     bool pdl = false;
 };
+
+// Shared memory a block of any kernel here may use (the sm_100-family opt-in maximum).
+constexpr int kMaxDynamicSmem = 227 * 1024;
+
+// Raise a kernel's dynamic shared-memory limit on the current device, once per
+// device (the attribute belongs to the device's context).  `devices` is the
+// kernel's own record of the devices already done (one bit per device < 64).
+template <typename Kernel>
+cudaError_t set_smem_attr(Kernel kernel, std::atomic<uint64_t> &devices)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0;
+    if (bit && (devices.load(std::memory_order_acquire) & bit))
+        return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+    if (e == cudaSuccess && bit)
+        devices.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
+// Set the attribute of every kernel instantiation on the current device
+// (called when a plan is made, so that no first launch happens inside a
+// stream capture).
+cudaError_t fma_prepare_device();
+cudaError_t tc_prepare_device();
+cudaError_t rows_prepare_device();
 
 // Launch with the programmatic-stream-serialisation attribute when `pdl` is set.
 template <typename Kernel, typename... Args>

@@ -36,7 +36,7 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kSub = 256;  // columns per lane sweep: 32 lanes x 8
-constexpr size_t kMaxSmem = 227 * 1024;
+constexpr size_t kMaxSmem = kMaxDynamicSmem;
 
 // 1-D bulk copy global -> shared, completion on an mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
@@ -277,9 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BC, int RW>
 cudaError_t prepare()
 {
-    static cudaError_t once = cudaFuncSetAttribute(rows_gemv_kernel<BC, RW>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
-    return once;
+    static std::atomic<uint64_t> devices{0};
+    return set_smem_attr(rows_gemv_kernel<BC, RW>, devices);
 }
 
 template <typename F>
@@ -331,6 +330,19 @@ int rows_blocks_per_sm(const dep_tactic_t &t, int64_t K)
             n = 0;
     });
     return n;
+}
+
+cudaError_t rows_prepare_device()
+{
+    cudaError_t e = cudaSuccess;
+    for (int cols : {1, 2, 4})
+        for (int tn : {8, 16})
+            with_rows_shape(cols, tn, [&](auto bc, auto rw) {
+                const cudaError_t r = prepare<decltype(bc)::value, decltype(rw)::value>();
+                if (r != cudaSuccess)
+                    e = r;
+            });
+    return e;
 }
 
 cudaError_t rows_run(const dep_tactic_t &t, const RunArgs &a)

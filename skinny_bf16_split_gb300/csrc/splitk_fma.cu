@@ -278,14 +278,13 @@ size_t smem_bytes(int stages)
     return (size_t)stages * S::STAGE_BYTES + 2 * (size_t)stages * sizeof(uint64_t);
 }
 
-constexpr size_t kMaxSmem = 227 * 1024;
+constexpr size_t kMaxSmem = kMaxDynamicSmem;
 
 template <class S>
 cudaError_t prepare()
 {
-    static cudaError_t once = cudaFuncSetAttribute(
-        splitk_fma_kernel<S::BC, S::TN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
-    return once;
+    static std::atomic<uint64_t> devices{0};
+    return set_smem_attr(splitk_fma_kernel<S::BC, S::TN>, devices);
 }
 
 // Call f with the Shape of (cols, tile rows); false if this build has no such kernel.
@@ -379,6 +378,19 @@ int fma_blocks_per_sm(const dep_tactic_t &t)
             n = 0;
     });
     return n;
+}
+
+cudaError_t fma_prepare_device()
+{
+    cudaError_t e = cudaSuccess;
+    for (int cols : {1, 2, 4, 8})
+        for (int tn : {32, 64})
+            with_shape(cols, tn, [&](auto sh) {
+                const cudaError_t r = prepare<decltype(sh)>();
+                if (r != cudaSuccess)
+                    e = r;
+            });
+    return e;
 }
 
 cudaError_t fma_run(const dep_tactic_t &t, const RunArgs &a)

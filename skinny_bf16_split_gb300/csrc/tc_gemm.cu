@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-constexpr size_t kMaxSmem = 227 * 1024;
+constexpr size_t kMaxSmem = kMaxDynamicSmem;
 
 template <int NT>
 size_t smem_bytes(int stages, int atoms)
@@ -348,9 +348,8 @@ size_t smem_bytes(int stages, int atoms)
 template <int NT>
 cudaError_t prepare()
 {
-    static cudaError_t once = cudaFuncSetAttribute(
-        tc_gemm_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMaxSmem);
-    return once;
+    static std::atomic<uint64_t> devices{0};
+    return set_smem_attr(tc_gemm_kernel<NT>, devices);
 }
 
 template <int NT>
@@ -446,6 +445,14 @@ int tc_blocks_per_sm(const dep_tactic_t &t)
     case 256: return blocks_per_sm<256>(t.stages, atoms);
     default: return 0;
     }
+}
+
+cudaError_t tc_prepare_device()
+{
+    for (cudaError_t e : {prepare<16>(), prepare<32>(), prepare<64>(), prepare<128>(), prepare<256>()})
+        if (e != cudaSuccess)
+            return e;
+    return cudaSuccess;
 }
 
 cudaError_t tc_run(const dep_tactic_t &t, const RunArgs &a)
