@@ -181,6 +181,16 @@ dep_status_t dep_projection_plan_table(dep_plan_t plan, dep_tactic_t *out, int32
  * validated and the split-K workspace must already be large enough for it. */
 dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic);
 
+/*
+ * Inspection: copy the plan's split-K partial area (FP32) to host memory after
+ * synchronising the device; *written = bytes copied (at most `bytes`).  Layout
+ * for a stream-K launch of C blocks: partial (block c, slot s, batch column j,
+ * tile row r) at float index ((c * 2 + s) * cols + j) * tile_n + r, slot 0 for
+ * the block's first tile and 1 for its last.  Lets a test re-add the partials of
+ * every split tile in block order and check the kernel's fix-up bit for bit.
+ */
+dep_status_t dep_projection_plan_partials(dep_plan_t plan, void *host, size_t bytes, size_t *written);
+
 /* Bytes of device workspace the plan owns (split-K partials, counters, status). */
 dep_status_t dep_projection_plan_workspace(dep_plan_t plan, size_t *bytes);
 

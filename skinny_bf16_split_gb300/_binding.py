@@ -45,6 +45,7 @@ EXPORTS = (
     "dep_projection_plan_save", "dep_projection_plan_load", "dep_projection_plan_destroy",
     "dep_projection_device_status", "dep_projection_selftest_timeout", "dep_bins_index",
     "dep_status_string", "dep_projection_version", "dep_projection_run_static",
+    "dep_projection_plan_partials",
 )
 
 
@@ -99,6 +100,7 @@ def lib():
         "dep_status_string": ([i32], ctypes.c_char_p),
         "dep_projection_version": ([], i32),
         "dep_projection_run_static": ([vp, vp, vp, i64, i64, i32, vp], i32),
+        "dep_projection_plan_partials": ([vp, vp, ctypes.c_size_t, P(ctypes.c_size_t)], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -211,6 +213,16 @@ def dep_projection_plan_workspace(plan) -> int:
     b = ctypes.c_size_t()
     _check(lib().dep_projection_plan_workspace(plan, ctypes.byref(b)), "dep_projection_plan_workspace")
     return b.value
+
+
+def dep_projection_plan_partials(plan, count: int):
+    """The first `count` FP32 split-K partials of the plan's workspace (numpy)."""
+    import numpy as np
+    out = np.empty(count, dtype=np.float32)
+    n = ctypes.c_size_t()
+    _check(lib().dep_projection_plan_partials(plan, out.ctypes.data, out.nbytes, ctypes.byref(n)),
+           "dep_projection_plan_partials")
+    return out[: n.value // 4]
 
 
 def dep_projection_plan_save(plan, path: str) -> None:

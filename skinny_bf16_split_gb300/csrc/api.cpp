@@ -686,6 +686,23 @@ dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic
     return DEP_OK;
 }
 
+dep_status_t dep_projection_plan_partials(dep_plan_t plan, void *host, size_t bytes, size_t *written)
+{
+    if (!plan || !written || (bytes && !host))
+        return DEP_ERR_INVALID_ARG;
+    *written = 0;
+    if (plan->host_only)
+        return DEP_ERR_UNSUPPORTED;
+    const size_t n = std::min(bytes, plan->ws_floats * sizeof(float));
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        (n && cudaMemcpy(host, plan->ws, n, cudaMemcpyDeviceToHost) != cudaSuccess)) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    *written = n;
+    return DEP_OK;
+}
+
 dep_status_t dep_projection_plan_workspace(dep_plan_t plan, size_t *bytes)
 {
     if (!plan || !bytes)

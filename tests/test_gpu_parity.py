@@ -539,3 +539,47 @@ def test_rows_refuses_when_x_does_not_fit(dep):
         assert e.value.status == dep.DEP_ERR_UNSUPPORTED
     finally:
         dep.dep_projection_plan_destroy(plan)
+
+
+def _stream_k_segments(U, C, KT, t):
+    """Blocks whose ranges meet tile t's units, and their slot for t (stream-K split)."""
+    begin = lambda c: c * U // C  # noqa: E731
+    owner = lambda u: ((u + 1) * C - 1) // U  # noqa: E731
+    c0, c1 = owner(t * KT), owner(t * KT + KT - 1)
+    return [(c, 0 if begin(c) // KT == t else 1) for c in range(c0, c1 + 1)]
+
+
+@pytest.mark.parametrize("NT,B,tile_k", [(16, 16, 256), (16, 5, 64), (32, 24, 128), (64, 64, 128)])
+def test_tc_fixup_bitexact_from_partials(dep, plan_cache, NT, B, tile_k):
+    """The tensor cores' own summation order is not documented, but the split-K
+    combination is the library's: for every tile split across blocks, the FP32
+    partials the blocks left in the workspace, added in increasing block order
+    and rounded to BF16 (nearest, ties to even), give y bit for bit."""
+    N, K = 1000, 4096
+    plan = get_plan(dep, plan_cache, N, K, (256,))
+    x = synth.normal_bf16(40 + NT, 2, (B, K))
+    W = synth.normal_bf16(41, 1, (N, K), sigma=0.02)
+    C = sm_count()
+    y = run(dep, plan, x, W, N, tc_tactic(dep, NT, C, 3, tile_k))
+    T, KT = -(-N // 128), -(-K // tile_k)
+    U = T * KT
+    C = min(C, U)
+    ws = dep.dep_projection_plan_partials(plan, C * 2 * NT * 128)
+    assert ws.size == C * 2 * NT * 128
+    checked = 0
+    for t in range(T):
+        segs = _stream_k_segments(U, C, KT, t)
+        if len(segs) < 2:
+            continue  # a whole tile: written straight from its accumulator
+        rows = np.arange(128)
+        n = t * 128 + rows
+        keep = n < N
+        for b in range(B):
+            s = None
+            for c, slot in segs:
+                p = ws[((c * 2 + slot) * NT + b) * 128 + rows].astype(np.float32)
+                s = p if s is None else (s + p).astype(np.float32)
+            want = synth.bf16_from_f64(s.astype(np.float64))  # float32 -> float64 is exact
+            np.testing.assert_array_equal(y[b, n[keep]], want[keep])
+            checked += int(keep.sum())
+    assert checked > 0
