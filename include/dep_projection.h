@@ -69,16 +69,22 @@ typedef enum {
 #define DEP_KIND_TC 2         /* tcgen05 MMA, TMEM accumulators, TMA-staged W and x */
 #define DEP_KIND_ROWS 3       /* warp split-K over whole weight rows, dynamic tiles, no
                                  cross-block fix-up; x resident in shared memory */
+#define DEP_KIND_TC_SPLIT 4   /* tcgen05 MMA over (128-row tile, K piece) items taken
+                                 dynamically; each tile cut into `splits` fixed K pieces
+                                 whose FP32 partials are added in piece order */
 
 /* One table entry: the tactic that serves batches of up to max_rows rows. */
 typedef struct {
     int32_t max_rows; /* table key (binning rule above) */
     int32_t kind;     /* DEP_KIND_* */
-    int32_t ctas;     /* persistent blocks launched (work split evenly: stream-K) */
+    int32_t ctas;     /* persistent blocks launched (FMA/TC: work split evenly,
+                         stream-K; ROWS/TC_SPLIT: work items taken dynamically) */
     int32_t tile_n;   /* weight rows per tile */
     int32_t tile_k;   /* reduction columns per pipeline stage */
     int32_t stages;   /* pipeline depth (shared-memory stages) */
     int32_t cols;     /* batch rows per pass (FMA/ROWS: x rows held; TC: MMA N) */
+    int32_t splits;   /* TC_SPLIT: K pieces per tile, 1..64 (capped at the tile's
+                         k-tiles, ceil(K / tile_k)); 0 for the other kinds */
 } dep_tactic_t;
 
 /* Plan flags. */
@@ -178,7 +184,9 @@ dep_status_t dep_projection_plan_table(dep_plan_t plan, dep_tactic_t *out, int32
                                        int32_t *n);
 
 /* Replace (or insert) the table entry with key tactic->max_rows.  The tactic is
- * validated and the split-K workspace must already be large enough for it. */
+ * validated (INVALID_ARG if not); if it needs more workspace, counters or
+ * staging than the plan owns, the plan's device block is re-allocated (after a
+ * device synchronisation; OOM leaves the plan unchanged). */
 dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic);
 
 /*
@@ -186,8 +194,11 @@ dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic
  * synchronising the device; *written = bytes copied (at most `bytes`).  Layout
  * for a stream-K launch of C blocks: partial (block c, slot s, batch column j,
  * tile row r) at float index ((c * 2 + s) * cols + j) * tile_n + r, slot 0 for
- * the block's first tile and 1 for its last.  Lets a test re-add the partials of
- * every split tile in block order and check the kernel's fix-up bit for bit.
+ * the block's first tile and 1 for its last.  For a K-piece launch (TC_SPLIT,
+ * S pieces in effect): partial (tile t, piece p, batch column j, tile row r) at
+ * float index ((t * S + p) * cols + j) * 128 + r.  Lets a test re-add the
+ * partials of every split tile in block or piece order and check the kernel's
+ * fix-up bit for bit.
  */
 dep_status_t dep_projection_plan_partials(dep_plan_t plan, void *host, size_t bytes, size_t *written);
 
@@ -196,7 +207,9 @@ dep_status_t dep_projection_plan_workspace(dep_plan_t plan, size_t *bytes);
 
 /*
  * Save the table as text keyed by (device name, SM count, N, K), and load it
- * back onto the current device (tuning need not be repeated).  Load checks the
+ * back onto the current device (tuning need not be repeated).  Files are
+ * written in format 2 (eight fields per entry); format 1 files (seven fields,
+ * no K pieces) still load.  Load checks the
  * shape (INVALID_ARG if it differs) and the SM count (UNSUPPORTED if the file
  * was made for another GPU).  Errors: IO for unreadable or malformed files.
  */

@@ -28,6 +28,7 @@ DEP_ERR_IO = 8
 DEP_KIND_SPLITK_FMA = 1
 DEP_KIND_TC = 2
 DEP_KIND_ROWS = 3
+DEP_KIND_TC_SPLIT = 4
 DEP_PLAN_DEFAULT = 0
 DEP_PLAN_TUNE = 1
 DEP_PLAN_PDL = 2
@@ -51,7 +52,7 @@ EXPORTS = (
 
 class dep_tactic_t(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int32) for name in
-                ("max_rows", "kind", "ctas", "tile_n", "tile_k", "stages", "cols")]
+                ("max_rows", "kind", "ctas", "tile_n", "tile_k", "stages", "cols", "splits")]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

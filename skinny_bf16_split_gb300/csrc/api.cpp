@@ -71,6 +71,10 @@ bool tactic_valid(const dep_tactic_t &t)
 {
     if (t.max_rows < 1)
         return false;
+    if (t.kind == DEP_KIND_TC_SPLIT)
+        return dep::tcs_valid(t);
+    if (t.splits != 0)
+        return false;  // only the K-piece tactic has pieces
     if (t.kind == DEP_KIND_SPLITK_FMA)
         return dep::fma_valid(t);
     if (t.kind == DEP_KIND_TC)
@@ -85,7 +89,10 @@ size_t ws_per_cta(const dep_tactic_t &t)
     switch (t.kind) {
     case DEP_KIND_SPLITK_FMA: return dep::fma_ws_per_cta(t);
     case DEP_KIND_TC: return dep::tc_ws_per_cta(t);
-    default: return 0;  // the whole-row tactic has no split-K partials
+    // K pieces size their partials per item (tactic_ws_floats); the plan still
+    // keeps room for the stream-K kernel of the same MMA width (headroom rule).
+    case DEP_KIND_TC_SPLIT: return dep::tc_ws_per_cta(t);
+    default: return 0;  // whole rows: no partials
     }
 }
 
@@ -101,6 +108,8 @@ int64_t effective_ctas(const dep_tactic_t &t, int64_t N, int64_t K)
 // Split-K partial floats a launch of tactic t on an [N,K] weight may write.
 size_t tactic_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K)
 {
+    if (t.kind == DEP_KIND_TC_SPLIT)
+        return dep::tcs_ws_floats(t, N, K);
     return (size_t)effective_ctas(t, N, K) * ws_per_cta(t);
 }
 
@@ -109,6 +118,7 @@ size_t tactic_counters(const dep_tactic_t &t, int64_t N)
     switch (t.kind) {
     case DEP_KIND_SPLITK_FMA: return dep::fma_counters(t, N);
     case DEP_KIND_TC: return dep::tc_counters(t, N);
+    case DEP_KIND_TC_SPLIT: return dep::tcs_counters(t, N);
     default: return 2;  // tile dispenser and finish count (the last two counters)
     }
 }
@@ -156,6 +166,14 @@ dep_tactic_t tc_tactic(int32_t rows, int32_t cols, int32_t stages, int32_t ctas,
     return t;
 }
 
+dep_tactic_t tcs_tactic(int32_t rows, int32_t cols, int32_t stages, int32_t ctas, int32_t tile_k, int32_t splits)
+{
+    dep_tactic_t t = tc_tactic(rows, cols, stages, ctas, tile_k);
+    t.kind = DEP_KIND_TC_SPLIT;
+    t.splits = splits;
+    return t;
+}
+
 // Deepest pipeline of the tensor-core kernel that fits in shared memory.
 int32_t tc_default_stages(int32_t cols)
 {
@@ -192,6 +210,19 @@ dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count, bo
     }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128;
+    if (2 * tiles <= sm_count) {
+        // At most half as many 128-row tiles as SMs (o_proj: 56): cut every tile
+        // into SMs / tiles fixed K pieces, one dynamically taken item per block,
+        // instead of stream-K segments (measured on GB300 for o_proj at 8 and 16
+        // rows, 2 pieces: 1 us per call faster).
+        const int32_t splits = (int32_t)std::min<int64_t>(64, sm_count / tiles);
+        for (int32_t tk : {256, 128})
+            for (int32_t st : {6, 5, 4, 3}) {
+                const dep_tactic_t t = tcs_tactic(rows, cols, st, sm_count, tk, splits);
+                if (dep::tcs_valid(t))
+                    return t;
+            }
+    }
     const int32_t ctas = (tiles <= sm_count && 4 * tiles >= 3 * (int64_t)sm_count) ? (int32_t)tiles : sm_count;
     // Widest stage (most contiguous bytes per weight row) that still leaves a
     // ring of at least three stages; 64-column stages for the widest batches.
@@ -240,8 +271,8 @@ dep_status_t allocate_device(dep_plan_s *p, size_t extra_ws_floats = 0, size_t e
     const size_t status_b = 256, cnt_b = up(cnt * sizeof(int)), ws_b = up(ws * sizeof(float));
     const size_t xs_b = up((size_t)rows * p->K * 2), ys_b = up((size_t)rows * p->N * 2);
     const size_t total = status_b + cnt_b + ws_b + xs_b + ys_b;
-    if (p->dev_block && total <= p->dev_bytes)
-        return DEP_OK;
+    if (p->dev_block && cnt <= p->n_counters && ws <= p->ws_floats && rows <= p->stage_rows)
+        return DEP_OK;  // the current block already has room for every part
     if (env_is("DEP_FAULT", "alloc"))
         return DEP_ERR_OOM;
     void *blk = nullptr;
@@ -332,6 +363,7 @@ dep_status_t make_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_b
             return DEP_ERR_UNSUPPORTED;
         }
         if (dep::fma_prepare_device() != cudaSuccess || dep::tc_prepare_device() != cudaSuccess ||
+            dep::tcs_prepare_device() != cudaSuccess ||
             dep::rows_prepare_device() != cudaSuccess) {
             cudaGetLastError();
             delete p;
@@ -400,6 +432,7 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
         return DEP_ERR_UNSUPPORTED;  // x and the ring do not fit in shared memory for this K
     cudaError_t e = t->kind == DEP_KIND_SPLITK_FMA ? dep::fma_run(*t, a)
                     : t->kind == DEP_KIND_TC       ? dep::tc_run(*t, a)
+                    : t->kind == DEP_KIND_TC_SPLIT ? dep::tcs_run(*t, a)
                                                    : dep::rows_run(*t, a);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -450,9 +483,22 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
         for (int32_t st : {2, 3, 4, 6, 8, 10, 12})
             for (int32_t g : grids)
                 c.push_back(tc_tactic(rows, cols, st, g, tk));
+    // Fixed K pieces taken dynamically: 1 to 8 pieces per tile, and as many as
+    // give one item per SM.
+    std::vector<int32_t> pieces{1, 2, 3, 4, 8};
+    if (tiles < sm_count && std::find(pieces.begin(), pieces.end(), (int32_t)(sm_count / tiles)) == pieces.end())
+        pieces.push_back((int32_t)std::min<int64_t>(64, sm_count / tiles));
+    for (int32_t tk : {128, 256})
+        for (int32_t st : {3, 4, 6})
+            for (int32_t sp : pieces)
+                c.push_back(tcs_tactic(rows, cols, st, sm_count, tk, sp));
+    // K pieces keep every piece's partial: leave out tactics whose partials
+    // would take more than 64 MB of workspace.
+    constexpr size_t kMaxPieceWorkspaceFloats = (64u << 20) / sizeof(float);
     std::vector<dep_tactic_t> ok;
     for (const auto &t : c)
-        if (tactic_valid(t) && (t.kind != DEP_KIND_ROWS || dep::rows_fits(t, K)))
+        if (tactic_valid(t) && (t.kind != DEP_KIND_ROWS || dep::rows_fits(t, K)) &&
+            (t.kind != DEP_KIND_TC_SPLIT || tactic_ws_floats(t, N, K) <= kMaxPieceWorkspaceFloats))
             ok.push_back(t);
     return ok;
 }
@@ -672,17 +718,25 @@ dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic
 {
     if (!plan || !tactic || !tactic_valid(*tactic))
         return DEP_ERR_INVALID_ARG;
-    if (!plan->host_only && (tactic_ws_floats(*tactic, plan->N, plan->K) > plan->ws_floats ||
-                             tactic_counters(*tactic, plan->N) > plan->n_counters ||
-                             tactic->max_rows > plan->stage_rows))
-        return DEP_ERR_INVALID_ARG;
+    const std::vector<dep_tactic_t> old = plan->table;
+    bool replaced = false;
     for (auto &t : plan->table)
         if (t.max_rows == tactic->max_rows) {
             t = *tactic;
-            return DEP_OK;
+            replaced = true;
         }
-    plan->table.push_back(*tactic);
-    sort_table(plan->table);
+    if (!replaced) {
+        plan->table.push_back(*tactic);
+        sort_table(plan->table);
+    }
+    if (!plan->host_only) {
+        // Grow the workspace if the new entry needs more (synchronises the device).
+        const dep_status_t st = allocate_device(plan);
+        if (st != DEP_OK) {
+            plan->table = old;
+            return st;
+        }
+    }
     return DEP_OK;
 }
 
@@ -722,12 +776,12 @@ dep_status_t dep_projection_plan_save(dep_plan_t plan, const char *path)
     for (char &ch : name)
         if (ch == ' ' || ch == '\t' || ch == '\n')
             ch = '_';
-    int ok = std::fprintf(f, "dep_projection_plan 1\ndevice %s\nsms %d\nshape %lld %lld\nentries %zu\n",
+    int ok = std::fprintf(f, "dep_projection_plan 2\ndevice %s\nsms %d\nshape %lld %lld\nentries %zu\n",
                           name.c_str(), plan->sm_count, (long long)plan->N, (long long)plan->K,
                           plan->table.size()) > 0;
     for (const auto &t : plan->table)
-        ok = ok && std::fprintf(f, "%d %d %d %d %d %d %d\n", t.max_rows, t.kind, t.ctas, t.tile_n,
-                                t.tile_k, t.stages, t.cols) > 0;
+        ok = ok && std::fprintf(f, "%d %d %d %d %d %d %d %d\n", t.max_rows, t.kind, t.ctas, t.tile_n,
+                                t.tile_k, t.stages, t.cols, t.splits) > 0;
     ok = (std::fclose(f) == 0) && ok;
     return ok ? DEP_OK : DEP_ERR_IO;
 }
@@ -749,12 +803,12 @@ dep_status_t dep_projection_plan_load(const char *path, int64_t N, int64_t K, de
     std::vector<dep_tactic_t> table;
     bool ok = std::fscanf(f, "dep_projection_plan %d device %511s sms %d shape %lld %lld entries %zu",
                           &version, name, &sms, &fn, &fk, &count) == 6 &&
-              version == 1 && count >= 1 && count <= 4096;
+              (version == 1 || version == 2) && count >= 1 && count <= 4096;
     for (size_t i = 0; ok && i < count; ++i) {
-        dep_tactic_t t{};
+        dep_tactic_t t{};  // version 1 files predate the K-piece field (0)
         ok = std::fscanf(f, "%d %d %d %d %d %d %d", &t.max_rows, &t.kind, &t.ctas, &t.tile_n,
                          &t.tile_k, &t.stages, &t.cols) == 7 &&
-             tactic_valid(t);
+             (version == 1 || std::fscanf(f, "%d", &t.splits) == 1) && tactic_valid(t);
         table.push_back(t);
     }
     std::fclose(f);

@@ -60,6 +60,7 @@ cudaError_t set_smem_attr(Kernel kernel, std::atomic<uint64_t> &devices)
 cudaError_t fma_prepare_device();
 cudaError_t tc_prepare_device();
 cudaError_t rows_prepare_device();
+cudaError_t tcs_prepare_device();
 
 // Launch with the programmatic-stream-serialisation attribute when `pdl` is set.
 template <typename Kernel, typename... Args>
@@ -156,6 +157,13 @@ size_t tc_ws_per_cta(const dep_tactic_t &t);
 size_t tc_counters(const dep_tactic_t &t, int64_t N);
 int tc_blocks_per_sm(const dep_tactic_t &t);
 cudaError_t tc_run(const dep_tactic_t &t, const RunArgs &a);
+
+// ---- tcgen05 tactic with fixed K pieces, dynamically scheduled (tc_split.cu) ----
+bool tcs_valid(const dep_tactic_t &t);
+size_t tcs_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K);  // every piece's partial
+size_t tcs_counters(const dep_tactic_t &t, int64_t N);               // includes the last 2 counters
+int tcs_blocks_per_sm(const dep_tactic_t &t);
+cudaError_t tcs_run(const dep_tactic_t &t, const RunArgs &a);       // uses the last 2 counters
 
 // ---- whole-row tactic (rows_gemv.cu) ----
 bool rows_valid(const dep_tactic_t &t);

@@ -1,0 +1,516 @@
+// tc_split.cu -- tcgen05 tactic with a fixed K split and dynamic scheduling.
+//
+// Computes y[B,N] = BF16(x[B,K] . W[N,K]^T), BF16 products accumulated in FP32
+// (runtime.hybrid page, HybridAttention.__init__: past the split-K rows the
+// projection runs the stock FP32-accumulated BF16 GEMM; runtime.dep page,
+// DepProjection), like the stream-K tensor-core tactic, with another schedule:
+//
+//  * Each 128-row weight tile is cut into S fixed pieces along K (piece p
+//    covers k-tiles [p KT / S, (p+1) KT / S)).  A work item is one (tile,
+//    piece) pair; item i is tile i / S, piece i % S.
+//  * Blocks take items dynamically: item blockIdx.x first, then the next free
+//    item from an integer counter, so a block that streams faster takes more
+//    items and the blocks finish together (a static split ends when its
+//    slowest block does).  The last block to finish taking items resets the
+//    counter for the next launch.
+//  * Swap-AB MMAs as in the stream-K kernel: M = 128 weight rows, N = the batch
+//    padded to NT, K = 16 per instruction; 128-byte-swizzled TMA stages of
+//    tile_k / 64 slices; accumulators in TMEM, two buffers of NT columns.
+//  * Every piece's FP32 partial goes to its own workspace slot [item][b][row];
+//    the last epilogue warp to arrive on the tile's integer counter adds the S
+//    partials in piece order 0..S-1 and rounds to BF16.  Which block ran which
+//    piece does not enter the arithmetic, so results are identical from run to
+//    run and equal to BF16 of the ordered FP32 sum of the pieces.  With S = 1 a
+//    tile is one item and y is stored directly (no workspace, no counter).
+//  * Warp roles: warp 0 TMA producer (takes the items), warp 1 TMEM owner and
+//    MMA issuer, warps 2-5 epilogue.  The producer tags each stage with its item
+//    and first/last flags; the MMA issuer passes the item of each finished
+//    accumulator to the epilogue through a tag slot and its own mbarrier.
+//  * Every wait is bounded in time; on a give-up the block records a code, lets
+//    every role finish, waits for its MMAs and copies, and frees TMEM.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dep {
+namespace {
+
+constexpr int kBM = 128;      // weight rows per tile (MMA M)
+constexpr int kBK = 64;       // columns per slice: one 128-byte swizzle row
+constexpr int kUmmaK = 16;    // K of one kind::f16 MMA
+constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA/TMEM, warps 2-5 epilogue
+constexpr int kEpiWarps = 4;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB weight slice
+constexpr int kMaxSplits = 64;
+
+template <int NT>
+struct SplitShape {
+    static constexpr int B_BYTES = NT * kBK * 2;
+    static constexpr int ATOM = kABytes + B_BYTES;
+    static constexpr uint32_t TMEM_COLS = 2 * NT < 32 ? 32 : 2 * NT;
+};
+
+// Shared memory after the 1 KB-aligned ring: full[stages], empty[stages],
+// accf[2], acce[2], tagb[2], done; then the stage tags, the accumulator items,
+// the TMEM address and the abort flag.
+__host__ __device__ inline size_t split_smem_bytes(int stages, int stage_bytes)
+{
+    return 1024 + (size_t)stages * stage_bytes + (size_t)(2 * stages + 7) * 8 + (size_t)stages * 8 + 16;
+}
+
+__device__ __forceinline__ int piece_begin(int p, int KT, int S)
+{
+    return (int)(((int64_t)p * KT) / S);
+}
+
+__device__ __forceinline__ uint16_t to_bf16(float v)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_split_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                    uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms, int S,
+                    float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ dispenser,
+                    int *__restrict__ status, uint64_t limit_ns)
+{
+    using Sh = SplitShape<NT>;
+    const int STAGE = atoms * Sh::ATOM;
+    const int KG = atoms * kBK;  // columns per k-tile (one stage)
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles need 1 KB alignment
+    uint8_t *smem = smem_raw + (base - raw);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * STAGE);
+    const uint32_t full0 = smem_u32(bars);
+    const uint32_t empty0 = full0 + 8 * stages;
+    const uint32_t accf0 = empty0 + 8 * stages;  // accumulator final, 2 buffers
+    const uint32_t acce0 = accf0 + 16;           // accumulator drained, 2 buffers
+    const uint32_t tagb0 = acce0 + 16;           // accumulator's item published, 2 buffers
+    const uint32_t done = tagb0 + 16;            // all MMAs complete
+    int2 *tags = reinterpret_cast<int2 *>(bars + 2 * stages + 7);  // (item, flags); item < 0: end
+    volatile int *acc_item = reinterpret_cast<volatile int *>(tags + stages);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tags + stages) + 2;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int T = (N + kBM - 1) / kBM, KT = (K + KG - 1) / KG, I = T * S;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int *grab = dispenser, *finished = dispenser + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, kEpiWarps);
+            mbar_init(tagb0 + 8 * b, 1);
+        }
+        mbar_init(done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        griddep_launch_dependents();
+    }
+    if (warp == 1) {
+        tc::alloc(smem_u32(tmem_slot), Sh::TMEM_COLS);
+        tc::relinquish();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- TMA producer: takes the items ----------------
+        if (lane == 0) {
+            prefetch_tmap(&tmW);
+            prefetch_tmap(&tmX);
+            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
+            int item = blockIdx.x;  // the grid never exceeds the item count
+            int tile = item / S, kt = piece_begin(item % S, KT, S), kt_end = piece_begin(item % S + 1, KT, S);
+            auto stage_addr = [&](int st) { return base + (uint32_t)(st * STAGE); };
+            auto issue_w = [&](int st) {
+                const int flags = (kt == piece_begin(item % S, KT, S) ? 1 : 0) | (kt == kt_end - 1 ? 2 : 0);
+                tags[st] = make_int2(item, flags);
+                mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)STAGE);
+                for (int a = 0; a < atoms; ++a)
+                    tma_load_2d(stage_addr(st) + (uint32_t)(a * kABytes), &tmW, kt * KG + a * kBK, tile * kBM,
+                                full0 + 8 * st, pol_w);
+            };
+            auto issue_x = [&](int st, int k_tile) {
+                const uint32_t xs = stage_addr(st) + (uint32_t)(atoms * kABytes);
+                for (int a = 0; a < atoms; ++a)
+                    tma_load_2d(xs + (uint32_t)(a * Sh::B_BYTES), &tmX, k_tile * KG + a * kBK, 0, full0 + 8 * st,
+                                pol_x);
+            };
+            // Phase 1: the weight is not written by preceding work -- fill the ring
+            // with the first k-tiles of the first item, then wait for the
+            // preceding grid before reading x or the item counter.
+            const int kt0 = kt;
+            const int pre = (kt_end - kt) < stages ? (kt_end - kt) : stages;
+            for (int i = 0; i < pre; ++i, ++kt)
+                issue_w(i);
+            griddep_wait();
+            for (int i = 0; i < pre; ++i)
+                issue_x(i, kt0 + i);
+            int s = pre % stages;
+            uint32_t ph = pre == stages ? 1u : 0u;
+            int64_t issued = pre;
+            bool ok = true;
+            for (;;) {
+                if (kt == kt_end) {  // the item is fully issued: take the next one
+                    item = (int)gridDim.x + atomicAdd(grab, 1);
+                    if (item < I) {
+                        tile = item / S;
+                        kt = piece_begin(item % S, KT, S);
+                        kt_end = piece_begin(item % S + 1, KT, S);
+                    }
+                }
+                if (*abort_flag) {
+                    ok = false;
+                    break;
+                }
+                if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, limit_ns)) {
+                    record_status(status, DEP_DEV_TIMEOUT_PRODUCER);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                if (item >= I) {  // end of the stream: an empty stage tagged -1
+                    tags[s] = make_int2(-1, 0);
+                    mbar_arrive(full0 + 8 * s);
+                    break;
+                }
+                issue_w(s);
+                issue_x(s, kt);
+                ++kt;
+                ++issued;
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            // Drain: walk back over the most recent fills from stage s.  After an
+            // end marker stage s holds the marker, so at most stages - 1 copies can
+            // still be in flight; after a give-up, stage s was never refilled.
+            const int64_t cap = ok ? stages - 1 : stages;
+            const int64_t n = issued < cap ? issued : cap;
+            int ds = s;
+            uint32_t dph = ph;
+            for (int64_t i = 0; i < n; ++i) {
+                if (--ds < 0) {
+                    ds = stages - 1;
+                    dph ^= 1u;
+                }
+                if (!mbar_wait(full0 + 8 * ds, dph, limit_ns))
+                    record_status(status, DEP_DEV_TIMEOUT_PRODUCER);
+            }
+            // The last block to finish taking items resets the counter.
+            if (atomicAdd(finished, 1) == (int)gridDim.x - 1) {
+                *grab = 0;
+                *finished = 0;
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, NT);
+            int s = 0, buf = 0;
+            uint32_t ph = 0, acce_ph = 0;
+            uint32_t accumulate = 0;
+            for (;;) {
+                if (!mbar_wait(full0 + 8 * s, ph, limit_ns)) {
+                    record_status(status, DEP_DEV_TIMEOUT_MMA);
+                    *abort_flag = 1;
+                    break;
+                }
+                tc::fence_after();
+                const int2 tag = tags[s];
+                if (tag.x < 0 || (tag.y & 1)) {
+                    // A new item (or the end): take accumulator buffer `buf` once the
+                    // epilogue has drained its previous use.
+                    if (!mbar_wait(acce0 + 8 * buf, ((acce_ph >> buf) & 1u) ^ 1u, limit_ns)) {
+                        record_status(status, DEP_DEV_TIMEOUT_MMA);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    acce_ph ^= 1u << buf;
+                    tc::fence_after();
+                    accumulate = 0;
+                }
+                if (tag.x < 0) {  // hand the end marker to the epilogue
+                    acc_item[buf] = -1;
+                    mbar_arrive(tagb0 + 8 * buf);
+                    break;
+                }
+                const uint32_t d = tmem + (uint32_t)(buf * NT);
+                const uint32_t st = base + (uint32_t)(s * STAGE);
+                for (int a = 0; a < atoms; ++a) {
+                    const uint64_t ad = tc::desc_sw128(st + (uint32_t)(a * kABytes));
+                    const uint64_t bd = tc::desc_sw128(st + (uint32_t)(atoms * kABytes + a * Sh::B_BYTES));
+#pragma unroll
+                    for (int j = 0; j < kBK / kUmmaK; ++j) {
+                        // advance along K inside the 128-byte swizzle row: 32 bytes per step
+                        const uint64_t off = (uint64_t)((j * kUmmaK * 2) >> 4);
+                        tc::mma_bf16(d, ad + off, bd + off, idesc, accumulate);
+                        accumulate = 1;
+                    }
+                }
+                tc::commit(empty0 + 8 * s);  // the stage is free once these MMAs finish
+                if (++s == stages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                if (tag.y & 2) {  // the item's last k-tile: publish the accumulator
+                    acc_item[buf] = tag.x;
+                    tc::commit(accf0 + 8 * buf);
+                    mbar_arrive(tagb0 + 8 * buf);
+                    buf ^= 1;
+                }
+            }
+            tc::commit(done);  // TMEM is freed at the end: wait for every MMA
+            if (!mbar_wait(done, 0, limit_ns))
+                record_status(status, DEP_DEV_TIMEOUT_MMA);
+        }
+    } else {
+        // ---------------- epilogue warps ----------------
+        griddep_wait();  // workspace, counters and y may still be in use by the preceding grid
+        const int q = warp & 3;  // TMEM lane quadrant this warp may access
+        const int row = 32 * q + lane;
+        uint32_t tag_ph = 0, accf_ph = 0;
+        int buf = 0;
+        for (;;) {
+            if (!mbar_wait(tagb0 + 8 * buf, (tag_ph >> buf) & 1u, limit_ns)) {
+                record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
+                *abort_flag = 1;
+                break;
+            }
+            tag_ph ^= 1u << buf;
+            const int item = acc_item[buf];
+            if (item < 0)
+                break;
+            if (!mbar_wait(accf0 + 8 * buf, (accf_ph >> buf) & 1u, limit_ns)) {
+                record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
+                *abort_flag = 1;
+                break;
+            }
+            accf_ph ^= 1u << buf;
+            tc::fence_after();
+            const int t = item / S;
+            const int64_t n = (int64_t)t * kBM + row;
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NT);
+            float *part = ws + (int64_t)item * NT * kBM + row;
+#pragma unroll 1
+            for (int c0 = 0; c0 < NT; c0 += 16) {
+                uint32_t v[16];
+                tc::ld16(taddr + (uint32_t)c0, v);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int b = c0 + j;
+                    if (b < B) {
+                        const float f = __uint_as_float(v[j]);
+                        if (S == 1) {
+                            if (n < N)
+                                y[(int64_t)b * N + n] = to_bf16(f);
+                        } else {
+                            __stcg(part + (int64_t)b * kBM, f);
+                        }
+                    }
+                }
+            }
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(acce0 + 8 * buf);
+            buf ^= 1;
+            if (S == 1)
+                continue;
+            __threadfence();
+            __syncwarp();
+            int prev = 0;
+            if (lane == 0)
+                prev = atomicAdd(&counters[t * kEpiWarps + q], 1);
+            prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
+            if (prev != S - 1)
+                continue;  // another piece of this tile is still running
+            __threadfence();
+            if (n < N) {
+                // Sum the pieces in order 0..S-1; the loads of up to 4 pieces x 16
+                // batch columns are issued together, then added.
+                const float *tile_ws = ws + (int64_t)t * S * NT * kBM + row;
+                for (int b0 = 0; b0 < B; b0 += 16) {
+                    float sum[16];
+                    for (int p0 = 0; p0 < S; p0 += 4) {
+                        float pv[4][16];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float *src = tile_ws + ((int64_t)(p0 + i) * NT + b0) * kBM;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                pv[i][j] = (p0 + i < S && b0 + j < B) ? __ldcg(src + (int64_t)j * kBM) : 0.0f;
+                        }
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (p0 + i < S)
+                                    sum[j] = (p0 + i == 0) ? pv[i][j] : sum[j] + pv[i][j];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (b0 + j < B)
+                            y[(int64_t)(b0 + j) * N + n] = to_bf16(sum[j]);
+                }
+            }
+            if (lane == 0)
+                counters[t * kEpiWarps + q] = 0;  // ready for the next launch
+        }
+    }
+
+    __syncwarp();
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after();
+        tc::dealloc(tmem, Sh::TMEM_COLS);
+    }
+}
+
+template <int NT>
+size_t smem_bytes(int stages, int atoms)
+{
+    return split_smem_bytes(stages, atoms * SplitShape<NT>::ATOM);
+}
+
+template <int NT>
+cudaError_t prepare()
+{
+    static std::atomic<uint64_t> devices{0};
+    return set_smem_attr(tc_split_kernel<NT>, devices);
+}
+
+// Pieces actually used: never more than the k-tiles of a tile (no empty piece).
+int64_t effective_splits(const dep_tactic_t &t, int64_t K)
+{
+    const int64_t KT = (K + t.tile_k - 1) / t.tile_k;
+    return t.splits < KT ? t.splits : KT;
+}
+
+template <int NT>
+cudaError_t run_nt(const dep_tactic_t &t, const RunArgs &a)
+{
+    cudaError_t e = prepare<NT>();
+    if (e != cudaSuccess)
+        return e;
+    CUtensorMap tmW, tmX;
+    if (encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) !=
+        CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    const int atoms = t.tile_k / kBK;
+    const int S = (int)effective_splits(t, a.K);
+    const int64_t items = ((a.N + kBM - 1) / kBM) * S;
+    const int grid = (int)(items < t.ctas ? items : t.ctas);
+    const size_t smem = smem_bytes<NT>(t.stages, atoms);
+    int *dispenser = a.counters + a.n_counters - 2;
+    for (int32_t r0 = 0; r0 < a.B; r0 += NT) {
+        const int32_t rows = a.B - r0 < NT ? a.B - r0 : NT;
+        if (encode_bf16_2d(&tmX, a.x + (size_t)r0 * a.K, (uint64_t)a.K, (uint64_t)rows, kBK, NT,
+                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        e = launch(tc_split_kernel<NT>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
+                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, S, a.ws, a.counters,
+                   dispenser, a.status, a.wait_limit_ns);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
+template <int NT>
+int blocks_per_sm(int stages, int atoms)
+{
+    if (prepare<NT>() != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_split_kernel<NT>, kThreads,
+                                                      smem_bytes<NT>(stages, atoms)) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+size_t smem_for(const dep_tactic_t &t)
+{
+    const int atoms = t.tile_k / kBK;
+    switch (t.cols) {
+    case 16: return smem_bytes<16>(t.stages, atoms);
+    case 32: return smem_bytes<32>(t.stages, atoms);
+    case 64: return smem_bytes<64>(t.stages, atoms);
+    case 128: return smem_bytes<128>(t.stages, atoms);
+    case 256: return smem_bytes<256>(t.stages, atoms);
+    default: return 0;
+    }
+}
+
+}  // namespace
+
+bool tcs_valid(const dep_tactic_t &t)
+{
+    if (t.kind != DEP_KIND_TC_SPLIT || t.ctas < 1 || t.tile_n != kBM)
+        return false;
+    if (t.tile_k != kBK && t.tile_k != 2 * kBK && t.tile_k != 4 * kBK)
+        return false;  // 1, 2 or 4 slices of 64 columns per stage
+    if (t.stages < 2 || t.stages > 16 || t.splits < 1 || t.splits > kMaxSplits)
+        return false;
+    const size_t smem = smem_for(t);
+    return smem != 0 && smem <= (size_t)kMaxDynamicSmem;
+}
+
+size_t tcs_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K)
+{
+    const int64_t S = effective_splits(t, K);
+    return S > 1 ? (size_t)((N + kBM - 1) / kBM) * (size_t)S * (size_t)t.cols * kBM : 0;
+}
+
+size_t tcs_counters(const dep_tactic_t &, int64_t N)
+{
+    return (size_t)((N + kBM - 1) / kBM) * kEpiWarps + 2;  // + the item counter pair at the end
+}
+
+int tcs_blocks_per_sm(const dep_tactic_t &t)
+{
+    const int atoms = t.tile_k / kBK;
+    switch (t.cols) {
+    case 16: return blocks_per_sm<16>(t.stages, atoms);
+    case 32: return blocks_per_sm<32>(t.stages, atoms);
+    case 64: return blocks_per_sm<64>(t.stages, atoms);
+    case 128: return blocks_per_sm<128>(t.stages, atoms);
+    case 256: return blocks_per_sm<256>(t.stages, atoms);
+    default: return 0;
+    }
+}
+
+cudaError_t tcs_prepare_device()
+{
+    for (cudaError_t e : {prepare<16>(), prepare<32>(), prepare<64>(), prepare<128>(), prepare<256>()})
+        if (e != cudaSuccess)
+            return e;
+    return cudaSuccess;
+}
+
+cudaError_t tcs_run(const dep_tactic_t &t, const RunArgs &a)
+{
+    switch (t.cols) {
+    case 16: return run_nt<16>(t, a);
+    case 32: return run_nt<32>(t, a);
+    case 64: return run_nt<64>(t, a);
+    case 128: return run_nt<128>(t, a);
+    case 256: return run_nt<256>(t, a);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace dep

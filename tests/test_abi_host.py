@@ -54,11 +54,12 @@ def test_default_table_follows_split_rule(dep):
         assert [t.max_rows for t in table] == [1, 2, 4, 8, 16]
         for t in table:
             assert t.ctas >= 152 and t.stages >= 2
-            assert t.kind in (dep.DEP_KIND_SPLITK_FMA, dep.DEP_KIND_TC, dep.DEP_KIND_ROWS)
+            assert t.kind in (dep.DEP_KIND_SPLITK_FMA, dep.DEP_KIND_TC, dep.DEP_KIND_ROWS,
+                              dep.DEP_KIND_TC_SPLIT)
             if t.max_rows <= 4:  # small batches: warp split-K on the FMA pipe
                 assert t.kind in (dep.DEP_KIND_SPLITK_FMA, dep.DEP_KIND_ROWS)
-            else:
-                assert t.kind == dep.DEP_KIND_TC
+            else:  # 56 tiles of 128 rows on 152 SMs: two K pieces per tile
+                assert (t.kind, t.splits) == (dep.DEP_KIND_TC_SPLIT, 2)
         for B, key in [(1, 1), (3, 4), (5, 8), (16, 16), (17, 16), (1000, 16)]:
             assert dep.dep_projection_plan_query(plan, B).max_rows == key
     finally:
@@ -68,7 +69,10 @@ def test_default_table_follows_split_rule(dep):
 def test_default_batches_when_none_given(dep):
     plan = dep.dep_projection_plan_host(14560, 7168, [], 152)
     try:
-        assert [t.max_rows for t in dep.dep_projection_plan_table(plan)] == [1, 2, 4, 8, 16, 32, 64, 128, 256]
+        table = dep.dep_projection_plan_table(plan)
+        assert [t.max_rows for t in table] == [1, 2, 4, 8, 16, 32, 64, 128, 256]
+        # 114 tiles of 128 rows nearly fill 152 SMs: one stream-K block per tile
+        assert all((t.kind, t.ctas) == (dep.DEP_KIND_TC, 114) for t in table if t.max_rows > 4)
     finally:
         dep.dep_projection_plan_destroy(plan)
 
@@ -128,11 +132,12 @@ def test_plan_save_format(dep, tmp_path):
         path = str(tmp_path / "plan.txt")
         dep.dep_projection_plan_save(plan, path)
         lines = open(path).read().split("\n")
-        assert lines[0] == "dep_projection_plan 1"
+        assert lines[0] == "dep_projection_plan 2"
         assert lines[2] == "sms 152" and lines[3] == "shape 49376 7168" and lines[4] == "entries 4"
         rows = [list(map(int, l.split())) for l in lines[5:9]]
         table = dep.dep_projection_plan_table(plan)
-        assert rows == [[t.max_rows, t.kind, t.ctas, t.tile_n, t.tile_k, t.stages, t.cols] for t in table]
+        assert rows == [[t.max_rows, t.kind, t.ctas, t.tile_n, t.tile_k, t.stages, t.cols, t.splits]
+                        for t in table]
     finally:
         dep.dep_projection_plan_destroy(plan)
 
@@ -152,3 +157,31 @@ def test_status_strings(dep):
     for s in range(0, 9):
         assert dep.dep_status_string(s)
     assert dep.dep_status_string(1234) == "unknown status"
+
+
+def test_k_piece_tactic_validation_and_save(dep, tmp_path):
+    """The K-piece tensor-core kind: 1..64 pieces, 128-row tiles, 1/2/4 slices
+    of 64 columns per stage; the piece count is rejected on every other kind and
+    is written as the eighth field of a plan file entry."""
+    plan = dep.dep_projection_plan_host(7168, 12288, [1, 16], 152)
+    try:
+        t = dep.dep_tactic_t(max_rows=16, kind=dep.DEP_KIND_TC_SPLIT, ctas=152, tile_n=128, tile_k=256,
+                             stages=3, cols=16, splits=8)
+        dep.dep_projection_plan_set(plan, t)
+        q = dep.dep_projection_plan_query(plan, 9)
+        assert (q.kind, q.splits, q.tile_k) == (dep.DEP_KIND_TC_SPLIT, 8, 256)
+        for field, value in (("splits", 0), ("splits", 65), ("tile_n", 64), ("tile_k", 192),
+                             ("stages", 1), ("cols", 24), ("stages", 12)):
+            bad = dep.dep_tactic_t(**{**t.as_dict(), field: value})
+            with pytest.raises(dep.DepError):
+                dep.dep_projection_plan_set(plan, bad)
+        fma = dep.dep_tactic_t(max_rows=3, kind=dep.DEP_KIND_SPLITK_FMA, ctas=152, tile_n=64, tile_k=256,
+                               stages=4, cols=4, splits=2)
+        with pytest.raises(dep.DepError):
+            dep.dep_projection_plan_set(plan, fma)
+        path = str(tmp_path / "plan.txt")
+        dep.dep_projection_plan_save(plan, path)
+        entries = [list(map(int, l.split())) for l in open(path).read().split("\n")[5:] if l]
+        assert [16, dep.DEP_KIND_TC_SPLIT, 152, 128, 256, 3, 16, 8] in entries
+    finally:
+        dep.dep_projection_plan_destroy(plan)

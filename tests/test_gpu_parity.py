@@ -323,13 +323,23 @@ def test_tc_parity_vs_oracle(dep, orc, plan_cache, N, K, NT, tile_k):
 
 
 @pytest.mark.parametrize("B", [5, 16, 64])
-def test_tc_determinism_and_graph_replay(dep, plan_cache, B):
-    """The tensor-core kernel's split-K fix-up is order-fixed: repeated runs and
-    CUDA-graph replays give identical bits."""
+@pytest.mark.parametrize("which", ["default", "stream-k"])
+def test_tc_determinism_and_graph_replay(dep, plan_cache, B, which):
+    """Both tensor-core kernels' split-K combinations are order-fixed: repeated
+    runs and CUDA-graph replays give identical bits (the default plan takes K
+    pieces for this 56-tile weight; the stream-K kernel is installed explicitly)."""
     N, K = 7168, 4096
     x, W = to_dev(synth.normal_bf16(B, 2, (B, K))), to_dev(synth.normal_bf16(5, 1, (N, K), 0.02))
-    plan = get_plan(dep, plan_cache, N, K)
-    assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC
+    if which == "default":
+        plan = get_plan(dep, plan_cache, N, K)
+        assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC_SPLIT
+    else:
+        plan = get_plan(dep, plan_cache, N, K, (B,))
+        NT = max(16, 1 << (B - 1).bit_length())
+        t = tc_tactic(dep, NT, sm_count(), 3, 128)
+        t.max_rows = B
+        dep.dep_projection_plan_set(plan, t)
+        assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC
     ref = empty_out(B, N)
     dep.dep_projection_run(plan, x, W, ref, B)
     torch.cuda.synchronize()
@@ -359,8 +369,11 @@ def test_tc_small_integers_exact(dep, orc, plan_cache):
     x = np.vectorize(exact_bf16)(xi).astype(np.uint16)
     W = np.vectorize(exact_bf16)(wi).astype(np.uint16)
     plan = get_plan(dep, plan_cache, N, K)
-    assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC
-    np.testing.assert_array_equal(run(dep, plan, x, W, N), orc.linear(x, W))
+    assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC_SPLIT
+    ref = orc.linear(x, W)
+    np.testing.assert_array_equal(run(dep, plan, x, W, N), ref)
+    for ctas in (1, 2, sm_count()):  # the stream-K kernel, split tiles included
+        np.testing.assert_array_equal(run(dep, plan, x, W, N, tc_tactic(dep, 32, ctas, 3, 128)), ref)
 
 
 def test_tc_negation_symmetric(dep, plan_cache):
@@ -583,3 +596,134 @@ def test_tc_fixup_bitexact_from_partials(dep, plan_cache, NT, B, tile_k):
             np.testing.assert_array_equal(y[b, n[keep]], want[keep])
             checked += int(keep.sum())
     assert checked > 0
+
+
+# ---------------- tensor-core tactic with fixed K pieces, dynamic items ----------------
+
+def tcs_tactic(dep, NT, ctas, splits, stages=3, tile_k=128, max_rows=None):
+    return dep.dep_tactic_t(max_rows=max_rows or NT, kind=dep.DEP_KIND_TC_SPLIT, ctas=ctas, tile_n=128,
+                            tile_k=tile_k, stages=stages, cols=NT, splits=splits)
+
+
+def tcs_plan(dep, N, K, tactics):
+    """A plan whose workspace is grown for the given K-piece tactics."""
+    plan = dep.dep_projection_plan(N, K, [1])
+    for t in tactics:
+        dep.dep_projection_plan_set(plan, t)
+    return plan
+
+
+TCS_STAGES = {(16, 64): 4, (16, 128): 3, (16, 256): 2, (32, 64): 4, (32, 256): 2, (64, 64): 4,
+              (64, 128): 3, (128, 64): 4, (128, 128): 2, (256, 64): 3}
+
+
+@pytest.mark.parametrize("N,K", [(128, 64), (333, 1000), (97, 264), (1000, 3000)])
+@pytest.mark.parametrize("NT,tile_k", sorted(TCS_STAGES))
+def test_tcs_parity_vs_oracle(dep, orc, N, K, NT, tile_k):
+    """K-piece tensor-core kernel, every MMA width and stage width: one piece
+    (direct stores), three pieces, and more pieces than k-tiles (capped); grids
+    of one block, seven blocks and every SM (items taken dynamically); partial
+    and full batches; ragged N and K tails."""
+    st = TCS_STAGES[(NT, tile_k)]
+    cases = [(1, 1), (1, sm_count()), (3, 1), (3, 7), (3, sm_count()), (64, sm_count())]
+    plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, c, s, st, tile_k, max_rows=300 + i)
+                                for i, (s, c) in enumerate(cases)])
+    try:
+        W = synth.normal_bf16(N + NT + 7, 1, (N, K), sigma=0.02)
+        for B in sorted({1, min(NT, 5), NT}):
+            x = synth.normal_bf16(B + NT + 7, 2, (B, K))
+            ref = orc.linear(x, W)
+            for splits, ctas in cases:
+                y = run(dep, plan, x, W, N, tcs_tactic(dep, NT, ctas, splits, st, tile_k))
+                ok, worst, idx = within_tolerance(y, ref)
+                assert ok, (B, splits, ctas, worst, idx)
+        assert dep.dep_projection_device_status(plan) == 0
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("NT,B,splits", [(16, 16, 5), (16, 3, 1), (64, 40, 4), (256, 256, 2)])
+def test_tcs_schedule_independent(dep, NT, B, splits):
+    """Which block runs which (tile, piece) item does not enter the arithmetic:
+    grids of 1, 7, 40 and all SMs give identical bits, run after run and in a
+    CUDA-graph replay."""
+    N, K = 1000, 4096
+    grids = [1, 7, 40, sm_count()]
+    plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, g, splits, 2, 128, max_rows=300 + i)
+                                for i, g in enumerate(grids)])
+    try:
+        x = to_dev(synth.normal_bf16(60 + B, 2, (B, K)))
+        W = to_dev(synth.normal_bf16(61, 1, (N, K), sigma=0.02))
+        outs = []
+        for g in grids:
+            for _ in range(2):
+                y = empty_out(B, N)
+                dep.dep_projection_run_tactic(plan, tcs_tactic(dep, NT, g, splits, 2, 128), x, W, y, B)
+                outs.append(y)
+        ys = [empty_out(B, N) for _ in range(3)]
+        tac = tcs_tactic(dep, NT, sm_count(), splits, 2, 128)
+        torch.cuda.synchronize()  # a plan serves one stream at a time
+        graph = torch.cuda.CUDAGraph()
+        stream = torch.cuda.Stream()
+        with torch.cuda.stream(stream):
+            dep.dep_projection_run_tactic(plan, tac, x, W, ys[0], B, stream)  # warm-up outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            for y in ys:
+                dep.dep_projection_run_tactic(plan, tac, x, W, y, B, stream)
+        graph.replay()
+        graph.replay()
+        torch.cuda.synchronize()
+        outs += ys
+        for y in outs[1:]:
+            assert torch.equal(y.view(torch.int16), outs[0].view(torch.int16))
+        assert dep.dep_projection_device_status(plan) == 0
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("NT,B,tile_k", [(16, 8, 256), (32, 32, 64), (128, 100, 128)])
+def test_tcs_one_piece_equals_whole_tile_stream_k(dep, NT, B, tile_k):
+    """With one piece per tile each tile is summed by one accumulator over all of
+    K in the same MMA sequence as the stream-K kernel launched with one block per
+    tile: the two kernels give identical bits."""
+    N, K = 1000, 3000
+    T = -(-N // 128)
+    plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, sm_count(), 1, 2, tile_k, max_rows=300),
+                                tc_tactic(dep, NT, T, 2, tile_k)])
+    try:
+        x = synth.normal_bf16(70 + B, 2, (B, K))
+        W = synth.normal_bf16(71, 1, (N, K), sigma=0.02)
+        y1 = run(dep, plan, x, W, N, tcs_tactic(dep, NT, sm_count(), 1, 2, tile_k))
+        y2 = run(dep, plan, x, W, N, tc_tactic(dep, NT, T, 2, tile_k))
+        np.testing.assert_array_equal(y1, y2)
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("NT,B,splits,tile_k", [(16, 16, 8, 256), (16, 5, 3, 64), (64, 64, 4, 128),
+                                                (256, 200, 2, 64)])
+def test_tcs_fixup_bitexact_from_partials(dep, NT, B, splits, tile_k):
+    """The K pieces' FP32 partials left in the workspace, added in piece order
+    0..S-1 in float32 and rounded to BF16 (nearest, ties to even), give y bit
+    for bit."""
+    N, K = 1000, 4096
+    plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, sm_count(), splits, 2, tile_k)])
+    try:
+        x = synth.normal_bf16(80 + NT, 2, (B, K))
+        W = synth.normal_bf16(81, 1, (N, K), sigma=0.02)
+        y = run(dep, plan, x, W, N, tcs_tactic(dep, NT, sm_count(), splits, 2, tile_k))
+        T = -(-N // 128)
+        S = min(splits, -(-K // tile_k))
+        ws = dep.dep_projection_plan_partials(plan, T * S * NT * 128).reshape(T, S, NT, 128)
+        rows = np.arange(128)
+        for t in range(T):
+            n = t * 128 + rows
+            keep = n < N
+            s = ws[t, 0, :B, :].copy()
+            for p in range(1, S):
+                s = (s + ws[t, p, :B, :]).astype(np.float32)
+            want = synth.bf16_from_f64(s.astype(np.float64))
+            np.testing.assert_array_equal(y[:, n[keep]], want[:, keep])
+    finally:
+        dep.dep_projection_plan_destroy(plan)
