@@ -69,9 +69,10 @@ typedef enum {
 #define DEP_KIND_TC 2         /* tcgen05 MMA, TMEM accumulators, TMA-staged W and x */
 #define DEP_KIND_ROWS 3       /* warp split-K over whole weight rows, dynamic tiles, no
                                  cross-block fix-up; x resident in shared memory */
-#define DEP_KIND_TC_SPLIT 4   /* tcgen05 MMA over (128-row tile, K piece) items taken
-                                 dynamically; each tile cut into `splits` fixed K pieces
-                                 whose FP32 partials are added in piece order */
+#define DEP_KIND_TC_SPLIT 4   /* tcgen05 MMA over (tile, K piece) items taken
+                                 dynamically; tiles of tile_n = 64 or 128 weight rows
+                                 (MMA M), each cut into `splits` fixed K pieces whose
+                                 FP32 partials are added in piece order */
 
 /* One table entry: the tactic that serves batches of up to max_rows rows. */
 typedef struct {
@@ -196,7 +197,7 @@ dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic
  * tile row r) at float index ((c * 2 + s) * cols + j) * tile_n + r, slot 0 for
  * the block's first tile and 1 for its last.  For a K-piece launch (TC_SPLIT,
  * S pieces in effect): partial (tile t, piece p, batch column j, tile row r) at
- * float index ((t * S + p) * cols + j) * 128 + r.  Lets a test re-add the
+ * float index ((t * S + p) * cols + j) * tile_n + r.  Lets a test re-add the
  * partials of every split tile in block or piece order and check the kernel's
  * fix-up bit for bit.
  */

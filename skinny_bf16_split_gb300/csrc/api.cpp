@@ -123,8 +123,6 @@ size_t tactic_counters(const dep_tactic_t &t, int64_t N)
     }
 }
 
-constexpr int32_t kFmaMaxRows = 4;  // default split point between the two kernels
-
 dep_tactic_t fma_tactic(int32_t rows, int32_t cols, int32_t stages, int sm_count, bool host_only,
                         int32_t tile_n = 32)
 {
@@ -166,10 +164,12 @@ dep_tactic_t tc_tactic(int32_t rows, int32_t cols, int32_t stages, int32_t ctas,
     return t;
 }
 
-dep_tactic_t tcs_tactic(int32_t rows, int32_t cols, int32_t stages, int32_t ctas, int32_t tile_k, int32_t splits)
+dep_tactic_t tcs_tactic(int32_t rows, int32_t cols, int32_t stages, int32_t ctas, int32_t tile_k, int32_t splits,
+                        int32_t tile_n)
 {
     dep_tactic_t t = tc_tactic(rows, cols, stages, ctas, tile_k);
     t.kind = DEP_KIND_TC_SPLIT;
+    t.tile_n = tile_n;
     t.splits = splits;
     return t;
 }
@@ -183,49 +183,47 @@ int32_t tc_default_stages(int32_t cols)
     return 2;
 }
 
-// The fixed rule: warp split-K on the FMA pipe for small batches; the
-// tensor-core kernel past them (runtime.hybrid page, HybridAttention.__init__:
-// warp split-K up to 16 rows, the GEMM path past it; the split point moves to
-// where the FMA pipe stops keeping up with HBM on this GPU).  The tensor-core
-// kernel runs one block per 128-row tile when the tiles nearly fill the GPU,
-// and the even stream-K split otherwise.
+// The fixed rule (runtime.hybrid page, HybridAttention.__init__: warp split-K
+// for the smallest batches, the GEMM path past them; the split point moves to
+// where each kernel measured fastest on this GPU):
+//  * one or two x rows: whole weight rows on the FMA pipe (no cross-block split);
+//  * up to 16 rows (a 16-wide MMA) while the 128-row tiles fit on the SMs: the
+//    tensor cores over fixed K pieces, SMs / tiles pieces per tile (o_proj: 2,
+//    DSA: 1), one item per block;
+//  * otherwise the stream-K tensor-core kernel, one block per tile when the
+//    tiles nearly fill the GPU.
+// Measured on GB300 (per call, CUDA events): at 4 rows the K-piece tensor-core
+// tactic is 1.9-2.8 us faster than the stream-K FMA kernel on all three
+// weights; at 8 and 16 rows it is 0.7-1.0 us faster than the stream-K
+// tensor-core kernel for o_proj and DSA and equal for KDA (386 tiles).
 dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count, bool host_only)
 {
+    (void)host_only;
     if (rows <= 2) {
         // Whole rows, no cross-block split: 16-row tiles, 4 stages of 1024
         // columns, handed out dynamically (measured on GB300: 5-8 % faster than
         // the stream-K FMA kernel at one x row, on all three weights).  Falls
-        // back to the FMA kernel where x does not fit in shared memory.
+        // through where x does not fit in shared memory.
         const int32_t cols = pow2_at_least(rows);
         const dep_tactic_t t = rows_tactic(rows, cols, 16, 1024, 4, sm_count);
         if (dep::rows_fits(t, K))
             return t;
     }
-    if (rows <= kFmaMaxRows) {
-        // 64-row tiles (each x value reused over 8 rows per warp), 4 stages of
-        // 32-34 KB; 6 stages for four x rows.  Measured on GB300 against 32-row
-        // tiles with up to 8 stages: equal or faster on all three weights.
-        const int32_t cols = pow2_at_least(rows);
-        return fma_tactic(rows, cols, cols >= 4 ? 6 : 4, sm_count, host_only, 64);
-    }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128;
-    if (2 * tiles <= sm_count) {
-        // At most half as many 128-row tiles as SMs (o_proj: 56): cut every tile
-        // into SMs / tiles fixed K pieces, one dynamically taken item per block,
-        // instead of stream-K segments (measured on GB300 for o_proj at 8 and 16
-        // rows, 2 pieces: 1 us per call faster).
-        const int32_t splits = (int32_t)std::min<int64_t>(64, sm_count / tiles);
+    // Widest stage (most contiguous bytes per weight row) that still leaves a
+    // ring of at least three stages.
+    if (cols == 16 && tiles <= sm_count) {
+        const int32_t splits = (int32_t)std::min<int64_t>(64, std::max<int64_t>(1, sm_count / tiles));
         for (int32_t tk : {256, 128})
             for (int32_t st : {6, 5, 4, 3}) {
-                const dep_tactic_t t = tcs_tactic(rows, cols, st, sm_count, tk, splits);
+                const dep_tactic_t t = tcs_tactic(rows, cols, st, sm_count, tk, splits, 128);
                 if (dep::tcs_valid(t))
                     return t;
             }
     }
     const int32_t ctas = (tiles <= sm_count && 4 * tiles >= 3 * (int64_t)sm_count) ? (int32_t)tiles : sm_count;
-    // Widest stage (most contiguous bytes per weight row) that still leaves a
-    // ring of at least three stages; 64-column stages for the widest batches.
+    // 64-column stages for the widest batches.
     for (int32_t tk : {256, 128}) {
         for (int32_t st : {6, 5, 4, 3}) {
             const dep_tactic_t t = tc_tactic(rows, cols, st, ctas, tk);
@@ -483,15 +481,19 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
         for (int32_t st : {2, 3, 4, 6, 8, 10, 12})
             for (int32_t g : grids)
                 c.push_back(tc_tactic(rows, cols, st, g, tk));
-    // Fixed K pieces taken dynamically: 1 to 8 pieces per tile, and as many as
-    // give one item per SM.
-    std::vector<int32_t> pieces{1, 2, 3, 4, 8};
-    if (tiles < sm_count && std::find(pieces.begin(), pieces.end(), (int32_t)(sm_count / tiles)) == pieces.end())
-        pieces.push_back((int32_t)std::min<int64_t>(64, sm_count / tiles));
-    for (int32_t tk : {128, 256})
-        for (int32_t st : {3, 4, 6})
-            for (int32_t sp : pieces)
-                c.push_back(tcs_tactic(rows, cols, st, sm_count, tk, sp));
+    // Fixed K pieces taken dynamically, on 64- and 128-row tiles: 1 to 8
+    // pieces per tile, and as many as give about one item per SM.
+    for (int32_t bm : {64, 128}) {
+        const int64_t t_bm = (N + bm - 1) / bm;
+        std::vector<int32_t> pieces{1, 2, 3, 4, 8};
+        const int32_t fill = (int32_t)std::min<int64_t>(64, std::max<int64_t>(1, sm_count / t_bm));
+        if (std::find(pieces.begin(), pieces.end(), fill) == pieces.end())
+            pieces.push_back(fill);
+        for (int32_t tk : {128, 256})
+            for (int32_t st : {3, 4, 5, 6})
+                for (int32_t sp : pieces)
+                    c.push_back(tcs_tactic(rows, cols, st, sm_count, tk, sp, bm));
+    }
     // K pieces keep every piece's partial: leave out tactics whose partials
     // would take more than 64 MB of workspace.
     constexpr size_t kMaxPieceWorkspaceFloats = (64u << 20) / sizeof(float);

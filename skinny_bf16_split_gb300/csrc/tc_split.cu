@@ -36,18 +36,18 @@
 namespace dep {
 namespace {
 
-constexpr int kBM = 128;      // weight rows per tile (MMA M)
 constexpr int kBK = 64;       // columns per slice: one 128-byte swizzle row
 constexpr int kUmmaK = 16;    // K of one kind::f16 MMA
 constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA/TMEM, warps 2-5 epilogue
 constexpr int kEpiWarps = 4;
-constexpr int kABytes = kBM * kBK * 2;  // 16 KB weight slice
 constexpr int kMaxSplits = 64;
 
-template <int NT>
+// BM = weight rows per tile = MMA M (64 or 128); NT = MMA N (the padded batch).
+template <int NT, int BM>
 struct SplitShape {
+    static constexpr int A_BYTES = BM * kBK * 2;  // one weight slice: 8 or 16 KB
     static constexpr int B_BYTES = NT * kBK * 2;
-    static constexpr int ATOM = kABytes + B_BYTES;
+    static constexpr int ATOM = A_BYTES + B_BYTES;
     static constexpr uint32_t TMEM_COLS = 2 * NT < 32 ? 32 : 2 * NT;
 };
 
@@ -69,14 +69,14 @@ __device__ __forceinline__ uint16_t to_bf16(float v)
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-template <int NT>
+template <int NT, int BM>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_split_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms, int S,
                     float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ dispenser,
                     int *__restrict__ status, uint64_t limit_ns)
 {
-    using Sh = SplitShape<NT>;
+    using Sh = SplitShape<NT, BM>;
     const int STAGE = atoms * Sh::ATOM;
     const int KG = atoms * kBK;  // columns per k-tile (one stage)
     extern __shared__ uint8_t smem_raw[];
@@ -95,11 +95,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tags + stages) + 2;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-    const int T = (N + kBM - 1) / kBM, KT = (K + KG - 1) / KG, I = T * S;
+    const int T = (N + BM - 1) / BM, KT = (K + KG - 1) / KG, I = T * S;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int *grab = dispenser, *finished = dispenser + 1;
 
+    // Producer state; the producer is thread 0 (warp 0, lane 0).
+    uint64_t pol_w = 0, pol_x = 0;
+    int item = blockIdx.x;  // the grid never exceeds the item count
+    int tile = item / S, kt = piece_begin(item % S, KT, S), kt_end = piece_begin(item % S + 1, KT, S);
+    const int kt0 = kt;
+    const int pre = (kt_end - kt) < stages ? (kt_end - kt) : stages;
+    auto stage_addr = [&](int st) { return base + (uint32_t)(st * STAGE); };
+    auto issue_w = [&](int st) {
+        const int flags = (kt == piece_begin(item % S, KT, S) ? 1 : 0) | (kt == kt_end - 1 ? 2 : 0);
+        tags[st] = make_int2(item, flags);
+        mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)STAGE);
+        for (int a = 0; a < atoms; ++a)
+            tma_load_2d(stage_addr(st) + (uint32_t)(a * Sh::A_BYTES), &tmW, kt * KG + a * kBK, tile * BM,
+                        full0 + 8 * st, pol_w);
+    };
+    auto issue_x = [&](int st, int k_tile) {
+        const uint32_t xs = stage_addr(st) + (uint32_t)(atoms * Sh::A_BYTES);
+        for (int a = 0; a < atoms; ++a)
+            tma_load_2d(xs + (uint32_t)(a * Sh::B_BYTES), &tmX, k_tile * KG + a * kBK, 0, full0 + 8 * st, pol_x);
+    };
+
     if (threadIdx.x == 0) {
+        prefetch_tmap(&tmW);
+        prefetch_tmap(&tmX);
         for (int s = 0; s < stages; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
@@ -113,6 +136,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_mbar_init();
         griddep_launch_dependents();
+        // Phase 1, while warp 1 allocates TMEM: the weight is not written by
+        // preceding work -- fill the ring with the first k-tiles of the first item.
+        pol_w = policy_evict_first();
+        pol_x = policy_evict_last();
+        for (int i = 0; i < pre; ++i, ++kt)
+            issue_w(i);
     }
     if (warp == 1) {
         tc::alloc(smem_u32(tmem_slot), Sh::TMEM_COLS);
@@ -126,33 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ---------------- TMA producer: takes the items ----------------
         if (lane == 0) {
-            prefetch_tmap(&tmW);
-            prefetch_tmap(&tmX);
-            const uint64_t pol_w = policy_evict_first(), pol_x = policy_evict_last();
-            int item = blockIdx.x;  // the grid never exceeds the item count
-            int tile = item / S, kt = piece_begin(item % S, KT, S), kt_end = piece_begin(item % S + 1, KT, S);
-            auto stage_addr = [&](int st) { return base + (uint32_t)(st * STAGE); };
-            auto issue_w = [&](int st) {
-                const int flags = (kt == piece_begin(item % S, KT, S) ? 1 : 0) | (kt == kt_end - 1 ? 2 : 0);
-                tags[st] = make_int2(item, flags);
-                mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)STAGE);
-                for (int a = 0; a < atoms; ++a)
-                    tma_load_2d(stage_addr(st) + (uint32_t)(a * kABytes), &tmW, kt * KG + a * kBK, tile * kBM,
-                                full0 + 8 * st, pol_w);
-            };
-            auto issue_x = [&](int st, int k_tile) {
-                const uint32_t xs = stage_addr(st) + (uint32_t)(atoms * kABytes);
-                for (int a = 0; a < atoms; ++a)
-                    tma_load_2d(xs + (uint32_t)(a * Sh::B_BYTES), &tmX, k_tile * KG + a * kBK, 0, full0 + 8 * st,
-                                pol_x);
-            };
-            // Phase 1: the weight is not written by preceding work -- fill the ring
-            // with the first k-tiles of the first item, then wait for the
-            // preceding grid before reading x or the item counter.
-            const int kt0 = kt;
-            const int pre = (kt_end - kt) < stages ? (kt_end - kt) : stages;
-            for (int i = 0; i < pre; ++i, ++kt)
-                issue_w(i);
+            // Phase 2: after the preceding grid -- x of the filled stages, then the
+            // rest of the items (taken from the counter).
             griddep_wait();
             for (int i = 0; i < pre; ++i)
                 issue_x(i, kt0 + i);
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, NT);
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, NT);
             int s = 0, buf = 0;
             uint32_t ph = 0, acce_ph = 0;
             uint32_t accumulate = 0;
@@ -249,8 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem + (uint32_t)(buf * NT);
                 const uint32_t st = base + (uint32_t)(s * STAGE);
                 for (int a = 0; a < atoms; ++a) {
-                    const uint64_t ad = tc::desc_sw128(st + (uint32_t)(a * kABytes));
-                    const uint64_t bd = tc::desc_sw128(st + (uint32_t)(atoms * kABytes + a * Sh::B_BYTES));
+                    const uint64_t ad = tc::desc_sw128(st + (uint32_t)(a * Sh::A_BYTES));
+                    const uint64_t bd = tc::desc_sw128(st + (uint32_t)(atoms * Sh::A_BYTES + a * Sh::B_BYTES));
 #pragma unroll
                     for (int j = 0; j < kBK / kUmmaK; ++j) {
                         // advance along K inside the 128-byte swizzle row: 32 bytes per step
@@ -279,7 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------- epilogue warps ----------------
         griddep_wait();  // workspace, counters and y may still be in use by the preceding grid
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
-        const int row = 32 * q + lane;
+        // M = 128: tile row r is TMEM lane r.  M = 64: rows 16q..16q+15 are lanes
+        // 0-15 of quadrant q (lanes 16-31 hold nothing of this MMA).
+        const int row = BM == 128 ? 32 * q + lane : 16 * q + lane;
+        const bool has_row = BM == 128 || lane < 16;
         uint32_t tag_ph = 0, accf_ph = 0;
         int buf = 0;
         for (;;) {
@@ -300,9 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             accf_ph ^= 1u << buf;
             tc::fence_after();
             const int t = item / S;
-            const int64_t n = (int64_t)t * kBM + row;
+            const int64_t n = (int64_t)t * BM + row;
+            const bool mine = has_row && n < N;  // this lane's output row exists
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NT);
-            float *part = ws + (int64_t)item * NT * kBM + row;
+            float *part = ws + (int64_t)item * NT * BM + row;
 #pragma unroll 1
             for (int c0 = 0; c0 < NT; c0 += 16) {
                 uint32_t v[16];
@@ -311,13 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int b = c0 + j;
-                    if (b < B) {
+                    if (b < B && has_row) {
                         const float f = __uint_as_float(v[j]);
                         if (S == 1) {
                             if (n < N)
                                 y[(int64_t)b * N + n] = to_bf16(f);
                         } else {
-                            __stcg(part + (int64_t)b * kBM, f);
+                            __stcg(part + (int64_t)b * BM, f);
                         }
                     }
                 }
@@ -338,20 +346,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (prev != S - 1)
                 continue;  // another piece of this tile is still running
             __threadfence();
-            if (n < N) {
+            if (mine) {
                 // Sum the pieces in order 0..S-1; the loads of up to 4 pieces x 16
                 // batch columns are issued together, then added.
-                const float *tile_ws = ws + (int64_t)t * S * NT * kBM + row;
+                const float *tile_ws = ws + (int64_t)t * S * NT * BM + row;
                 for (int b0 = 0; b0 < B; b0 += 16) {
                     float sum[16];
                     for (int p0 = 0; p0 < S; p0 += 4) {
                         float pv[4][16];
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const float *src = tile_ws + ((int64_t)(p0 + i) * NT + b0) * kBM;
+                            const float *src = tile_ws + ((int64_t)(p0 + i) * NT + b0) * BM;
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
-                                pv[i][j] = (p0 + i < S && b0 + j < B) ? __ldcg(src + (int64_t)j * kBM) : 0.0f;
+                                pv[i][j] = (p0 + i < S && b0 + j < B) ? __ldcg(src + (int64_t)j * BM) : 0.0f;
                         }
 #pragma unroll
                         for (int i = 0; i < 4; ++i)
@@ -380,17 +388,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int NT>
+template <int NT, int BM>
 size_t smem_bytes(int stages, int atoms)
 {
-    return split_smem_bytes(stages, atoms * SplitShape<NT>::ATOM);
+    return split_smem_bytes(stages, atoms * SplitShape<NT, BM>::ATOM);
 }
 
-template <int NT>
+template <int NT, int BM>
 cudaError_t prepare()
 {
     static std::atomic<uint64_t> devices{0};
-    return set_smem_attr(tc_split_kernel<NT>, devices);
+    return set_smem_attr(tc_split_kernel<NT, BM>, devices);
 }
 
 // Pieces actually used: never more than the k-tiles of a tile (no empty piece).
@@ -400,28 +408,33 @@ int64_t effective_splits(const dep_tactic_t &t, int64_t K)
     return t.splits < KT ? t.splits : KT;
 }
 
-template <int NT>
-cudaError_t run_nt(const dep_tactic_t &t, const RunArgs &a)
+int64_t tiles_of(const dep_tactic_t &t, int64_t N)
 {
-    cudaError_t e = prepare<NT>();
+    return (N + t.tile_n - 1) / t.tile_n;
+}
+
+template <int NT, int BM>
+cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
+{
+    cudaError_t e = prepare<NT, BM>();
     if (e != cudaSuccess)
         return e;
     CUtensorMap tmW, tmX;
-    if (encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) !=
+    if (encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, BM, CU_TENSOR_MAP_SWIZZLE_128B) !=
         CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const int atoms = t.tile_k / kBK;
     const int S = (int)effective_splits(t, a.K);
-    const int64_t items = ((a.N + kBM - 1) / kBM) * S;
+    const int64_t items = tiles_of(t, a.N) * S;
     const int grid = (int)(items < t.ctas ? items : t.ctas);
-    const size_t smem = smem_bytes<NT>(t.stages, atoms);
+    const size_t smem = smem_bytes<NT, BM>(t.stages, atoms);
     int *dispenser = a.counters + a.n_counters - 2;
     for (int32_t r0 = 0; r0 < a.B; r0 += NT) {
         const int32_t rows = a.B - r0 < NT ? a.B - r0 : NT;
         if (encode_bf16_2d(&tmX, a.x + (size_t)r0 * a.K, (uint64_t)a.K, (uint64_t)rows, kBK, NT,
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        e = launch(tc_split_kernel<NT>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
+        e = launch(tc_split_kernel<NT, BM>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
                    a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, S, a.ws, a.counters,
                    dispenser, a.status, a.wait_limit_ns);
         if (e != cudaSuccess)
@@ -430,37 +443,56 @@ cudaError_t run_nt(const dep_tactic_t &t, const RunArgs &a)
     return cudaSuccess;
 }
 
-template <int NT>
-int blocks_per_sm(int stages, int atoms)
+template <int NT, int BM>
+int blocks_per_sm_shape(const dep_tactic_t &t)
 {
-    if (prepare<NT>() != cudaSuccess)
+    if (prepare<NT, BM>() != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_split_kernel<NT>, kThreads,
-                                                      smem_bytes<NT>(stages, atoms)) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tc_split_kernel<NT, BM>, kThreads,
+                                                      smem_bytes<NT, BM>(t.stages, t.tile_k / kBK)) != cudaSuccess)
         return 0;
     return n;
 }
 
-size_t smem_for(const dep_tactic_t &t)
+template <int NT, int BM>
+size_t smem_shape(const dep_tactic_t &t)
 {
-    const int atoms = t.tile_k / kBK;
-    switch (t.cols) {
-    case 16: return smem_bytes<16>(t.stages, atoms);
-    case 32: return smem_bytes<32>(t.stages, atoms);
-    case 64: return smem_bytes<64>(t.stages, atoms);
-    case 128: return smem_bytes<128>(t.stages, atoms);
-    case 256: return smem_bytes<256>(t.stages, atoms);
-    default: return 0;
-    }
+    return smem_bytes<NT, BM>(t.stages, t.tile_k / kBK);
 }
+
+template <int NT, int BM>
+cudaError_t prepare_shape(const dep_tactic_t &)
+{
+    return prepare<NT, BM>();
+}
+
+// The tactic's instantiation: MMA width (cols) x tile rows (tile_n).
+#define DEP_TCS_DISPATCH(NAME, RET, FN, BAD)                                    \
+    RET NAME(const dep_tactic_t &t)                                             \
+    {                                                                           \
+        const bool m64 = t.tile_n == 64;                                        \
+        switch (t.cols) {                                                       \
+        case 16: return m64 ? FN<16, 64>(t) : FN<16, 128>(t);                   \
+        case 32: return m64 ? FN<32, 64>(t) : FN<32, 128>(t);                   \
+        case 64: return m64 ? FN<64, 64>(t) : FN<64, 128>(t);                   \
+        case 128: return m64 ? FN<128, 64>(t) : FN<128, 128>(t);                \
+        case 256: return m64 ? FN<256, 64>(t) : FN<256, 128>(t);                \
+        default: return BAD;                                                    \
+        }                                                                       \
+    }
+
+DEP_TCS_DISPATCH(smem_for, size_t, smem_shape, 0)
+DEP_TCS_DISPATCH(blocks_for, int, blocks_per_sm_shape, 0)
+DEP_TCS_DISPATCH(prepare_for, cudaError_t, prepare_shape, cudaErrorInvalidValue)
+#undef DEP_TCS_DISPATCH
 
 }  // namespace
 
 bool tcs_valid(const dep_tactic_t &t)
 {
-    if (t.kind != DEP_KIND_TC_SPLIT || t.ctas < 1 || t.tile_n != kBM)
-        return false;
+    if (t.kind != DEP_KIND_TC_SPLIT || t.ctas < 1 || (t.tile_n != 64 && t.tile_n != 128))
+        return false;  // MMA M = 64 or 128 weight rows
     if (t.tile_k != kBK && t.tile_k != 2 * kBK && t.tile_k != 4 * kBK)
         return false;  // 1, 2 or 4 slices of 64 columns per stage
     if (t.stages < 2 || t.stages > 16 || t.splits < 1 || t.splits > kMaxSplits)
@@ -472,43 +504,42 @@ bool tcs_valid(const dep_tactic_t &t)
 size_t tcs_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K)
 {
     const int64_t S = effective_splits(t, K);
-    return S > 1 ? (size_t)((N + kBM - 1) / kBM) * (size_t)S * (size_t)t.cols * kBM : 0;
+    return S > 1 ? (size_t)tiles_of(t, N) * (size_t)S * (size_t)t.cols * (size_t)t.tile_n : 0;
 }
 
-size_t tcs_counters(const dep_tactic_t &, int64_t N)
+size_t tcs_counters(const dep_tactic_t &t, int64_t N)
 {
-    return (size_t)((N + kBM - 1) / kBM) * kEpiWarps + 2;  // + the item counter pair at the end
+    return (size_t)tiles_of(t, N) * kEpiWarps + 2;  // + the item counter pair at the end
 }
 
 int tcs_blocks_per_sm(const dep_tactic_t &t)
 {
-    const int atoms = t.tile_k / kBK;
-    switch (t.cols) {
-    case 16: return blocks_per_sm<16>(t.stages, atoms);
-    case 32: return blocks_per_sm<32>(t.stages, atoms);
-    case 64: return blocks_per_sm<64>(t.stages, atoms);
-    case 128: return blocks_per_sm<128>(t.stages, atoms);
-    case 256: return blocks_per_sm<256>(t.stages, atoms);
-    default: return 0;
-    }
+    return blocks_for(t);
 }
 
 cudaError_t tcs_prepare_device()
 {
-    for (cudaError_t e : {prepare<16>(), prepare<32>(), prepare<64>(), prepare<128>(), prepare<256>()})
-        if (e != cudaSuccess)
-            return e;
+    for (int32_t cols : {16, 32, 64, 128, 256})
+        for (int32_t bm : {64, 128}) {
+            dep_tactic_t t{};
+            t.cols = cols;
+            t.tile_n = bm;
+            const cudaError_t e = prepare_for(t);
+            if (e != cudaSuccess)
+                return e;
+        }
     return cudaSuccess;
 }
 
 cudaError_t tcs_run(const dep_tactic_t &t, const RunArgs &a)
 {
+    const bool m64 = t.tile_n == 64;
     switch (t.cols) {
-    case 16: return run_nt<16>(t, a);
-    case 32: return run_nt<32>(t, a);
-    case 64: return run_nt<64>(t, a);
-    case 128: return run_nt<128>(t, a);
-    case 256: return run_nt<256>(t, a);
+    case 16: return m64 ? run_shape<16, 64>(t, a) : run_shape<16, 128>(t, a);
+    case 32: return m64 ? run_shape<32, 64>(t, a) : run_shape<32, 128>(t, a);
+    case 64: return m64 ? run_shape<64, 64>(t, a) : run_shape<64, 128>(t, a);
+    case 128: return m64 ? run_shape<128, 64>(t, a) : run_shape<128, 128>(t, a);
+    case 256: return m64 ? run_shape<256, 64>(t, a) : run_shape<256, 128>(t, a);
     default: return cudaErrorInvalidValue;
     }
 }

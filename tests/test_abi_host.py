@@ -56,10 +56,10 @@ def test_default_table_follows_split_rule(dep):
             assert t.ctas >= 152 and t.stages >= 2
             assert t.kind in (dep.DEP_KIND_SPLITK_FMA, dep.DEP_KIND_TC, dep.DEP_KIND_ROWS,
                               dep.DEP_KIND_TC_SPLIT)
-            if t.max_rows <= 4:  # small batches: warp split-K on the FMA pipe
-                assert t.kind in (dep.DEP_KIND_SPLITK_FMA, dep.DEP_KIND_ROWS)
+            if t.max_rows <= 2:  # the smallest batches: warp split-K over whole rows
+                assert t.kind == dep.DEP_KIND_ROWS
             else:  # 56 tiles of 128 rows on 152 SMs: two K pieces per tile
-                assert (t.kind, t.splits) == (dep.DEP_KIND_TC_SPLIT, 2)
+                assert (t.kind, t.tile_n, t.splits, t.cols) == (dep.DEP_KIND_TC_SPLIT, 128, 2, 16)
         for B, key in [(1, 1), (3, 4), (5, 8), (16, 16), (17, 16), (1000, 16)]:
             assert dep.dep_projection_plan_query(plan, B).max_rows == key
     finally:
@@ -71,8 +71,9 @@ def test_default_batches_when_none_given(dep):
     try:
         table = dep.dep_projection_plan_table(plan)
         assert [t.max_rows for t in table] == [1, 2, 4, 8, 16, 32, 64, 128, 256]
-        # 114 tiles of 128 rows nearly fill 152 SMs: one stream-K block per tile
-        assert all((t.kind, t.ctas) == (dep.DEP_KIND_TC, 114) for t in table if t.max_rows > 4)
+        # 114 tiles of 128 rows nearly fill 152 SMs: whole tiles, one per block
+        assert all((t.kind, t.splits) == (dep.DEP_KIND_TC_SPLIT, 1) for t in table if 2 < t.max_rows <= 16)
+        assert all((t.kind, t.ctas) == (dep.DEP_KIND_TC, 114) for t in table if t.max_rows > 16)
     finally:
         dep.dep_projection_plan_destroy(plan)
 
@@ -170,7 +171,7 @@ def test_k_piece_tactic_validation_and_save(dep, tmp_path):
         dep.dep_projection_plan_set(plan, t)
         q = dep.dep_projection_plan_query(plan, 9)
         assert (q.kind, q.splits, q.tile_k) == (dep.DEP_KIND_TC_SPLIT, 8, 256)
-        for field, value in (("splits", 0), ("splits", 65), ("tile_n", 64), ("tile_k", 192),
+        for field, value in (("splits", 0), ("splits", 65), ("tile_n", 32), ("tile_k", 192),
                              ("stages", 1), ("cols", 24), ("stages", 12)):
             bad = dep.dep_tactic_t(**{**t.as_dict(), field: value})
             with pytest.raises(dep.DepError):

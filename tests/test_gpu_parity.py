@@ -332,7 +332,8 @@ def test_tc_determinism_and_graph_replay(dep, plan_cache, B, which):
     x, W = to_dev(synth.normal_bf16(B, 2, (B, K))), to_dev(synth.normal_bf16(5, 1, (N, K), 0.02))
     if which == "default":
         plan = get_plan(dep, plan_cache, N, K)
-        assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC_SPLIT
+        want = dep.DEP_KIND_TC_SPLIT if B <= 16 else dep.DEP_KIND_TC
+        assert dep.dep_projection_plan_query(plan, B).kind == want
     else:
         plan = get_plan(dep, plan_cache, N, K, (B,))
         NT = max(16, 1 << (B - 1).bit_length())
@@ -369,11 +370,20 @@ def test_tc_small_integers_exact(dep, orc, plan_cache):
     x = np.vectorize(exact_bf16)(xi).astype(np.uint16)
     W = np.vectorize(exact_bf16)(wi).astype(np.uint16)
     plan = get_plan(dep, plan_cache, N, K)
-    assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC_SPLIT
+    assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC
     ref = orc.linear(x, W)
     np.testing.assert_array_equal(run(dep, plan, x, W, N), ref)
     for ctas in (1, 2, sm_count()):  # the stream-K kernel, split tiles included
         np.testing.assert_array_equal(run(dep, plan, x, W, N, tc_tactic(dep, 32, ctas, 3, 128)), ref)
+    pieces = tcs_plan(dep, N, K, [tcs_tactic(dep, 32, sm_count(), s, 3, 128, max_rows=300 + s, tile_n=bm)
+                                  for s in (1, 5) for bm in (64, 128)])
+    try:  # the K-piece kernel, one and five pieces, 64- and 128-row tiles
+        for s in (1, 5):
+            for bm in (64, 128):
+                y = run(dep, pieces, x, W, N, tcs_tactic(dep, 32, sm_count(), s, 3, 128, tile_n=bm))
+                np.testing.assert_array_equal(y, ref)
+    finally:
+        dep.dep_projection_plan_destroy(pieces)
 
 
 def test_tc_negation_symmetric(dep, plan_cache):
@@ -600,8 +610,8 @@ def test_tc_fixup_bitexact_from_partials(dep, plan_cache, NT, B, tile_k):
 
 # ---------------- tensor-core tactic with fixed K pieces, dynamic items ----------------
 
-def tcs_tactic(dep, NT, ctas, splits, stages=3, tile_k=128, max_rows=None):
-    return dep.dep_tactic_t(max_rows=max_rows or NT, kind=dep.DEP_KIND_TC_SPLIT, ctas=ctas, tile_n=128,
+def tcs_tactic(dep, NT, ctas, splits, stages=3, tile_k=128, max_rows=None, tile_n=128):
+    return dep.dep_tactic_t(max_rows=max_rows or NT, kind=dep.DEP_KIND_TC_SPLIT, ctas=ctas, tile_n=tile_n,
                             tile_k=tile_k, stages=stages, cols=NT, splits=splits)
 
 
@@ -619,14 +629,15 @@ TCS_STAGES = {(16, 64): 4, (16, 128): 3, (16, 256): 2, (32, 64): 4, (32, 256): 2
 
 @pytest.mark.parametrize("N,K", [(128, 64), (333, 1000), (97, 264), (1000, 3000)])
 @pytest.mark.parametrize("NT,tile_k", sorted(TCS_STAGES))
-def test_tcs_parity_vs_oracle(dep, orc, N, K, NT, tile_k):
-    """K-piece tensor-core kernel, every MMA width and stage width: one piece
-    (direct stores), three pieces, and more pieces than k-tiles (capped); grids
-    of one block, seven blocks and every SM (items taken dynamically); partial
-    and full batches; ragged N and K tails."""
+@pytest.mark.parametrize("BM", [128, 64])
+def test_tcs_parity_vs_oracle(dep, orc, N, K, NT, tile_k, BM):
+    """K-piece tensor-core kernel, every MMA width and stage width, MMA M of 128
+    and 64 weight rows: one piece (direct stores), three pieces, and more pieces
+    than k-tiles (capped); grids of one block, seven blocks and every SM (items
+    taken dynamically); partial and full batches; ragged N and K tails."""
     st = TCS_STAGES[(NT, tile_k)]
     cases = [(1, 1), (1, sm_count()), (3, 1), (3, 7), (3, sm_count()), (64, sm_count())]
-    plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, c, s, st, tile_k, max_rows=300 + i)
+    plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, c, s, st, tile_k, max_rows=300 + i, tile_n=BM)
                                 for i, (s, c) in enumerate(cases)])
     try:
         W = synth.normal_bf16(N + NT + 7, 1, (N, K), sigma=0.02)
@@ -634,7 +645,7 @@ def test_tcs_parity_vs_oracle(dep, orc, N, K, NT, tile_k):
             x = synth.normal_bf16(B + NT + 7, 2, (B, K))
             ref = orc.linear(x, W)
             for splits, ctas in cases:
-                y = run(dep, plan, x, W, N, tcs_tactic(dep, NT, ctas, splits, st, tile_k))
+                y = run(dep, plan, x, W, N, tcs_tactic(dep, NT, ctas, splits, st, tile_k, tile_n=BM))
                 ok, worst, idx = within_tolerance(y, ref)
                 assert ok, (B, splits, ctas, worst, idx)
         assert dep.dep_projection_device_status(plan) == 0
@@ -642,14 +653,15 @@ def test_tcs_parity_vs_oracle(dep, orc, N, K, NT, tile_k):
         dep.dep_projection_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("NT,B,splits", [(16, 16, 5), (16, 3, 1), (64, 40, 4), (256, 256, 2)])
-def test_tcs_schedule_independent(dep, NT, B, splits):
+@pytest.mark.parametrize("NT,B,splits,BM", [(16, 16, 5, 128), (16, 3, 1, 128), (64, 40, 4, 128),
+                                            (256, 256, 2, 128), (16, 16, 3, 64), (128, 77, 1, 64)])
+def test_tcs_schedule_independent(dep, NT, B, splits, BM):
     """Which block runs which (tile, piece) item does not enter the arithmetic:
     grids of 1, 7, 40 and all SMs give identical bits, run after run and in a
     CUDA-graph replay."""
     N, K = 1000, 4096
     grids = [1, 7, 40, sm_count()]
-    plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, g, splits, 2, 128, max_rows=300 + i)
+    plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, g, splits, 2, 128, max_rows=300 + i, tile_n=BM)
                                 for i, g in enumerate(grids)])
     try:
         x = to_dev(synth.normal_bf16(60 + B, 2, (B, K)))
@@ -658,10 +670,10 @@ def test_tcs_schedule_independent(dep, NT, B, splits):
         for g in grids:
             for _ in range(2):
                 y = empty_out(B, N)
-                dep.dep_projection_run_tactic(plan, tcs_tactic(dep, NT, g, splits, 2, 128), x, W, y, B)
+                dep.dep_projection_run_tactic(plan, tcs_tactic(dep, NT, g, splits, 2, 128, tile_n=BM), x, W, y, B)
                 outs.append(y)
         ys = [empty_out(B, N) for _ in range(3)]
-        tac = tcs_tactic(dep, NT, sm_count(), splits, 2, 128)
+        tac = tcs_tactic(dep, NT, sm_count(), splits, 2, 128, tile_n=BM)
         torch.cuda.synchronize()  # a plan serves one stream at a time
         graph = torch.cuda.CUDAGraph()
         stream = torch.cuda.Stream()
@@ -701,24 +713,25 @@ def test_tcs_one_piece_equals_whole_tile_stream_k(dep, NT, B, tile_k):
         dep.dep_projection_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("NT,B,splits,tile_k", [(16, 16, 8, 256), (16, 5, 3, 64), (64, 64, 4, 128),
-                                                (256, 200, 2, 64)])
-def test_tcs_fixup_bitexact_from_partials(dep, NT, B, splits, tile_k):
+@pytest.mark.parametrize("NT,B,splits,tile_k,BM", [(16, 16, 8, 256, 128), (16, 5, 3, 64, 128),
+                                                   (64, 64, 4, 128, 128), (256, 200, 2, 64, 128),
+                                                   (16, 16, 4, 256, 64), (32, 20, 3, 128, 64)])
+def test_tcs_fixup_bitexact_from_partials(dep, NT, B, splits, tile_k, BM):
     """The K pieces' FP32 partials left in the workspace, added in piece order
     0..S-1 in float32 and rounded to BF16 (nearest, ties to even), give y bit
     for bit."""
     N, K = 1000, 4096
-    plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, sm_count(), splits, 2, tile_k)])
+    plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, sm_count(), splits, 2, tile_k, tile_n=BM)])
     try:
         x = synth.normal_bf16(80 + NT, 2, (B, K))
         W = synth.normal_bf16(81, 1, (N, K), sigma=0.02)
-        y = run(dep, plan, x, W, N, tcs_tactic(dep, NT, sm_count(), splits, 2, tile_k))
-        T = -(-N // 128)
+        y = run(dep, plan, x, W, N, tcs_tactic(dep, NT, sm_count(), splits, 2, tile_k, tile_n=BM))
+        T = -(-N // BM)
         S = min(splits, -(-K // tile_k))
-        ws = dep.dep_projection_plan_partials(plan, T * S * NT * 128).reshape(T, S, NT, 128)
-        rows = np.arange(128)
+        ws = dep.dep_projection_plan_partials(plan, T * S * NT * BM).reshape(T, S, NT, BM)
+        rows = np.arange(BM)
         for t in range(T):
-            n = t * 128 + rows
+            n = t * BM + rows
             keep = n < N
             s = ws[t, 0, :B, :].copy()
             for p in range(1, S):
