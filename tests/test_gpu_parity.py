@@ -740,3 +740,25 @@ def test_tcs_fixup_bitexact_from_partials(dep, NT, B, splits, tile_k, BM):
             np.testing.assert_array_equal(y[:, n[keep]], want[:, keep])
     finally:
         dep.dep_projection_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("B,NT,splits,BM", [(40, 16, 2, 128), (300, 256, 1, 128), (33, 32, 3, 64)])
+def test_tcs_batches_wider_than_the_mma(dep, orc, B, NT, splits, BM):
+    """A batch wider than the MMA's N runs as consecutive launches of NT rows of x
+    each (the last one ragged), every launch reusing the plan's item counter and
+    piece counters: all rows match the oracle and a second run gives the same bits."""
+    N, K = 700, 2048
+    t = tcs_tactic(dep, NT, sm_count(), splits, 2, 128, max_rows=B, tile_n=BM)
+    plan = tcs_plan(dep, N, K, [t])
+    try:
+        x = synth.normal_bf16(100 + B, 2, (B, K))
+        W = synth.normal_bf16(101, 1, (N, K), sigma=0.02)
+        y1 = run(dep, plan, x, W, N)
+        y2 = run(dep, plan, x, W, N)
+        np.testing.assert_array_equal(y1, y2)
+        ok, worst, idx = within_tolerance(y1, orc.linear(x, W))
+        assert ok, (worst, idx)
+        assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC_SPLIT
+        assert dep.dep_projection_device_status(plan) == 0
+    finally:
+        dep.dep_projection_plan_destroy(plan)
