@@ -196,9 +196,8 @@ int32_t tc_default_stages(int32_t cols)
 // tactic is 1.9-2.8 us faster than the stream-K FMA kernel on all three
 // weights; at 8 and 16 rows it is 0.7-1.0 us faster than the stream-K
 // tensor-core kernel for o_proj and DSA and equal for KDA (386 tiles).
-dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count, bool host_only)
+dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
 {
-    (void)host_only;
     if (rows <= 2) {
         // Whole rows, no cross-block split: 16-row tiles, 4 stages of 1024
         // columns, handed out dynamically (measured on GB300: 5-8 % faster than
@@ -369,7 +368,7 @@ dep_status_t make_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_b
         }
     }
     for (int32_t b : bs)
-        p->table.push_back(default_tactic(b, N, K, p->sm_count, host_only));
+        p->table.push_back(default_tactic(b, N, K, p->sm_count));
     sort_table(p->table);
     if (!host_only) {
         st = allocate_device(p);
