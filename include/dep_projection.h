@@ -195,13 +195,21 @@ dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic
  * synchronising the device; *written = bytes copied (at most `bytes`).  Layout
  * for a stream-K launch of C blocks: partial (block c, slot s, batch column j,
  * tile row r) at float index ((c * 2 + s) * cols + j) * tile_n + r, slot 0 for
- * the block's first tile and 1 for its last.  For a K-piece launch (TC_SPLIT,
- * S pieces in effect): partial (tile t, piece p, batch column j, tile row r) at
- * float index ((t * S + p) * cols + j) * tile_n + r.  Lets a test re-add the
- * partials of every split tile in block or piece order and check the kernel's
- * fix-up bit for bit.
+ * the block's first tile and 1 for its last.  Lets a test re-add the partials
+ * of every split tile in block order and check the kernel's fix-up bit for bit.
  */
 dep_status_t dep_projection_plan_partials(dep_plan_t plan, void *host, size_t bytes, size_t *written);
+
+/*
+ * Inspection: copy the plan's K-piece exchange region (64-bit words) to host
+ * memory after synchronising the device; *written = bytes copied (at most
+ * `bytes`).  For a K-piece launch (TC_SPLIT, S > 1 pieces in effect) the word of
+ * (tile t, piece p, batch column j, tile row r) is at index
+ * ((t * S + p) * cols + j) * tile_n + r; its low 32 bits are the piece's FP32
+ * partial, its high 32 bits the "full" flag (0 once the launch has finished).
+ * Lets a test re-add the pieces in order and check y bit for bit.
+ */
+dep_status_t dep_projection_plan_exchange(dep_plan_t plan, void *host, size_t bytes, size_t *written);
 
 /* Bytes of device workspace the plan owns (split-K partials, counters, status). */
 dep_status_t dep_projection_plan_workspace(dep_plan_t plan, size_t *bytes);
@@ -225,7 +233,9 @@ void dep_projection_plan_destroy(dep_plan_t plan);
  * Read and clear the plan's device status word (synchronises `stream`).
  * *code = 0 if every kernel since the last read finished its waits; otherwise
  * the first nonzero code a kernel recorded (see DEP_DEV_* below), and the
- * return value is DEP_ERR_TIMEOUT.
+ * return value is DEP_ERR_TIMEOUT; the plan's split-K counters and K-piece
+ * exchange flags, which a give-up may leave mid-protocol, are then cleared
+ * (synchronises the device) so that later runs start clean.
  */
 dep_status_t dep_projection_device_status(dep_plan_t plan, void *stream, int32_t *code);
 

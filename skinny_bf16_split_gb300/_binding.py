@@ -46,7 +46,7 @@ EXPORTS = (
     "dep_projection_plan_save", "dep_projection_plan_load", "dep_projection_plan_destroy",
     "dep_projection_device_status", "dep_projection_selftest_timeout", "dep_bins_index",
     "dep_status_string", "dep_projection_version", "dep_projection_run_static",
-    "dep_projection_plan_partials",
+    "dep_projection_plan_partials", "dep_projection_plan_exchange",
 )
 
 
@@ -102,6 +102,7 @@ def lib():
         "dep_projection_version": ([], i32),
         "dep_projection_run_static": ([vp, vp, vp, i64, i64, i32, vp], i32),
         "dep_projection_plan_partials": ([vp, vp, ctypes.c_size_t, P(ctypes.c_size_t)], i32),
+        "dep_projection_plan_exchange": ([vp, vp, ctypes.c_size_t, P(ctypes.c_size_t)], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -224,6 +225,16 @@ def dep_projection_plan_partials(plan, count: int):
     _check(lib().dep_projection_plan_partials(plan, out.ctypes.data, out.nbytes, ctypes.byref(n)),
            "dep_projection_plan_partials")
     return out[: n.value // 4]
+
+
+def dep_projection_plan_exchange(plan, count: int):
+    """The first `count` 64-bit K-piece exchange words of the plan (numpy uint64)."""
+    import numpy as np
+    out = np.empty(count, dtype=np.uint64)
+    n = ctypes.c_size_t()
+    _check(lib().dep_projection_plan_exchange(plan, out.ctypes.data, out.nbytes, ctypes.byref(n)),
+           "dep_projection_plan_exchange")
+    return out[: n.value // 8]
 
 
 def dep_projection_plan_save(plan, path: str) -> None:

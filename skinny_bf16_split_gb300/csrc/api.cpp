@@ -32,6 +32,8 @@ struct dep_plan_s {
     size_t n_counters = 0;
     float *ws = nullptr;
     size_t ws_floats = 0;
+    unsigned long long *xch = nullptr;  // K-piece exchange words, zeroed at allocation
+    size_t xch_words = 0;
     uint16_t *x_stage = nullptr;
     uint16_t *y_stage = nullptr;
     int32_t stage_rows = 0;
@@ -89,8 +91,9 @@ size_t ws_per_cta(const dep_tactic_t &t)
     switch (t.kind) {
     case DEP_KIND_SPLITK_FMA: return dep::fma_ws_per_cta(t);
     case DEP_KIND_TC: return dep::tc_ws_per_cta(t);
-    // K pieces size their partials per item (tactic_ws_floats); the plan still
-    // keeps room for the stream-K kernel of the same MMA width (headroom rule).
+    // K pieces exchange their partials through their own region (tactic_xch_words);
+    // the plan still keeps room for the stream-K kernel of the same MMA width
+    // (headroom rule).
     case DEP_KIND_TC_SPLIT: return dep::tc_ws_per_cta(t);
     default: return 0;  // whole rows: no partials
     }
@@ -109,8 +112,14 @@ int64_t effective_ctas(const dep_tactic_t &t, int64_t N, int64_t K)
 size_t tactic_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K)
 {
     if (t.kind == DEP_KIND_TC_SPLIT)
-        return dep::tcs_ws_floats(t, N, K);
+        return 0;
     return (size_t)effective_ctas(t, N, K) * ws_per_cta(t);
+}
+
+// K-piece exchange words a launch of tactic t may use.
+size_t tactic_xch_words(const dep_tactic_t &t, int64_t N, int64_t K)
+{
+    return t.kind == DEP_KIND_TC_SPLIT ? dep::tcs_xch_words(t, N, K) : 0;
 }
 
 size_t tactic_counters(const dep_tactic_t &t, int64_t N)
@@ -250,25 +259,28 @@ const dep_tactic_t *lookup(const dep_plan_s *p, int32_t B)
 }
 
 // Allocate (or re-allocate) the plan's device block for its current table.
-dep_status_t allocate_device(dep_plan_s *p, size_t extra_ws_floats = 0, size_t extra_counters = 0)
+dep_status_t allocate_device(dep_plan_s *p, size_t extra_ws_floats = 0, size_t extra_counters = 0,
+                             size_t extra_xch_words = 0)
 {
     // Room for the table's tactics, for any tactic of the same per-block
     // footprint on up to one block per SM, and for FMA-sized footprints on up to
     // four blocks per SM (explicit tactics of tests and tuning use other grids).
     size_t ws = std::max(extra_ws_floats, (size_t)4 * (size_t)p->sm_count * 512);
     size_t cnt = std::max<size_t>(256, extra_counters);
+    size_t xw = extra_xch_words;
     int32_t rows = 1;
     for (const auto &t : p->table) {
         ws = std::max(ws, tactic_ws_floats(t, p->N, p->K));
         ws = std::max(ws, (size_t)p->sm_count * ws_per_cta(t));
         cnt = std::max(cnt, tactic_counters(t, p->N));
+        xw = std::max(xw, tactic_xch_words(t, p->N, p->K));
         rows = std::max(rows, t.max_rows);
     }
     auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
-    const size_t status_b = 256, cnt_b = up(cnt * sizeof(int)), ws_b = up(ws * sizeof(float));
+    const size_t status_b = 256, cnt_b = up(cnt * sizeof(int)), xch_b = up(xw * 8), ws_b = up(ws * sizeof(float));
     const size_t xs_b = up((size_t)rows * p->K * 2), ys_b = up((size_t)rows * p->N * 2);
-    const size_t total = status_b + cnt_b + ws_b + xs_b + ys_b;
-    if (p->dev_block && cnt <= p->n_counters && ws <= p->ws_floats && rows <= p->stage_rows)
+    const size_t total = status_b + cnt_b + xch_b + ws_b + xs_b + ys_b;
+    if (p->dev_block && cnt <= p->n_counters && xw <= p->xch_words && ws <= p->ws_floats && rows <= p->stage_rows)
         return DEP_OK;  // the current block already has room for every part
     if (env_is("DEP_FAULT", "alloc"))
         return DEP_ERR_OOM;
@@ -277,7 +289,7 @@ dep_status_t allocate_device(dep_plan_s *p, size_t extra_ws_floats = 0, size_t e
         cudaGetLastError();
         return DEP_ERR_OOM;
     }
-    if (cudaMemset(blk, 0, status_b + cnt_b) != cudaSuccess) {
+    if (cudaMemset(blk, 0, status_b + cnt_b + xch_b) != cudaSuccess) {  // status, counters, exchange flags
         cudaFree(blk);
         return DEP_ERR_CUDA;
     }
@@ -291,10 +303,12 @@ dep_status_t allocate_device(dep_plan_s *p, size_t extra_ws_floats = 0, size_t e
     p->status = reinterpret_cast<int *>(c);
     p->counters = reinterpret_cast<int *>(c + status_b);
     p->n_counters = cnt_b / sizeof(int);
-    p->ws = reinterpret_cast<float *>(c + status_b + cnt_b);
+    p->xch = reinterpret_cast<unsigned long long *>(c + status_b + cnt_b);
+    p->xch_words = xch_b / 8;
+    p->ws = reinterpret_cast<float *>(c + status_b + cnt_b + xch_b);
     p->ws_floats = ws_b / sizeof(float);
-    p->x_stage = reinterpret_cast<uint16_t *>(c + status_b + cnt_b + ws_b);
-    p->y_stage = reinterpret_cast<uint16_t *>(c + status_b + cnt_b + ws_b + xs_b);
+    p->x_stage = reinterpret_cast<uint16_t *>(c + status_b + cnt_b + xch_b + ws_b);
+    p->y_stage = reinterpret_cast<uint16_t *>(c + status_b + cnt_b + xch_b + ws_b + xs_b);
     p->stage_rows = rows;
     return DEP_OK;
 }
@@ -406,7 +420,8 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
         cudaGetLastError();
         return DEP_ERR_INVALID_ARG;
     }
-    if (tactic_ws_floats(*t, p->N, p->K) > p->ws_floats || tactic_counters(*t, p->N) > p->n_counters)
+    if (tactic_ws_floats(*t, p->N, p->K) > p->ws_floats || tactic_counters(*t, p->N) > p->n_counters ||
+        tactic_xch_words(*t, p->N, p->K) > p->xch_words)
         return DEP_ERR_INVALID_ARG;
     if (p->fault_launch)
         return DEP_ERR_CUDA;
@@ -421,6 +436,8 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
     a.ws_floats = p->ws_floats;
     a.counters = p->counters;
     a.n_counters = p->n_counters;
+    a.xch = p->xch;
+    a.xch_words = p->xch_words;
     a.status = p->status;
     a.stream = static_cast<cudaStream_t>(stream);
     a.wait_limit_ns = p->wait_limit_ns;
@@ -493,13 +510,13 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
                 for (int32_t sp : pieces)
                     c.push_back(tcs_tactic(rows, cols, st, sm_count, tk, sp, bm));
     }
-    // K pieces keep every piece's partial: leave out tactics whose partials
-    // would take more than 64 MB of workspace.
-    constexpr size_t kMaxPieceWorkspaceFloats = (64u << 20) / sizeof(float);
+    // K pieces keep every piece's partial: leave out tactics whose exchange words
+    // would take more than 64 MB.
+    constexpr size_t kMaxPieceWords = (64u << 20) / 8;
     std::vector<dep_tactic_t> ok;
     for (const auto &t : c)
         if (tactic_valid(t) && (t.kind != DEP_KIND_ROWS || dep::rows_fits(t, K)) &&
-            (t.kind != DEP_KIND_TC_SPLIT || tactic_ws_floats(t, N, K) <= kMaxPieceWorkspaceFloats))
+            (t.kind != DEP_KIND_TC_SPLIT || tactic_xch_words(t, N, K) <= kMaxPieceWords))
             ok.push_back(t);
     return ok;
 }
@@ -510,17 +527,18 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
 dep_status_t tune_plan(dep_plan_s *p)
 {
     std::vector<std::vector<dep_tactic_t>> cands;
-    size_t ws_need = 0, cnt_need = 0;
+    size_t ws_need = 0, cnt_need = 0, xch_need = 0;
     int32_t rows_max = 1;
     for (const auto &t : p->table) {
         cands.push_back(candidates(t.max_rows, p->N, p->K, p->sm_count));
         for (const auto &c : cands.back()) {
             ws_need = std::max(ws_need, tactic_ws_floats(c, p->N, p->K));
             cnt_need = std::max(cnt_need, tactic_counters(c, p->N));
+            xch_need = std::max(xch_need, tactic_xch_words(c, p->N, p->K));
         }
         rows_max = std::max(rows_max, t.max_rows);
     }
-    dep_status_t st = allocate_device(p, ws_need, cnt_need);
+    dep_status_t st = allocate_device(p, ws_need, cnt_need, xch_need);
     if (st != DEP_OK)
         return st;
     int l2 = 0;
@@ -758,6 +776,23 @@ dep_status_t dep_projection_plan_partials(dep_plan_t plan, void *host, size_t by
     return DEP_OK;
 }
 
+dep_status_t dep_projection_plan_exchange(dep_plan_t plan, void *host, size_t bytes, size_t *written)
+{
+    if (!plan || !written || (bytes && !host))
+        return DEP_ERR_INVALID_ARG;
+    *written = 0;
+    if (plan->host_only)
+        return DEP_ERR_UNSUPPORTED;
+    const size_t n = std::min(bytes, plan->xch_words * 8);
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        (n && cudaMemcpy(host, plan->xch, n, cudaMemcpyDeviceToHost) != cudaSuccess)) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    *written = n;
+    return DEP_OK;
+}
+
 dep_status_t dep_projection_plan_workspace(dep_plan_t plan, size_t *bytes)
 {
     if (!plan || !bytes)
@@ -868,6 +903,13 @@ dep_status_t dep_projection_device_status(dep_plan_t plan, void *stream, int32_t
     if (cudaStreamSynchronize(s) != cudaSuccess ||
         cudaMemcpy(&h, plan->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
         cudaMemset(plan->status, 0, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    // After a give-up, counters and exchange flags may be left mid-protocol:
+    // clear them so that the plan's next runs start from a clean state.
+    if (h && (cudaDeviceSynchronize() != cudaSuccess ||
+              cudaMemset(plan->counters, 0, plan->n_counters * sizeof(int) + plan->xch_words * 8) != cudaSuccess)) {
         cudaGetLastError();
         return DEP_ERR_CUDA;
     }

@@ -23,6 +23,8 @@ struct RunArgs {
     size_t ws_floats;
     int *counters;      // per-tile arrival counters (zero between launches)
     size_t n_counters;
+    unsigned long long *xch = nullptr;  // K-piece exchange words (flags clear between launches)
+    size_t xch_words = 0;
     int *status;        // device status word (0 = fine)
     cudaStream_t stream;
     uint64_t wait_limit_ns;
@@ -160,8 +162,8 @@ cudaError_t tc_run(const dep_tactic_t &t, const RunArgs &a);
 
 // ---- tcgen05 tactic with fixed K pieces, dynamically scheduled (tc_split.cu) ----
 bool tcs_valid(const dep_tactic_t &t);
-size_t tcs_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K);  // every piece's partial
-size_t tcs_counters(const dep_tactic_t &t, int64_t N);               // includes the last 2 counters
+size_t tcs_xch_words(const dep_tactic_t &t, int64_t N, int64_t K);  // every piece's exchange word
+size_t tcs_counters(const dep_tactic_t &t, int64_t N);               // the last 2 counters
 int tcs_blocks_per_sm(const dep_tactic_t &t);
 cudaError_t tcs_run(const dep_tactic_t &t, const RunArgs &a);       // uses the last 2 counters
 

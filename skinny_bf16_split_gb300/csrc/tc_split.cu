@@ -16,12 +16,20 @@
 //  * Swap-AB MMAs as in the stream-K kernel: M = 128 weight rows, N = the batch
 //    padded to NT, K = 16 per instruction; 128-byte-swizzled TMA stages of
 //    tile_k / 64 slices; accumulators in TMEM, two buffers of NT columns.
-//  * Every piece's FP32 partial goes to its own workspace slot [item][b][row];
-//    the last epilogue warp to arrive on the tile's integer counter adds the S
-//    partials in piece order 0..S-1 and rounds to BF16.  Which block ran which
-//    piece does not enter the arithmetic, so results are identical from run to
-//    run and equal to BF16 of the ordered FP32 sum of the pieces.  With S = 1 a
-//    tile is one item and y is stored directly (no workspace, no counter).
+//  * Pieces are exchanged through the plan's exchange region, one 64-bit word
+//    per (tile, piece, b, row): the FP32 partial in the low half and a "full"
+//    flag in the high half, written by one single-copy-atomic store (no fence,
+//    no atomic counter).  The block that runs the last piece of a tile reduces:
+//    it waits (bounded) until the words of pieces 0..S-2 are full, adds them in
+//    piece order and its own piece last, rounds to BF16, and clears the flags
+//    for the next launch (the values stay for inspection).  Which block ran
+//    which piece does not enter the arithmetic, so results are identical from
+//    run to run and equal to BF16 of the ordered FP32 sum of the pieces.  With
+//    S = 1 a tile is one item and y is stored directly.
+//    No deadlock: items are handed out in increasing order and the pieces of a
+//    tile precede its last piece, so every piece a reducer waits for is already
+//    held by a running block (or was run earlier by the same block), and the
+//    earliest pending reduction never waits on a later one.
 //  * Warp roles: warp 0 TMA producer (takes the items), warp 1 TMEM owner and
 //    MMA issuer, warps 2-5 epilogue.  The producer tags each stage with its item
 //    and first/last flags; the MMA issuer passes the item of each finished
@@ -69,11 +77,25 @@ __device__ __forceinline__ uint16_t to_bf16(float v)
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+// Exchange words: value bits | kFull.  Relaxed GPU-scope accesses (coherent in
+// L2, single-copy atomic for an aligned 64-bit word).
+constexpr unsigned long long kFull = 1ull << 32;
+__device__ __forceinline__ unsigned long long ld_word(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_word(unsigned long long *p, unsigned long long v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 template <int NT, int BM>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_split_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms, int S,
-                    float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ dispenser,
+                    unsigned long long *__restrict__ xch, int *__restrict__ dispenser,
                     int *__restrict__ status, uint64_t limit_ns)
 {
     using Sh = SplitShape<NT, BM>;
@@ -281,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue warps ----------------
-        griddep_wait();  // workspace, counters and y may still be in use by the preceding grid
+        griddep_wait();  // the exchange words and y may still be in use by the preceding grid
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         // M = 128: tile row r is TMEM lane r.  M = 64: rows 16q..16q+15 are lanes
         // 0-15 of quadrant q (lanes 16-31 hold nothing of this MMA).
@@ -306,76 +328,96 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             accf_ph ^= 1u << buf;
             tc::fence_after();
-            const int t = item / S;
+            const int t = item / S, piece = item % S;
             const int64_t n = (int64_t)t * BM + row;
             const bool mine = has_row && n < N;  // this lane's output row exists
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NT);
-            float *part = ws + (int64_t)item * NT * BM + row;
+            // tile t's exchange words, [piece][b][row]
+            unsigned long long *tile_x = xch + (int64_t)t * S * NT * BM + row;
+            bool ok = true;
 #pragma unroll 1
-            for (int c0 = 0; c0 < NT; c0 += 16) {
+            for (int c0 = 0; c0 < NT && c0 < B; c0 += 16) {
+                __syncwarp();  // tcgen05.ld is warp-collective: every lane, converged
                 uint32_t v[16];
                 tc::ld16(taddr + (uint32_t)c0, v);
                 tc::wait_ld();
+                if (S == 1) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int b = c0 + j;
-                    if (b < B && has_row) {
-                        const float f = __uint_as_float(v[j]);
-                        if (S == 1) {
-                            if (n < N)
-                                y[(int64_t)b * N + n] = to_bf16(f);
-                        } else {
-                            __stcg(part + (int64_t)b * BM, f);
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < B && mine)
+                            y[(int64_t)(c0 + j) * N + n] = to_bf16(__uint_as_float(v[j]));
+                    continue;
+                }
+                unsigned long long *own = tile_x + ((int64_t)piece * NT + c0) * BM;
+                if (piece != S - 1) {  // publish this piece
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (c0 + j < B && has_row)
+                            st_word(own + (int64_t)j * BM, kFull | v[j]);
+                    continue;
+                }
+                if (!has_row)
+                    continue;  // (lanes 16-31 of an M = 64 tile; the warp reconverges above)
+                // Reduce: own piece kept for inspection (flag clear), then pieces
+                // 0..S-2 in order, two at a time, each once its words are full.
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (c0 + j < B)
+                        st_word(own + (int64_t)j * BM, (unsigned long long)v[j]);
+                float sum[16];
+                for (int p0 = 0; p0 < S - 1; p0 += 2) {
+                    unsigned long long w[2][16];
+                    unsigned long long *src[2];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        src[i] = tile_x + ((int64_t)(p0 + i) * NT + c0) * BM;
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            w[i][j] = (p0 + i < S - 1 && c0 + j < B) ? ld_word(src[i] + (int64_t)j * BM) : kFull;
+                    }
+                    uint64_t t0 = 0;
+                    for (;;) {  // bounded wait for the other pieces
+                        bool all = true;
+#pragma unroll
+                        for (int i = 0; i < 2; ++i)
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (!(w[i][j] & kFull)) {
+                                    all = false;
+                                    w[i][j] = ld_word(src[i] + (int64_t)j * BM);
+                                }
+                        if (all)
+                            break;
+                        const uint64_t now = globaltimer_ns();
+                        if (!t0) {
+                            t0 = now;
+                        } else if (now - t0 > limit_ns) {
+                            record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
+                            ok = false;
+                            break;
                         }
                     }
+#pragma unroll
+                    for (int i = 0; i < 2; ++i)
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            if (p0 + i < S - 1) {
+                                const float f = __uint_as_float((uint32_t)w[i][j]);
+                                sum[j] = (p0 + i == 0) ? f : sum[j] + f;
+                                if (c0 + j < B)  // clear the flag for the next launch
+                                    st_word(src[i] + (int64_t)j * BM, w[i][j] & 0xFFFFFFFFull);
+                            }
                 }
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (c0 + j < B && mine && ok)
+                        y[(int64_t)(c0 + j) * N + n] = to_bf16(sum[j] + __uint_as_float(v[j]));
             }
             tc::fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(acce0 + 8 * buf);
             buf ^= 1;
-            if (S == 1)
-                continue;
-            __threadfence();
-            __syncwarp();
-            int prev = 0;
-            if (lane == 0)
-                prev = atomicAdd(&counters[t * kEpiWarps + q], 1);
-            prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
-            if (prev != S - 1)
-                continue;  // another piece of this tile is still running
-            __threadfence();
-            if (mine) {
-                // Sum the pieces in order 0..S-1; the loads of up to 4 pieces x 16
-                // batch columns are issued together, then added.
-                const float *tile_ws = ws + (int64_t)t * S * NT * BM + row;
-                for (int b0 = 0; b0 < B; b0 += 16) {
-                    float sum[16];
-                    for (int p0 = 0; p0 < S; p0 += 4) {
-                        float pv[4][16];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float *src = tile_ws + ((int64_t)(p0 + i) * NT + b0) * BM;
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                pv[i][j] = (p0 + i < S && b0 + j < B) ? __ldcg(src + (int64_t)j * BM) : 0.0f;
-                        }
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                if (p0 + i < S)
-                                    sum[j] = (p0 + i == 0) ? pv[i][j] : sum[j] + pv[i][j];
-                    }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (b0 + j < B)
-                            y[(int64_t)(b0 + j) * N + n] = to_bf16(sum[j]);
-                }
-            }
-            if (lane == 0)
-                counters[t * kEpiWarps + q] = 0;  // ready for the next launch
         }
     }
 
@@ -435,8 +477,8 @@ cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
         e = launch(tc_split_kernel<NT, BM>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
-                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, S, a.ws, a.counters,
-                   dispenser, a.status, a.wait_limit_ns);
+                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, S, a.xch, dispenser,
+                   a.status, a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }
@@ -501,15 +543,15 @@ bool tcs_valid(const dep_tactic_t &t)
     return smem != 0 && smem <= (size_t)kMaxDynamicSmem;
 }
 
-size_t tcs_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K)
+size_t tcs_xch_words(const dep_tactic_t &t, int64_t N, int64_t K)
 {
     const int64_t S = effective_splits(t, K);
     return S > 1 ? (size_t)tiles_of(t, N) * (size_t)S * (size_t)t.cols * (size_t)t.tile_n : 0;
 }
 
-size_t tcs_counters(const dep_tactic_t &t, int64_t N)
+size_t tcs_counters(const dep_tactic_t &, int64_t)
 {
-    return (size_t)tiles_of(t, N) * kEpiWarps + 2;  // + the item counter pair at the end
+    return 2;  // the item counter pair at the end
 }
 
 int tcs_blocks_per_sm(const dep_tactic_t &t)

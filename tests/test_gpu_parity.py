@@ -717,9 +717,9 @@ def test_tcs_one_piece_equals_whole_tile_stream_k(dep, NT, B, tile_k):
                                                    (64, 64, 4, 128, 128), (256, 200, 2, 64, 128),
                                                    (16, 16, 4, 256, 64), (32, 20, 3, 128, 64)])
 def test_tcs_fixup_bitexact_from_partials(dep, NT, B, splits, tile_k, BM):
-    """The K pieces' FP32 partials left in the workspace, added in piece order
-    0..S-1 in float32 and rounded to BF16 (nearest, ties to even), give y bit
-    for bit."""
+    """The K pieces' FP32 partials left in the exchange words, added in piece
+    order 0..S-1 in float32 and rounded to BF16 (nearest, ties to even), give y
+    bit for bit; every "full" flag is clear once the launch has finished."""
     N, K = 1000, 4096
     plan = tcs_plan(dep, N, K, [tcs_tactic(dep, NT, sm_count(), splits, 2, tile_k, tile_n=BM)])
     try:
@@ -728,7 +728,9 @@ def test_tcs_fixup_bitexact_from_partials(dep, NT, B, splits, tile_k, BM):
         y = run(dep, plan, x, W, N, tcs_tactic(dep, NT, sm_count(), splits, 2, tile_k, tile_n=BM))
         T = -(-N // BM)
         S = min(splits, -(-K // tile_k))
-        ws = dep.dep_projection_plan_partials(plan, T * S * NT * BM).reshape(T, S, NT, BM)
+        words = dep.dep_projection_plan_exchange(plan, T * S * NT * BM).reshape(T, S, NT, BM)
+        assert not (words[:, :, :B, :] >> np.uint64(32)).any()  # flags cleared for the next launch
+        ws = (words & np.uint64(0xFFFFFFFF)).astype(np.uint32).view(np.float32)
         rows = np.arange(BM)
         for t in range(T):
             n = t * BM + rows
