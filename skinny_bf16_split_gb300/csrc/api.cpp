@@ -196,15 +196,16 @@ int32_t tc_default_stages(int32_t cols)
 // for the smallest batches, the GEMM path past them; the split point moves to
 // where each kernel measured fastest on this GPU):
 //  * one or two x rows: whole weight rows on the FMA pipe (no cross-block split);
-//  * up to 16 rows (a 16-wide MMA) while the 128-row tiles fit on the SMs: the
-//    tensor cores over fixed K pieces, SMs / tiles pieces per tile (o_proj: 2,
-//    DSA: 1), one item per block;
-//  * otherwise the stream-K tensor-core kernel, one block per tile when the
+//  * up to 16 rows (a 16-wide MMA): the tensor cores over fixed K pieces taken
+//    dynamically -- SMs / tiles pieces per 128-row tile while the tiles fit on
+//    the SMs (o_proj: 2, DSA: 1, one item per block), 3 pieces otherwise (KDA:
+//    386 tiles, 1158 items);
+//  * wider batches: the stream-K tensor-core kernel, one block per tile when the
 //    tiles nearly fill the GPU.
 // Measured on GB300 (per call, CUDA events): at 4 rows the K-piece tensor-core
 // tactic is 1.9-2.8 us faster than the stream-K FMA kernel on all three
-// weights; at 8 and 16 rows it is 0.7-1.0 us faster than the stream-K
-// tensor-core kernel for o_proj and DSA and equal for KDA (386 tiles).
+// weights; at 4-16 rows it is 1.3-2.3 us faster than the stream-K tensor-core
+// kernel for o_proj, equal for DSA and up to 1.7 us faster for KDA.
 dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
 {
     if (rows <= 2) {
@@ -221,8 +222,9 @@ dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
     const int64_t tiles = (N + 127) / 128;
     // Widest stage (most contiguous bytes per weight row) that still leaves a
     // ring of at least three stages.
-    if (cols == 16 && tiles <= sm_count) {
-        const int32_t splits = (int32_t)std::min<int64_t>(64, std::max<int64_t>(1, sm_count / tiles));
+    if (cols == 16) {
+        const int32_t splits =
+            tiles <= sm_count ? (int32_t)std::min<int64_t>(64, std::max<int64_t>(1, sm_count / tiles)) : 3;
         for (int32_t tk : {256, 128})
             for (int32_t st : {6, 5, 4, 3}) {
                 const dep_tactic_t t = tcs_tactic(rows, cols, st, sm_count, tk, splits, 128);

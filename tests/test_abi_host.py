@@ -66,6 +66,17 @@ def test_default_table_follows_split_rule(dep):
         dep.dep_projection_plan_destroy(plan)
 
 
+def test_default_many_tiles_take_three_pieces(dep):
+    plan = dep.dep_projection_plan_host(49376, 7168, [1, 4, 16, 32], 152)
+    try:
+        kinds = {t.max_rows: (t.kind, t.splits) for t in dep.dep_projection_plan_table(plan)}
+        assert kinds[1] == (dep.DEP_KIND_ROWS, 0)
+        assert kinds[4] == kinds[16] == (dep.DEP_KIND_TC_SPLIT, 3)  # 386 tiles > 152 SMs
+        assert kinds[32] == (dep.DEP_KIND_TC, 0)
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
 def test_default_batches_when_none_given(dep):
     plan = dep.dep_projection_plan_host(14560, 7168, [], 152)
     try:
