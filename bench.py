@@ -52,8 +52,8 @@ WORKLOAD_TEXT = {
 # Workloads whose plan is tuned by default (the verify-step tables are measured).
 TUNED_BY_DEFAULT = {"dsa_verify", "tp_sharded"}
 # Sources each kernel family is built from (a traffic record is stale once they change).
-KERNEL_SOURCES = {"splitk_fma": ["splitk_fma.cu"], "tc_gemm": ["tc_gemm.cu"], "tc_split": ["tc_split.cu"],
-                  "rows_gemv": ["rows_gemv.cu"]}
+KERNEL_SOURCES = {"splitk_fma": ["splitk_fma.cu"], "tc_gemm": ["tc_gemm.cu", "exchange.cuh"],
+                  "tc_split": ["tc_split.cu", "exchange.cuh"], "rows_gemv": ["rows_gemv.cu"]}
 SHARED_SOURCES = ["ptx.cuh", "internal.h"]
 
 

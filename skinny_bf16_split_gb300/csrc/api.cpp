@@ -90,12 +90,7 @@ size_t ws_per_cta(const dep_tactic_t &t)
 {
     switch (t.kind) {
     case DEP_KIND_SPLITK_FMA: return dep::fma_ws_per_cta(t);
-    case DEP_KIND_TC: return dep::tc_ws_per_cta(t);
-    // K pieces exchange their partials through their own region (tactic_xch_words);
-    // the plan still keeps room for the stream-K kernel of the same MMA width
-    // (headroom rule).
-    case DEP_KIND_TC_SPLIT: return dep::tc_ws_per_cta(t);
-    default: return 0;  // whole rows: no partials
+    default: return 0;  // whole rows: no partials; tensor cores: exchange words instead
     }
 }
 
@@ -116,17 +111,19 @@ size_t tactic_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K)
     return (size_t)effective_ctas(t, N, K) * ws_per_cta(t);
 }
 
-// K-piece exchange words a launch of tactic t may use.
+// Exchange words a launch of tactic t may use (tensor-core kinds).
 size_t tactic_xch_words(const dep_tactic_t &t, int64_t N, int64_t K)
 {
-    return t.kind == DEP_KIND_TC_SPLIT ? dep::tcs_xch_words(t, N, K) : 0;
+    return t.kind == DEP_KIND_TC_SPLIT ? dep::tcs_xch_words(t, N, K)
+           : t.kind == DEP_KIND_TC     ? dep::tc_xch_words(t, N, K)
+                                       : 0;
 }
 
 size_t tactic_counters(const dep_tactic_t &t, int64_t N)
 {
     switch (t.kind) {
     case DEP_KIND_SPLITK_FMA: return dep::fma_counters(t, N);
-    case DEP_KIND_TC: return dep::tc_counters(t, N);
+    case DEP_KIND_TC: return 0;  // the exchange words need no counters
     case DEP_KIND_TC_SPLIT: return dep::tcs_counters(t, N);
     default: return 2;  // tile dispenser and finish count (the last two counters)
     }
@@ -276,6 +273,8 @@ dep_status_t allocate_device(dep_plan_s *p, size_t extra_ws_floats = 0, size_t e
         ws = std::max(ws, (size_t)p->sm_count * ws_per_cta(t));
         cnt = std::max(cnt, tactic_counters(t, p->N));
         xw = std::max(xw, tactic_xch_words(t, p->N, p->K));
+        if (t.kind == DEP_KIND_TC || t.kind == DEP_KIND_TC_SPLIT)  // room for stream-K on every SM
+            xw = std::max(xw, (size_t)p->sm_count * dep::tc_xch_words_per_cta(t));
         rows = std::max(rows, t.max_rows);
     }
     auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };

@@ -155,8 +155,8 @@ cudaError_t selftest_timeout(int32_t limit_us, int32_t *code);
 // ---- tcgen05 tactic (tc_gemm.cu) ----
 bool tc_valid(const dep_tactic_t &t);
 int64_t tc_units(const dep_tactic_t &t, int64_t N, int64_t K);
-size_t tc_ws_per_cta(const dep_tactic_t &t);
-size_t tc_counters(const dep_tactic_t &t, int64_t N);
+size_t tc_xch_words_per_cta(const dep_tactic_t &t);              // exchange words per block
+size_t tc_xch_words(const dep_tactic_t &t, int64_t N, int64_t K);  // exchange words of a launch
 int tc_blocks_per_sm(const dep_tactic_t &t);
 cudaError_t tc_run(const dep_tactic_t &t, const RunArgs &a);
 

@@ -21,13 +21,20 @@
 //  * Warps 2-5: epilogue.  Each owns the 32 TMEM lanes (= weight rows) of its
 //    quadrant, reads its accumulator with tcgen05.ld, frees it for the MMA of
 //    the next-but-one segment, and either stores BF16 y (segment = whole tile)
-//    or writes FP32 partials for the split-K fix-up: the last warp to arrive on
-//    the tile's counter adds the partials in increasing block order.  No float
-//    atomics and no inter-block waits: results are identical from run to run.
+//    or exchanges FP32 partials for the split-K reduction through flagged
+//    64-bit words (exchange.cuh): every block publishes at most one piece (in
+//    its slot 0) -- the segment of a split tile whose last unit it does not
+//    own; the block owning the tile's last unit reduces, adding the pieces in
+//    increasing block order, its own last (kept in its slot 1 for inspection).  The other blocks meet that
+//    tile as the last tile of their range, which they visit first, so they
+//    publish before doing anything else and never wait: no deadlock, and the
+//    reducer's words are usually ready when it gets there.  No float atomics:
+//    results are identical from run to run.
 //  * Every wait is bounded in time; on a give-up the block records a code,
 //    lets every role finish, waits for its MMAs and copies, and frees TMEM.
 #include <cuda_bf16.h>
 
+#include "exchange.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -59,7 +66,7 @@ template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms,
-                   float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ status,
+                   unsigned long long *__restrict__ xch, int *__restrict__ status,
                    uint64_t limit_ns)
 {
     using S = TcShape<NT>;
@@ -236,10 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ---------------- epilogue warps ----------------
-        griddep_wait();  // workspace, counters and y may still be in use by the preceding grid
+        griddep_wait();  // the exchange words and y may still be in use by the preceding grid
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         const int row = 32 * q + lane;
-        const int64_t first_t = u_begin / KTILES;
         uint32_t accf_ph = 0;
         int buf = 0;
         const SegOrder order(u_begin, u_end, KTILES);
@@ -255,76 +261,46 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_after();
             const int64_t n = t * kBM + row;
             const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NT);
-            const int slot = (t == first_t) ? 0 : 1;
-            float *part = ws + ((c * 2 + slot) * NT) * kBM + row;
+            // Pieces of tile t: the segments of blocks c_first..c_last, in block order.
+            // Exchange words: [block][slot][b][row]; slot 0 published, slot 1 own.
+            const int64_t c_first = sk_owner(t * KTILES, U, C);
+            const int64_t c_last = sk_owner(t * KTILES + KTILES - 1, U, C);
+            bool ok = true;
 #pragma unroll 1
-            for (int c0 = 0; c0 < NT; c0 += 16) {
+            for (int c0 = 0; c0 < NT && c0 < B; c0 += 16) {
+                __syncwarp();  // tcgen05.ld is warp-collective: every lane, converged
                 uint32_t v[16];
                 tc::ld16(taddr + (uint32_t)c0, v);
                 tc::wait_ld();
+                const int ncols = B - c0 < 16 ? B - c0 : 16;
+                if (whole) {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int b = c0 + j;
-                    if (b < B) {
-                        const float f = __uint_as_float(v[j]);
-                        if (whole) {
-                            if (n < N)
-                                y[(int64_t)b * N + n] = to_bf16(f);
-                        } else {
-                            __stcg(part + (int64_t)b * kBM, f);
-                        }
-                    }
+                    for (int j = 0; j < 16; ++j)
+                        if (j < ncols && n < N)
+                            y[(int64_t)(c0 + j) * N + n] = to_bf16(__uint_as_float(v[j]));
+                    continue;
                 }
+                if (c != c_last) {  // publish this block's piece
+                    xch::publish16(xch + ((c * 2) * NT + c0) * kBM + row, kBM, v, ncols);
+                    continue;
+                }
+                float sum[16];
+                if (!xch::reduce16(xch + ((c_first * 2) * NT + c0) * kBM + row, 2 * (int64_t)NT * kBM, kBM,
+                                   (int)(c_last - c_first), ncols, v, xch + ((c * 2 + 1) * NT + c0) * kBM + row,
+                                   sum, limit_ns)) {
+                    record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
+                    ok = false;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (j < ncols && n < N && ok)
+                        y[(int64_t)(c0 + j) * N + n] = to_bf16(sum[j]);
             }
             tc::fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(acce0 + 8 * buf);
             buf ^= 1;
-            if (whole)
-                continue;
-            __threadfence();
-            __syncwarp();
-            int prev = 0;
-            if (lane == 0)
-                prev = atomicAdd(&counters[t * kEpiWarps + q], 1);
-            prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
-            const int64_t c_first = sk_owner(t * KTILES, U, C);
-            const int64_t c_last = sk_owner(t * KTILES + KTILES - 1, U, C);
-            if (prev != (int)(c_last - c_first))
-                continue;  // another block finishes this tile
-            __threadfence();
-            if (n < N) {
-                // Sum the segments in increasing block order.  The loads of up to
-                // 4 segments x 16 batch columns are issued together, then added.
-                for (int b0 = 0; b0 < B; b0 += 16) {
-                    float sum[16];
-                    for (int64_t g0 = c_first; g0 <= c_last; g0 += 4) {
-                        float p[4][16];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int64_t cc = g0 + i;
-                            const int sl = (t == sk_begin(cc, U, C) / KTILES) ? 0 : 1;
-                            const float *src = ws + ((cc * 2 + sl) * NT + b0) * kBM + row;
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                p[i][j] = (cc <= c_last && b0 + j < B) ? __ldcg(src + (int64_t)j * kBM) : 0.0f;
-                        }
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                if (g0 + i <= c_last)
-                                    sum[j] = (g0 + i == c_first) ? p[i][j] : sum[j] + p[i][j];
-                    }
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (b0 + j < B)
-                            y[(int64_t)(b0 + j) * N + n] = to_bf16(sum[j]);
-                }
-            }
-            if (lane == 0)
-                counters[t * kEpiWarps + q] = 0;  // ready for the next launch
         }
     }
 
@@ -372,8 +348,8 @@ cudaError_t run_nt(const dep_tactic_t &t, const RunArgs &a)
                            CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
         e = launch(tc_gemm_kernel<NT>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
-                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, a.ws, a.counters,
-                   a.status, a.wait_limit_ns);
+                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, a.xch, a.status,
+                   a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }
@@ -424,14 +400,16 @@ int64_t tc_units(const dep_tactic_t &t, int64_t N, int64_t K)
     return ((N + kBM - 1) / kBM) * ((K + t.tile_k - 1) / t.tile_k);
 }
 
-size_t tc_ws_per_cta(const dep_tactic_t &t)
+size_t tc_xch_words_per_cta(const dep_tactic_t &t)
 {
-    return 2 * (size_t)t.cols * kBM;  // head and tail segment partials
+    return 2 * (size_t)t.cols * kBM;  // slot 0 published piece, slot 1 own piece
 }
 
-size_t tc_counters(const dep_tactic_t &, int64_t N)
+size_t tc_xch_words(const dep_tactic_t &t, int64_t N, int64_t K)
 {
-    return (size_t)((N + kBM - 1) / kBM) * kEpiWarps;
+    const int64_t T = (N + kBM - 1) / kBM, U = tc_units(t, N, K);
+    const int64_t C = U < t.ctas ? U : t.ctas;
+    return C == T ? 0 : (size_t)C * tc_xch_words_per_cta(t);  // one block per tile: no split
 }
 
 int tc_blocks_per_sm(const dep_tactic_t &t)

@@ -38,6 +38,7 @@
 //    every role finish, waits for its MMAs and copies, and frees TMEM.
 #include <cuda_bf16.h>
 
+#include "exchange.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -77,19 +78,6 @@ __device__ __forceinline__ uint16_t to_bf16(float v)
     return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-// Exchange words: value bits | kFull.  Relaxed GPU-scope accesses (coherent in
-// L2, single-copy atomic for an aligned 64-bit word).
-constexpr unsigned long long kFull = 1ull << 32;
-__device__ __forceinline__ unsigned long long ld_word(const unsigned long long *p)
-{
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_word(unsigned long long *p, unsigned long long v)
-{
-    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
 
 template <int NT, int BM>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -349,69 +337,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
                 unsigned long long *own = tile_x + ((int64_t)piece * NT + c0) * BM;
+                const int ncols = B - c0 < 16 ? B - c0 : 16;
                 if (piece != S - 1) {  // publish this piece
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (c0 + j < B && has_row)
-                            st_word(own + (int64_t)j * BM, kFull | v[j]);
+                    if (has_row)
+                        xch::publish16(own, BM, v, ncols);
                     continue;
                 }
                 if (!has_row)
                     continue;  // (lanes 16-31 of an M = 64 tile; the warp reconverges above)
-                // Reduce: own piece kept for inspection (flag clear), then pieces
-                // 0..S-2 in order, two at a time, each once its words are full.
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (c0 + j < B)
-                        st_word(own + (int64_t)j * BM, (unsigned long long)v[j]);
+                // Reduce: pieces 0..S-2 in order, then this block's own piece.
                 float sum[16];
-                for (int p0 = 0; p0 < S - 1; p0 += 2) {
-                    unsigned long long w[2][16];
-                    unsigned long long *src[2];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        src[i] = tile_x + ((int64_t)(p0 + i) * NT + c0) * BM;
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            w[i][j] = (p0 + i < S - 1 && c0 + j < B) ? ld_word(src[i] + (int64_t)j * BM) : kFull;
-                    }
-                    uint64_t t0 = 0;
-                    for (;;) {  // bounded wait for the other pieces
-                        bool all = true;
-#pragma unroll
-                        for (int i = 0; i < 2; ++i)
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                if (!(w[i][j] & kFull)) {
-                                    all = false;
-                                    w[i][j] = ld_word(src[i] + (int64_t)j * BM);
-                                }
-                        if (all)
-                            break;
-                        const uint64_t now = globaltimer_ns();
-                        if (!t0) {
-                            t0 = now;
-                        } else if (now - t0 > limit_ns) {
-                            record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
-                            ok = false;
-                            break;
-                        }
-                    }
-#pragma unroll
-                    for (int i = 0; i < 2; ++i)
-#pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (p0 + i < S - 1) {
-                                const float f = __uint_as_float((uint32_t)w[i][j]);
-                                sum[j] = (p0 + i == 0) ? f : sum[j] + f;
-                                if (c0 + j < B)  // clear the flag for the next launch
-                                    st_word(src[i] + (int64_t)j * BM, w[i][j] & 0xFFFFFFFFull);
-                            }
+                if (!xch::reduce16(tile_x + (int64_t)c0 * BM, (int64_t)NT * BM, BM, S - 1, ncols, v, own, sum,
+                                   limit_ns)) {
+                    record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
+                    ok = false;
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    if (c0 + j < B && mine && ok)
-                        y[(int64_t)(c0 + j) * N + n] = to_bf16(sum[j] + __uint_as_float(v[j]));
+                    if (j < ncols && mine && ok)
+                        y[(int64_t)(c0 + j) * N + n] = to_bf16(sum[j]);
             }
             tc::fence_before();
             __syncwarp();

@@ -565,19 +565,20 @@ def test_rows_refuses_when_x_does_not_fit(dep):
 
 
 def _stream_k_segments(U, C, KT, t):
-    """Blocks whose ranges meet tile t's units, and their slot for t (stream-K split)."""
-    begin = lambda c: c * U // C  # noqa: E731
+    """Blocks whose ranges meet tile t's units, in block order, and the exchange slot
+    each left its piece in (stream-K split): 0 = published, 1 = the reducer's own."""
     owner = lambda u: ((u + 1) * C - 1) // U  # noqa: E731
     c0, c1 = owner(t * KT), owner(t * KT + KT - 1)
-    return [(c, 0 if begin(c) // KT == t else 1) for c in range(c0, c1 + 1)]
+    return [(c, 1 if c == c1 else 0) for c in range(c0, c1 + 1)]
 
 
 @pytest.mark.parametrize("NT,B,tile_k", [(16, 16, 256), (16, 5, 64), (32, 24, 128), (64, 64, 128)])
 def test_tc_fixup_bitexact_from_partials(dep, plan_cache, NT, B, tile_k):
     """The tensor cores' own summation order is not documented, but the split-K
     combination is the library's: for every tile split across blocks, the FP32
-    partials the blocks left in the workspace, added in increasing block order
-    and rounded to BF16 (nearest, ties to even), give y bit for bit."""
+    partials the blocks left in their exchange words, added in increasing block
+    order and rounded to BF16 (nearest, ties to even), give y bit for bit; every
+    "full" flag is clear once the launch has finished."""
     N, K = 1000, 4096
     plan = get_plan(dep, plan_cache, N, K, (256,))
     x = synth.normal_bf16(40 + NT, 2, (B, K))
@@ -587,8 +588,10 @@ def test_tc_fixup_bitexact_from_partials(dep, plan_cache, NT, B, tile_k):
     T, KT = -(-N // 128), -(-K // tile_k)
     U = T * KT
     C = min(C, U)
-    ws = dep.dep_projection_plan_partials(plan, C * 2 * NT * 128)
-    assert ws.size == C * 2 * NT * 128
+    words = dep.dep_projection_plan_exchange(plan, C * 2 * NT * 128)
+    assert words.size == C * 2 * NT * 128
+    assert not (words >> np.uint64(32)).any()  # flags cleared for the next launch
+    ws = (words & np.uint64(0xFFFFFFFF)).astype(np.uint32).view(np.float32)
     checked = 0
     for t in range(T):
         segs = _stream_k_segments(U, C, KT, t)
