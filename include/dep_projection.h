@@ -142,12 +142,19 @@ dep_status_t dep_projection_run_tactic(dep_plan_t plan, const dep_tactic_t *tact
                                        int32_t B, void *stream);
 
 /*
- * End-to-end call with the activations in host memory: copies x_host [B,K] to
+ * End-to-end call with the activations in host memory: brings x_host [B,K] to
  * the plan's device staging buffer, runs the projection against the resident
- * device weight W, and copies y back to y_host [B,N], all enqueued on `stream`
- * (pinned host memory makes the copies asynchronous).  The caller synchronises
- * the stream before reading y_host.  B must not exceed the plan's largest table
- * key (the staging capacity).  Errors as dep_projection_run.
+ * device weight W, and puts y back to y_host [B,N], all enqueued on `stream`.
+ * The caller synchronises the stream before reading y_host.  B must not exceed
+ * the plan's largest table key (the staging capacity).  Errors as
+ * dep_projection_run.
+ *   - Pinned host buffers (mapped into the device's address space, 16-byte
+ *     aligned): two small kernels read x_host and write y_host directly
+ *     (zero-copy), chained to the projection by programmatic dependent launch,
+ *     so the projection streams its first weight stages while x arrives.
+ *   - Any other host memory: cudaMemcpyAsync both ways.
+ *   Both give the same bits as dep_projection_run.  The environment variable
+ *   DEP_STAGING=copy forces the copy path (for comparisons).
  */
 dep_status_t dep_projection_run_host(dep_plan_t plan, const void *x_host, const void *W,
                                      void *y_host, int32_t B, void *stream);

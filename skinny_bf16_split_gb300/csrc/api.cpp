@@ -401,7 +401,8 @@ dep_status_t make_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_b
 }
 
 dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const void *W, void *y,
-                      int32_t B, void *stream)
+                      int32_t B, void *stream,
+                      bool force_pdl = false)
 {
     if (!p || B < 0)
         return DEP_ERR_INVALID_ARG;
@@ -442,7 +443,7 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
     a.status = p->status;
     a.stream = static_cast<cudaStream_t>(stream);
     a.wait_limit_ns = p->wait_limit_ns;
-    a.pdl = p->pdl;
+    a.pdl = p->pdl || force_pdl;
     if (t->kind == DEP_KIND_ROWS && !dep::rows_fits(*t, p->K))
         return DEP_ERR_UNSUPPORTED;  // x and the ring do not fit in shared memory for this K
     cudaError_t e = t->kind == DEP_KIND_SPLITK_FMA ? dep::fma_run(*t, a)
@@ -699,6 +700,33 @@ dep_status_t dep_projection_run_host(dep_plan_t plan, const void *x_host, const 
         return DEP_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t xb = (size_t)B * plan->K * 2, yb = (size_t)B * plan->N * 2;
+    // Pinned (mapped) host buffers: zero-copy staging kernels chained to the
+    // projection by programmatic dependent launch.  Anything else: memcpys.
+    cudaPointerAttributes ax{}, ay{};
+    const bool mapped = cudaPointerGetAttributes(&ax, x_host) == cudaSuccess &&
+                        cudaPointerGetAttributes(&ay, y_host) == cudaSuccess && ax.type == cudaMemoryTypeHost &&
+                        ay.type == cudaMemoryTypeHost && ax.devicePointer && ay.devicePointer &&
+                        aligned16(ax.devicePointer) && aligned16(ay.devicePointer) && !env_is("DEP_STAGING", "copy");
+    cudaGetLastError();  // the attribute query of an unregistered pointer may leave an error
+    if (mapped) {
+        const dep_tactic_t *t = lookup(plan, B);
+        if (dep::stage_copy(static_cast<const uint16_t *>(ax.devicePointer), plan->x_stage, (size_t)B * plan->K,
+                            false, s) != cudaSuccess) {
+            cudaGetLastError();
+            return DEP_ERR_CUDA;
+        }
+        // The projection may start while the gather runs: it streams W first and
+        // reads x only after waiting for the gather (the gather does not write W).
+        dep_status_t st = run_impl(plan, t, plan->x_stage, W, plan->y_stage, B, stream, true);
+        if (st != DEP_OK)
+            return st;
+        if (dep::stage_copy(plan->y_stage, static_cast<uint16_t *>(ay.devicePointer), (size_t)B * plan->N, true,
+                            s) != cudaSuccess) {
+            cudaGetLastError();
+            return DEP_ERR_CUDA;
+        }
+        return DEP_OK;
+    }
     if (cudaMemcpyAsync(plan->x_stage, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess) {
         cudaGetLastError();
         return DEP_ERR_CUDA;

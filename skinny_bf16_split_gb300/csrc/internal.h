@@ -174,6 +174,12 @@ int64_t rows_tiles(const dep_tactic_t &t, int64_t N);
 int rows_blocks_per_sm(const dep_tactic_t &t, int64_t K);
 cudaError_t rows_run(const dep_tactic_t &t, const RunArgs &a);  // uses the last 2 counters
 
+// ---- zero-copy staging for the host-buffer entry point (staging.cu) ----
+// Copy n BF16 elements src -> dst (16-byte aligned; either side may be mapped
+// host memory).  after_preceding: launched with programmatic dependent launch,
+// waits for the preceding grid before reading src.
+cudaError_t stage_copy(const uint16_t *src, uint16_t *dst, size_t n, bool after_preceding, cudaStream_t stream);
+
 // ---- TMA descriptors (tma.cpp) ----
 // 2-D BF16 tensor map over a row-major [outer, inner] array with a row pitch of
 // `inner` elements; box = [box_outer rows, box_inner elements]; out-of-range

@@ -1,0 +1,55 @@
+// staging.cu -- zero-copy staging of x and y for the host-buffer entry point.
+//
+// When the caller's host buffers are pinned (mapped into the device's address
+// space), x is gathered into the plan's device staging area and y written back
+// by two small kernels instead of two memcpys.  Chained by programmatic
+// dependent launch: the gather triggers its dependents at once, so the
+// projection kernel launches early and streams its first weight stages while x
+// is still arriving (it reads x only after its griddepcontrol.wait); the
+// write-back kernel launches early the same way and waits for the projection
+// before it reads y.  Plain loads and stores of mapped host memory; 16-byte
+// vectors where both sides allow it, 2-byte elements for the rest.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dep {
+namespace {
+
+constexpr int kStageThreads = 256;
+
+__global__ void __launch_bounds__(kStageThreads)
+    stage_copy_kernel(const uint16_t *__restrict__ src, uint16_t *__restrict__ dst, size_t n, int wait_first)
+{
+    if (wait_first)
+        griddep_wait();  // the source is written by the preceding grid
+    griddep_launch_dependents();
+    const size_t tid = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    const size_t nv = n / 8;  // 16-byte vectors (both pointers are 16-byte aligned)
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+    for (size_t i = tid; i < nv; i += stride)
+        d4[i] = s4[i];
+    for (size_t i = nv * 8 + tid; i < n; i += stride)
+        dst[i] = src[i];
+}
+
+int copy_grid(size_t n)
+{
+    const size_t vecs = (n + 7) / 8;
+    const size_t blocks = (vecs + kStageThreads - 1) / kStageThreads;
+    return (int)(blocks < 1 ? 1 : blocks > 256 ? 256 : blocks);
+}
+
+}  // namespace
+
+cudaError_t stage_copy(const uint16_t *src, uint16_t *dst, size_t n, bool after_preceding, cudaStream_t stream)
+{
+    // The gather (after_preceding = false) is an ordinary launch: it waits for
+    // all earlier work in the stream.  The write-back is launched with the
+    // programmatic attribute and waits for the projection itself.
+    return launch(stage_copy_kernel, dim3(copy_grid(n)), dim3(kStageThreads), 0, stream, after_preceding, src, dst,
+                  n, after_preceding ? 1 : 0);
+}
+
+}  // namespace dep

@@ -244,18 +244,32 @@ def test_argument_errors_on_device(dep, plan_cache):
     assert e.value.status == dep.DEP_ERR_INVALID_ARG
 
 
-def test_run_host_end_to_end(dep, orc, plan_cache):
-    N, K, B = 640, 2048, 5
+@pytest.mark.parametrize("B,N", [(5, 640), (1, 333), (16, 7168), (40, 1001)])
+@pytest.mark.parametrize("memory", ["pinned", "pageable", "pinned-copy"])
+def test_run_host_end_to_end(dep, orc, plan_cache, monkeypatch, B, N, memory):
+    """The host-buffer entry point gives the device entry point's bits: pinned
+    buffers through the zero-copy staging kernels (chained by programmatic
+    dependent launch, N odd included: a 2-byte tail), pageable buffers and
+    DEP_STAGING=copy through memcpys.  Ten calls back to back, one sync."""
+    K = 2048
     plan = get_plan(dep, plan_cache, N, K)
-    x = synth.normal_bf16(2, 2, (B, K))
+    if memory == "pinned-copy":
+        monkeypatch.setenv("DEP_STAGING", "copy")
+    xs = [synth.normal_bf16(2 + i, 2, (B, K)) for i in range(10)]
     W = synth.normal_bf16(2, 1, (N, K), sigma=0.02)
-    xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
-    yh = torch.empty((B, N), dtype=torch.bfloat16).pin_memory()
     Wd = to_dev(W)
-    dep.dep_projection_run_host(plan, xh, Wd, yh, B)
+    if memory == "pageable":
+        xh = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16) for x in xs]
+        yh = [torch.full((B, N), float("nan"), dtype=torch.bfloat16) for _ in xs]
+    else:
+        xh = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs]
+        yh = [torch.full((B, N), float("nan"), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    for i in range(len(xs)):
+        dep.dep_projection_run_host(plan, xh[i], Wd, yh[i], B)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(yh.view(torch.int16).numpy().view(np.uint16),
-                                  run(dep, plan, x, W, N))
+    for x, y in zip(xs, yh):
+        np.testing.assert_array_equal(y.view(torch.int16).numpy().view(np.uint16), run(dep, plan, x, W, N))
+    assert dep.dep_projection_device_status(plan) == 0
 
 
 def test_plan_save_load_roundtrip(dep, plan_cache, tmp_path):
