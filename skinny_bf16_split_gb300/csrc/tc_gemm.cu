@@ -22,14 +22,15 @@
 //    quadrant, reads its accumulator with tcgen05.ld, frees it for the MMA of
 //    the next-but-one segment, and either stores BF16 y (segment = whole tile)
 //    or exchanges FP32 partials for the split-K reduction through flagged
-//    64-bit words (exchange.cuh): every block publishes at most one piece (in
-//    its slot 0) -- the segment of a split tile whose last unit it does not
-//    own; the block owning the tile's last unit reduces, adding the pieces in
-//    increasing block order, its own last (kept in its slot 1 for inspection).  The other blocks meet that
-//    tile as the last tile of their range, which they visit first, so they
-//    publish before doing anything else and never wait: no deadlock, and the
-//    reducer's words are usually ready when it gets there.  No float atomics:
-//    results are identical from run to run.
+//    64-bit words (exchange.cuh).  Every block publishes at most one piece (in
+//    its slot 0): the segment of a split tile whose last unit it does not own.
+//    The block owning the tile's last unit reduces, adding the pieces in
+//    increasing block order with its own last (kept in its slot 1 for
+//    inspection).  The other blocks meet that tile as the last tile of their
+//    range, which they visit first, so they publish before doing anything else
+//    and never wait: no deadlock, and the reducer's words are usually ready
+//    when it gets there.  No float atomics: results are identical from run to
+//    run.
 //  * Every wait is bounded in time; on a give-up the block records a code,
 //    lets every role finish, waits for its MMAs and copies, and frees TMEM.
 #include <cuda_bf16.h>

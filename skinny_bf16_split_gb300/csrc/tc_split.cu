@@ -13,9 +13,11 @@
 //    items and the blocks finish together (a static split ends when its
 //    slowest block does).  The last block to finish taking items resets the
 //    counter for the next launch.
-//  * Swap-AB MMAs as in the stream-K kernel: M = 128 weight rows, N = the batch
-//    padded to NT, K = 16 per instruction; 128-byte-swizzled TMA stages of
-//    tile_k / 64 slices; accumulators in TMEM, two buffers of NT columns.
+//  * Swap-AB MMAs as in the stream-K kernel: M = BM = 128 (or 64) weight rows,
+//    N = the batch padded to NT, K = 16 per instruction; 128-byte-swizzled TMA
+//    stages of tile_k / 64 slices; accumulators in TMEM, two buffers of NT
+//    columns.  The first stages are issued by thread 0 right after the barrier
+//    set-up, while warp 1 allocates TMEM.
 //  * Pieces are exchanged through the plan's exchange region, one 64-bit word
 //    per (tile, piece, b, row): the FP32 partial in the low half and a "full"
 //    flag in the high half, written by one single-copy-atomic store (no fence,
