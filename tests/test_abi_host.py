@@ -113,6 +113,14 @@ def test_host_plan_cannot_run(dep):
         with pytest.raises(dep.DepError) as e:
             dep.dep_projection_run(plan, 16, 16, 16, -1, 0)
         assert e.value.status == dep.DEP_ERR_INVALID_ARG
+        # inspection and host-buffer entry points refuse a host-only plan before any CUDA call
+        for call in (lambda: dep.dep_projection_plan_partials(plan, 4),
+                     lambda: dep.dep_projection_plan_exchange(plan, 4),
+                     lambda: dep.dep_projection_device_status(plan, 0),
+                     lambda: dep.dep_projection_run_host(plan, 16, 16, 16, 1, 0)):
+            with pytest.raises(dep.DepError) as e:
+                call()
+            assert e.value.status == dep.DEP_ERR_UNSUPPORTED
     finally:
         dep.dep_projection_plan_destroy(plan)
 
