@@ -200,9 +200,10 @@ int32_t tc_default_stages(int32_t cols)
 //  * wider batches: the stream-K tensor-core kernel, one block per tile when the
 //    tiles nearly fill the GPU.
 // Measured on GB300 (per call, CUDA events): at 4 rows the K-piece tensor-core
-// tactic is 1.9-2.8 us faster than the stream-K FMA kernel on all three
-// weights; at 4-16 rows it is 1.3-2.3 us faster than the stream-K tensor-core
-// kernel for o_proj, equal for DSA and up to 1.7 us faster for KDA.
+// tactic is 1.9-2.8 us faster than the stream-K FMA kernel and 3-34 us faster
+// than the whole-row kernel on all three weights; at 4-16 rows it is 0.2-1.5 us
+// faster than the stream-K tensor-core kernel for o_proj, equal for DSA and up
+// to 1 us faster for KDA.
 dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
 {
     if (rows <= 2) {
