@@ -272,6 +272,35 @@ def test_run_host_end_to_end(dep, orc, plan_cache, monkeypatch, B, N, memory):
     assert dep.dep_projection_device_status(plan) == 0
 
 
+def test_run_host_captured_in_a_graph(dep, plan_cache):
+    """The host-buffer entry point with pinned buffers inside a CUDA graph: the
+    zero-copy gather, the projection and the write-back (chained by programmatic
+    dependent launch) replay with new inputs written into the same pinned
+    buffers, and every replay gives the device entry point's bits."""
+    N, K, B = 7168, 4096, 8
+    plan = get_plan(dep, plan_cache, N, K)
+    W = synth.normal_bf16(120, 1, (N, K), sigma=0.02)
+    Wd = to_dev(W)
+    xh = torch.empty((B, K), dtype=torch.bfloat16).pin_memory()
+    yh = torch.empty((B, N), dtype=torch.bfloat16).pin_memory()
+    stream = torch.cuda.Stream()
+    xh.copy_(torch.from_numpy(synth.normal_bf16(121, 2, (B, K)).view(np.int16)).view(torch.bfloat16))
+    with torch.cuda.stream(stream):
+        dep.dep_projection_run_host(plan, xh, Wd, yh, B, stream)  # warm-up outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        dep.dep_projection_run_host(plan, xh, Wd, yh, B, stream)
+    for i in range(3):
+        x = synth.normal_bf16(122 + i, 2, (B, K))
+        xh.copy_(torch.from_numpy(x.view(np.int16)).view(torch.bfloat16))
+        yh.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(yh.view(torch.int16).numpy().view(np.uint16), run(dep, plan, x, W, N))
+    assert dep.dep_projection_device_status(plan) == 0
+
+
 def test_plan_save_load_roundtrip(dep, plan_cache, tmp_path):
     N, K = 7168, 12288
     plan = get_plan(dep, plan_cache, N, K, (1, 2, 4, 8, 16))
