@@ -53,7 +53,8 @@ WORKLOAD_TEXT = {
 TUNED_BY_DEFAULT = {"dsa_verify", "tp_sharded"}
 # Sources each kernel family is built from (a traffic record is stale once they change).
 KERNEL_SOURCES = {"splitk_fma": ["splitk_fma.cu"], "tc_gemm": ["tc_gemm.cu", "exchange.cuh"],
-                  "tc_split": ["tc_split.cu", "exchange.cuh"], "rows_gemv": ["rows_gemv.cu"]}
+                  "tc_split": ["tc_split.cu", "exchange.cuh"], "rows_gemv": ["rows_gemv.cu"],
+                  "tc_wide": ["tc_wide.cu"], "tc_cluster": ["tc_cluster.cu"]}
 SHARED_SOURCES = ["ptx.cuh", "internal.h"]
 
 
@@ -296,6 +297,10 @@ def kernel_name(t) -> str:
         return f"rows_gemv_c{t.cols}"
     if t.kind == dep.DEP_KIND_TC_SPLIT:
         return f"tc_split_n{t.cols}"
+    if t.kind == dep.DEP_KIND_TC_WIDE:
+        return f"tc_wide_n{t.cols}_g{t.tile_n // 128}"
+    if t.kind == dep.DEP_KIND_TC_CLUSTER:
+        return f"tc_cluster_n{t.cols}_g{t.tile_n // 128}_k{t.splits}"
     return f"tc_gemm_n{t.cols}"
 
 

@@ -73,14 +73,30 @@ typedef enum {
                                  dynamically; tiles of tile_n = 64 or 128 weight rows
                                  (MMA M), each cut into `splits` fixed K pieces whose
                                  FP32 partials are added in piece order */
+#define DEP_KIND_TC_WIDE 5    /* tcgen05 MMA for wide batches: each block streams a
+                                 group of tile_n / 128 = 2 or 4 weight tiles of 128
+                                 rows against every x slice (one MMA per tile, the
+                                 same x operand), stream-K over (group, k-tile)
+                                 units; split groups are reduced by the blocks
+                                 that share them, each a part of the columns, adding
+                                 the blocks' FP32 partials in block order */
+#define DEP_KIND_TC_CLUSTER 6 /* tcgen05 MMA for wide batches: a thread-block cluster
+                                 of `splits` = k CTAs per group of tile_n / 128 = 2 or
+                                 4 weight tiles (one MMA per tile, the same x
+                                 operand), CTA rank r streaming K piece r; the K
+                                 pieces are added in rank order through distributed
+                                 shared memory (no global workspace); `stages` =
+                                 weight stages (x has its own 2-4 stage ring);
+                                 `ctas` = a multiple of k; tile_k = 64 */
 
 /* One table entry: the tactic that serves batches of up to max_rows rows. */
 typedef struct {
     int32_t max_rows; /* table key (binning rule above) */
     int32_t kind;     /* DEP_KIND_* */
-    int32_t ctas;     /* persistent blocks launched (FMA/TC: work split evenly,
-                         stream-K; ROWS/TC_SPLIT: work items taken dynamically) */
-    int32_t tile_n;   /* weight rows per tile */
+    int32_t ctas;     /* persistent blocks launched (FMA/TC/TC_WIDE: work split
+                         evenly, stream-K; ROWS/TC_SPLIT: work items taken
+                         dynamically) */
+    int32_t tile_n;   /* weight rows per tile (TC_WIDE: per group, 256 or 512) */
     int32_t tile_k;   /* reduction columns per pipeline stage */
     int32_t stages;   /* pipeline depth (shared-memory stages) */
     int32_t cols;     /* batch rows per pass (FMA/ROWS: x rows held; TC: MMA N) */
@@ -98,6 +114,10 @@ typedef struct {
  * read-only).  Consecutive runs then overlap one kernel's tail with the next
  * one's ramp-up, also inside CUDA graphs. */
 #define DEP_PLAN_PDL 2u
+/* Inspection: the wide-batch kernel (DEP_KIND_TC_WIDE) also stores the partials
+ * each block reduces itself, so that dep_projection_plan_partials returns every
+ * block's piece of every split group (extra writes; same results). */
+#define DEP_PLAN_KEEP_PIECES 4u
 
 /*
  * Build a plan for weights of shape [N,K] on the current CUDA device.
@@ -204,6 +224,14 @@ dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic
  * tile row r) at float index ((c * 2 + s) * cols + j) * tile_n + r, slot 0 for
  * the block's first tile and 1 for its last.  Lets a test re-add the partials
  * of every split tile in block order and check the kernel's fix-up bit for bit.
+ * For a DEP_KIND_TC_WIDE launch of C blocks with MMA width NT on groups of
+ * R = tile_n rows: block c's piece of a split group sits in slot s (1 for the
+ * group the block starts in, 0 for its last group when it has more than one)
+ * at float offset (c * 2 + s) * R * NT; inside it, epilogue warp e (0..7, TMEM
+ * lane quadrant (e + 2) % 4, column half e / 4 of the G * NT accumulator
+ * columns) owns 32 * G * NT / 2 floats, accumulator column j of TMEM lane l
+ * at (j / 4 * 32 + l % 32) * 4 + j % 4.  Without DEP_PLAN_KEEP_PIECES the
+ * columns a block reduces itself are not stored.
  */
 dep_status_t dep_projection_plan_partials(dep_plan_t plan, void *host, size_t bytes, size_t *written);
 

@@ -29,9 +29,12 @@ DEP_KIND_SPLITK_FMA = 1
 DEP_KIND_TC = 2
 DEP_KIND_ROWS = 3
 DEP_KIND_TC_SPLIT = 4
+DEP_KIND_TC_WIDE = 5
+DEP_KIND_TC_CLUSTER = 6
 DEP_PLAN_DEFAULT = 0
 DEP_PLAN_TUNE = 1
 DEP_PLAN_PDL = 2
+DEP_PLAN_KEEP_PIECES = 4
 
 DEP_DEV_TIMEOUT_PRODUCER = 1
 DEP_DEV_TIMEOUT_CONSUMER = 2

@@ -41,6 +41,7 @@ struct dep_plan_s {
     bool fault_launch = false;
     bool log = false;
     bool pdl = false;  // DEP_PLAN_PDL
+    bool keep_pieces = false;  // DEP_PLAN_KEEP_PIECES
 };
 
 namespace {
@@ -75,6 +76,10 @@ bool tactic_valid(const dep_tactic_t &t)
         return false;
     if (t.kind == DEP_KIND_TC_SPLIT)
         return dep::tcs_valid(t);
+    if (t.kind == DEP_KIND_TC_WIDE)
+        return dep::wide_valid(t);
+    if (t.kind == DEP_KIND_TC_CLUSTER)
+        return dep::cluster_valid(t);
     if (t.splits != 0)
         return false;  // only the K-piece tactic has pieces
     if (t.kind == DEP_KIND_SPLITK_FMA)
@@ -90,7 +95,8 @@ size_t ws_per_cta(const dep_tactic_t &t)
 {
     switch (t.kind) {
     case DEP_KIND_SPLITK_FMA: return dep::fma_ws_per_cta(t);
-    default: return 0;  // whole rows: no partials; tensor cores: exchange words instead
+    case DEP_KIND_TC_WIDE: return dep::wide_ws_per_cta(t);
+    default: return 0;  // whole rows: no partials; other tensor-core kinds: exchange words instead
     }
 }
 
@@ -99,6 +105,7 @@ int64_t effective_ctas(const dep_tactic_t &t, int64_t N, int64_t K)
 {
     const int64_t U = t.kind == DEP_KIND_SPLITK_FMA ? dep::fma_units(t, N, K)
                       : t.kind == DEP_KIND_TC       ? dep::tc_units(t, N, K)
+                      : t.kind == DEP_KIND_TC_WIDE  ? dep::wide_units(t, N, K)
                                                     : dep::rows_tiles(t, N);
     return U < t.ctas ? U : t.ctas;
 }
@@ -119,11 +126,13 @@ size_t tactic_xch_words(const dep_tactic_t &t, int64_t N, int64_t K)
                                        : 0;
 }
 
-size_t tactic_counters(const dep_tactic_t &t, int64_t N)
+size_t tactic_counters(const dep_tactic_t &t, int64_t N, int64_t K)
 {
     switch (t.kind) {
     case DEP_KIND_SPLITK_FMA: return dep::fma_counters(t, N);
     case DEP_KIND_TC: return 0;  // the exchange words need no counters
+    case DEP_KIND_TC_WIDE: return (size_t)effective_ctas(t, N, K) * dep::wide_flags_per_cta(t);  // flags
+    case DEP_KIND_TC_CLUSTER: return 0;  // partials stay in the cluster's shared memory
     case DEP_KIND_TC_SPLIT: return dep::tcs_counters(t, N);
     default: return 2;  // tile dispenser and finish count (the last two counters)
     }
@@ -180,6 +189,25 @@ dep_tactic_t tcs_tactic(int32_t rows, int32_t cols, int32_t stages, int32_t ctas
     return t;
 }
 
+dep_tactic_t wide_tactic(int32_t rows, int32_t cols, int32_t groups_of_tiles, int32_t stages, int32_t ctas,
+                         int32_t tile_k = 64)
+{
+    dep_tactic_t t = tc_tactic(rows, cols, stages, ctas, tile_k);
+    t.kind = DEP_KIND_TC_WIDE;
+    t.tile_n = 128 * groups_of_tiles;
+    return t;
+}
+
+dep_tactic_t cluster_tactic(int32_t rows, int32_t cols, int32_t groups_of_tiles, int32_t k, int32_t stages,
+                            int32_t ctas)
+{
+    dep_tactic_t t = tc_tactic(rows, cols, stages, ctas, 64);
+    t.kind = DEP_KIND_TC_CLUSTER;
+    t.tile_n = 128 * groups_of_tiles;
+    t.splits = k;
+    return t;
+}
+
 // Deepest pipeline of the tensor-core kernel that fits in shared memory.
 int32_t tc_default_stages(int32_t cols)
 {
@@ -197,8 +225,10 @@ int32_t tc_default_stages(int32_t cols)
 //    dynamically -- SMs / tiles pieces per 128-row tile while the tiles fit on
 //    the SMs (o_proj: 2, DSA: 1, one item per block), 3 pieces otherwise (KDA:
 //    386 tiles, 1158 items);
-//  * wider batches: the stream-K tensor-core kernel, one block per tile when the
-//    tiles nearly fill the GPU.
+//  * 32 rows, and wider batches the rule below does not give to clusters: the
+//    stream-K tensor-core kernel, one block per tile when the tiles nearly fill
+//    the GPU;
+//  * 64 rows and more: a thread-block cluster per group of weight tiles (below).
 // Measured on GB300 (per call, CUDA events): at 4 rows the K-piece tensor-core
 // tactic is 1.9-2.8 us faster than the stream-K FMA kernel and 3-34 us faster
 // than the whole-row kernel on all three weights; at 4-16 rows it is 0.2-1.5 us
@@ -229,6 +259,33 @@ dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
                 if (dep::tcs_valid(t))
                     return t;
             }
+    }
+    // 64 batch rows and more: a cluster of k CTAs per group of two 128-row
+    // tiles (x bytes per weight byte halved; the K pieces added through
+    // distributed shared memory), k = SMs / groups up to 4, while the groups fit
+    // on the SMs in one wave of clusters of two; at 256 rows also past that.
+    // Where they do not, 128 rows take groups of four tiles, one CTA each, if
+    // those fit.  Measured on GB300 (per launch, back to back): DSA 14560 x
+    // 7168 B = 128 / 256: 44.6 / 50.0 us against 45.4 / 61.0 us for the one-tile
+    // kernel; o_proj 7168 x 12288 B = 64..256 (k = 4): 37.2 / 41.0 / 49.9 us; KDA
+    // 49376 x 7168 B = 128 (four-tile groups) / 256 (k = 2): 119.6 / 152.6 us.
+    if (cols >= 64) {
+        const int64_t t2 = (N + 255) / 256, t4 = (N + 511) / 512;
+        const int32_t sw = cols == 256 ? 4 : (cols == 128 ? 6 : 5);
+        if (2 * t2 <= sm_count) {
+            const int32_t k = (int32_t)std::min<int64_t>(4, sm_count / t2);
+            const dep_tactic_t t = cluster_tactic(rows, cols, 2, k, sw, (int32_t)t2 * k);
+            if (dep::cluster_valid(t))
+                return t;
+        } else if (cols == 256) {
+            const dep_tactic_t t = cluster_tactic(rows, cols, 2, 2, sw, (sm_count / 2) * 2);
+            if (dep::cluster_valid(t))
+                return t;
+        } else if (cols == 128 && t4 <= sm_count) {
+            const dep_tactic_t t = cluster_tactic(rows, cols, 4, 1, 3, (int32_t)t4);
+            if (dep::cluster_valid(t))
+                return t;
+        }
     }
     const int32_t ctas = (tiles <= sm_count && 4 * tiles >= 3 * (int64_t)sm_count) ? (int32_t)tiles : sm_count;
     // 64-column stages for the widest batches.
@@ -272,10 +329,18 @@ dep_status_t allocate_device(dep_plan_s *p, size_t extra_ws_floats = 0, size_t e
     for (const auto &t : p->table) {
         ws = std::max(ws, tactic_ws_floats(t, p->N, p->K));
         ws = std::max(ws, (size_t)p->sm_count * ws_per_cta(t));
-        cnt = std::max(cnt, tactic_counters(t, p->N));
+        cnt = std::max(cnt, tactic_counters(t, p->N, p->K));
         xw = std::max(xw, tactic_xch_words(t, p->N, p->K));
-        if (t.kind == DEP_KIND_TC || t.kind == DEP_KIND_TC_SPLIT)  // room for stream-K on every SM
-            xw = std::max(xw, (size_t)p->sm_count * dep::tc_xch_words_per_cta(t));
+        // Room for the stream-K tensor-core kernels on every SM at this width
+        // (explicit tactics of tests and tuning), whatever kind the table holds.
+        if (t.kind == DEP_KIND_TC || t.kind == DEP_KIND_TC_SPLIT || t.kind == DEP_KIND_TC_WIDE ||
+            t.kind == DEP_KIND_TC_CLUSTER) {
+            dep_tactic_t one = t;
+            one.tile_n = 128;
+            xw = std::max(xw, (size_t)p->sm_count * dep::tc_xch_words_per_cta(one));
+        }
+        if (t.kind == DEP_KIND_TC_WIDE)
+            cnt = std::max(cnt, (size_t)p->sm_count * dep::wide_flags_per_cta(t));
         rows = std::max(rows, t.max_rows);
     }
     auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
@@ -376,7 +441,8 @@ dep_status_t make_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_b
             return DEP_ERR_UNSUPPORTED;
         }
         if (dep::fma_prepare_device() != cudaSuccess || dep::tc_prepare_device() != cudaSuccess ||
-            dep::tcs_prepare_device() != cudaSuccess ||
+            dep::tcs_prepare_device() != cudaSuccess || dep::wide_prepare_device() != cudaSuccess ||
+            dep::cluster_prepare_device() != cudaSuccess ||
             dep::rows_prepare_device() != cudaSuccess) {
             cudaGetLastError();
             delete p;
@@ -423,7 +489,7 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
         cudaGetLastError();
         return DEP_ERR_INVALID_ARG;
     }
-    if (tactic_ws_floats(*t, p->N, p->K) > p->ws_floats || tactic_counters(*t, p->N) > p->n_counters ||
+    if (tactic_ws_floats(*t, p->N, p->K) > p->ws_floats || tactic_counters(*t, p->N, p->K) > p->n_counters ||
         tactic_xch_words(*t, p->N, p->K) > p->xch_words)
         return DEP_ERR_INVALID_ARG;
     if (p->fault_launch)
@@ -445,11 +511,14 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
     a.stream = static_cast<cudaStream_t>(stream);
     a.wait_limit_ns = p->wait_limit_ns;
     a.pdl = p->pdl || force_pdl;
+    a.keep_pieces = p->keep_pieces;
     if (t->kind == DEP_KIND_ROWS && !dep::rows_fits(*t, p->K))
         return DEP_ERR_UNSUPPORTED;  // x and the ring do not fit in shared memory for this K
     cudaError_t e = t->kind == DEP_KIND_SPLITK_FMA ? dep::fma_run(*t, a)
                     : t->kind == DEP_KIND_TC       ? dep::tc_run(*t, a)
                     : t->kind == DEP_KIND_TC_SPLIT ? dep::tcs_run(*t, a)
+                    : t->kind == DEP_KIND_TC_WIDE  ? dep::wide_run(*t, a)
+                    : t->kind == DEP_KIND_TC_CLUSTER ? dep::cluster_run(*t, a)
                                                    : dep::rows_run(*t, a);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -513,6 +582,25 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
                 for (int32_t sp : pieces)
                     c.push_back(tcs_tactic(rows, cols, st, sm_count, tk, sp, bm));
     }
+    // Groups of 2 or 4 weight tiles per x slice (wide batches), stream-K on every SM.
+    if (cols >= 32)
+        for (int32_t g : {2, 4})
+            for (int32_t tk : {64, 128})
+                for (int32_t st : {2, 3, 4, 5, 6})
+                    if (cols * g <= 512)
+                        c.push_back(wide_tactic(rows, cols, g, st, sm_count, tk));
+    // A cluster of k CTAs per group of 2 or 4 tiles: k = 1..4, as many clusters
+    // as groups (at most one wave of the SMs).
+    if (cols >= 32)
+        for (int32_t g : {2, 4})
+            for (int32_t k : {1, 2, 3, 4})
+                for (int32_t st : {3, 4, 5, 6}) {
+                    if (cols * g > 512)
+                        continue;
+                    const int64_t groups = (N + 128 * g - 1) / (128 * g);
+                    const int32_t clusters = (int32_t)std::max<int64_t>(1, std::min<int64_t>(groups, sm_count / k));
+                    c.push_back(cluster_tactic(rows, cols, g, k, st, clusters * k));
+                }
     // K pieces keep every piece's partial: leave out tactics whose exchange words
     // would take more than 64 MB.
     constexpr size_t kMaxPieceWords = (64u << 20) / 8;
@@ -536,7 +624,7 @@ dep_status_t tune_plan(dep_plan_s *p)
         cands.push_back(candidates(t.max_rows, p->N, p->K, p->sm_count));
         for (const auto &c : cands.back()) {
             ws_need = std::max(ws_need, tactic_ws_floats(c, p->N, p->K));
-            cnt_need = std::max(cnt_need, tactic_counters(c, p->N));
+            cnt_need = std::max(cnt_need, tactic_counters(c, p->N, p->K));
             xch_need = std::max(xch_need, tactic_xch_words(c, p->N, p->K));
         }
         rows_max = std::max(rows_max, t.max_rows);
@@ -593,8 +681,11 @@ dep_status_t tune_plan(dep_plan_s *p)
             std::sort(ms.begin(), ms.end());
             const float med = ms[0];
             if (p->log)
-                std::fprintf(stderr, "[dep] tune N=%lld K=%lld B=%d kind=%d cols=%d stages=%d ctas=%d: %.2f us\n",
-                             (long long)p->N, (long long)p->K, B, c.kind, c.cols, c.stages, c.ctas, med * 1e3f);
+                std::fprintf(stderr,
+                             "[dep] tune N=%lld K=%lld B=%d kind=%d cols=%d tile_n=%d tile_k=%d stages=%d ctas=%d "
+                             "splits=%d: %.2f us\n",
+                             (long long)p->N, (long long)p->K, B, c.kind, c.cols, c.tile_n, c.tile_k, c.stages, c.ctas,
+                             c.splits, med * 1e3f);
             if (med < best) {
                 best = med;
                 best_t = c;
@@ -645,7 +736,7 @@ int32_t dep_bins_index(const int32_t *keys, int32_t n_keys, int32_t B)
 dep_status_t dep_projection_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_batches,
                                  uint32_t flags, dep_plan_t *out)
 {
-    if (flags & ~(DEP_PLAN_DEFAULT | DEP_PLAN_TUNE | DEP_PLAN_PDL)) {
+    if (flags & ~(DEP_PLAN_DEFAULT | DEP_PLAN_TUNE | DEP_PLAN_PDL | DEP_PLAN_KEEP_PIECES)) {
         if (out)
             *out = nullptr;
         return DEP_ERR_INVALID_ARG;
@@ -654,6 +745,7 @@ dep_status_t dep_projection_plan(int64_t N, int64_t K, const int32_t *batches, i
     if (st != DEP_OK)
         return st;
     (*out)->pdl = (flags & DEP_PLAN_PDL) != 0;
+    (*out)->keep_pieces = (flags & DEP_PLAN_KEEP_PIECES) != 0;
     if (!(flags & DEP_PLAN_TUNE))
         return st;
     st = tune_plan(*out);

@@ -32,6 +32,8 @@ struct RunArgs {
     // grid in the stream finishes; it streams its first weight stages before
     // waiting for that grid (the weight must not be written by preceding work).
     bool pdl = false;
+    // The wide kernel also stores the partials its blocks reduce themselves.
+    bool keep_pieces = false;
 };
 
 // Shared memory a block of any kernel here may use (the sm_100-family opt-in maximum).
@@ -63,6 +65,8 @@ cudaError_t fma_prepare_device();
 cudaError_t tc_prepare_device();
 cudaError_t rows_prepare_device();
 cudaError_t tcs_prepare_device();
+cudaError_t wide_prepare_device();
+cudaError_t cluster_prepare_device();
 
 // Launch with the programmatic-stream-serialisation attribute when `pdl` is set.
 template <typename Kernel, typename... Args>
@@ -166,6 +170,18 @@ size_t tcs_xch_words(const dep_tactic_t &t, int64_t N, int64_t K);  // every pie
 size_t tcs_counters(const dep_tactic_t &t, int64_t N);               // the last 2 counters
 int tcs_blocks_per_sm(const dep_tactic_t &t);
 cudaError_t tcs_run(const dep_tactic_t &t, const RunArgs &a);       // uses the last 2 counters
+
+// ---- tcgen05 tactic for wide batches, groups of tiles per x slice (tc_wide.cu) ----
+bool wide_valid(const dep_tactic_t &t);
+int64_t wide_units(const dep_tactic_t &t, int64_t N, int64_t K);  // stream-K work units
+size_t wide_ws_per_cta(const dep_tactic_t &t);                    // partial floats per block (two slots)
+size_t wide_flags_per_cta(const dep_tactic_t &t);                 // flag ints per block (the first counters)
+int wide_blocks_per_sm(const dep_tactic_t &t);
+cudaError_t wide_run(const dep_tactic_t &t, const RunArgs &a);
+
+// ---- tcgen05 tactic for wide batches, a cluster of CTAs per group (tc_cluster.cu) ----
+bool cluster_valid(const dep_tactic_t &t);
+cudaError_t cluster_run(const dep_tactic_t &t, const RunArgs &a);
 
 // ---- whole-row tactic (rows_gemv.cu) ----
 bool rows_valid(const dep_tactic_t &t);

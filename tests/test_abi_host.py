@@ -84,7 +84,37 @@ def test_default_batches_when_none_given(dep):
         assert [t.max_rows for t in table] == [1, 2, 4, 8, 16, 32, 64, 128, 256]
         # 114 tiles of 128 rows nearly fill 152 SMs: whole tiles, one per block
         assert all((t.kind, t.splits) == (dep.DEP_KIND_TC_SPLIT, 1) for t in table if 2 < t.max_rows <= 16)
-        assert all((t.kind, t.ctas) == (dep.DEP_KIND_TC, 114) for t in table if t.max_rows > 16)
+        assert all((t.kind, t.ctas) == (dep.DEP_KIND_TC, 114) for t in table if t.max_rows == 32)
+        # 64 rows and more: 57 groups of two tiles, a cluster of two CTAs each
+        wide = [t for t in table if t.max_rows >= 64]
+        assert all((t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, 256, 2, 114) for t in wide)
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("N,sms,expect", [
+    (7168, 152, (256, 4, 112)),    # o_proj: 28 groups, clusters of four
+    (14560, 152, (256, 2, 114)),   # DSA: 57 groups, clusters of two
+    (49376, 152, None),            # KDA: 193 groups do not fit in one wave (see below)
+    (1000, 8, (256, 2, 8)),        # 4 groups on 8 SMs
+])
+def test_default_rule_wide_batches(dep, N, sms, expect):
+    """The default rule for 64-256 rows: a cluster of k = SMs / groups (at most
+    4) CTAs per group of two 128-row tiles while the groups fit on the SMs in
+    clusters of two; otherwise clusters of two at 256 rows, groups of four tiles
+    one CTA each at 128 rows if they fit, the one-tile stream-K kernel else."""
+    plan = dep.dep_projection_plan_host(N, 7168, [64, 128, 256], sms)
+    try:
+        table = {t.max_rows: t for t in dep.dep_projection_plan_table(plan)}
+        if expect is not None:
+            for b in (64, 128, 256):
+                t = table[b]
+                assert (t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, *expect), (b, t)
+        else:
+            assert (table[256].kind, table[256].splits, table[256].ctas) == (dep.DEP_KIND_TC_CLUSTER, 2, 152)
+            assert (table[128].kind, table[128].tile_n, table[128].splits, table[128].ctas) == \
+                (dep.DEP_KIND_TC_CLUSTER, 512, 1, 97)
+            assert table[64].kind == dep.DEP_KIND_TC
     finally:
         dep.dep_projection_plan_destroy(plan)
 

@@ -1,12 +1,14 @@
-"""The no-allocation entry point, dep_projection_run_static, against the plan path.
+"""The no-allocation entry point, dep_projection_run_static, against the mirror, oracle and plan path.
 
 Callers that must not allocate device memory -- code inside a device-memory
 allocator or pool, hosts that reserve all device memory up front, paths that
 cannot take cudaMalloc's implicit synchronisation -- cannot build a plan, since
 a plan allocates its workspace.  dep_projection_run_static serves them with a
 fixed scratch array compiled into the library.  This test calls it through the
-C ABI twice in a row, on different problems, and checks each output against the
-plan-based dep_projection_run within the acceptance tolerance of the tests.
+C ABI three times in a row, on different problems, and checks each output bit
+for bit against the FP32 mirror of the kernel it runs, and within the acceptance
+tolerance of the tests against the exact oracle and the plan-based
+dep_projection_run.
 
 The file is named so that pytest collects it last: if it fails, a run that stops
 at the first failure has already run every other test.  It also passes alone in
@@ -26,17 +28,30 @@ from skinny_bf16_split_gb300 import synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 
-def test_static_scratch_entry_matches_plan_entry(dep):
-    problems = [(3, 1000, 3000, 11), (8, 7168, 4096, 12)]  # (B, N, K, seed): two calls in a row
+def test_static_scratch_entry_matches_plan_entry(dep, orc):
+    """Three calls in a row on one stream, then three checks per output: bit for
+    bit against the FP32 mirror of the split-K FMA kernel the entry runs (32-row
+    tiles, 256-column k-tiles, one block per SM), within the acceptance
+    tolerance of the exact oracle, and within it of the plan-based
+    dep_projection_run.  The 13-row batch runs as two passes of 8 rows, so its
+    second pass reuses the tile counters and partials the first pass left."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    problems = [(3, 1000, 3000, 11), (8, 7168, 4096, 12), (13, 777, 2000, 13)]  # (B, N, K, seed)
     outs = []
     for B, N, K, seed in problems:
-        x = to_dev(synth.normal_bf16(seed, synth.X_ID, (B, K)))
-        W = to_dev(synth.normal_bf16(seed, synth.W_ID, (N, K), sigma=0.02))
+        xh = synth.normal_bf16(seed, synth.X_ID, (B, K))
+        Wh = synth.normal_bf16(seed, synth.W_ID, (N, K), sigma=0.02)
+        x, W = to_dev(xh), to_dev(Wh)
         y = empty_out(B, N)
         dep.dep_projection_run_static(x, W, y, N, K, B)
-        outs.append((y, x, W, B, N, K))
+        outs.append((y, x, W, xh, Wh, B, N, K))
     torch.cuda.synchronize()
-    for y, x, W, B, N, K in outs:
+    for y, x, W, xh, Wh, B, N, K in outs:
+        got = to_host(y)
+        units = -(-N // 32) * -(-K // 256)
+        np.testing.assert_array_equal(got, orc.mirror_fma(xh, Wh, min(sms, units), 32))
+        ok, worst, idx = within_tolerance(got, orc.linear(xh, Wh))
+        assert ok, (B, N, K, worst, idx)
         plan = dep.dep_projection_plan(N, K, [B])
         try:
             ref = empty_out(B, N)
@@ -44,7 +59,7 @@ def test_static_scratch_entry_matches_plan_entry(dep):
             torch.cuda.synchronize()
         finally:
             dep.dep_projection_plan_destroy(plan)
-        ok, worst, idx = within_tolerance(to_host(y), to_host(ref))
+        ok, worst, idx = within_tolerance(got, to_host(ref))
         assert ok, (B, N, K, worst, idx)
 
 
