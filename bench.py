@@ -2,11 +2,20 @@
 """Benchmark of the GB300 decode projection y[B,N] = BF16(x[B,K] . W[N,K]^T).
 
 One step = one pass of the projection over every call of the workload (default:
-the o_proj sweep, x[B,12288] . W[7168,12288]^T for B = 1, 2, 4, 8, 16 with seeds
-0..4, i.e. five distinct 176 MB weights).  Inputs are resident in HBM before the
-timed region; every weight is larger than the 129 MB L2 and each step cycles
-five of them, so no weight is served from L2.  The metric is achieved HBM
-bandwidth: algorithmic bytes (W + x + y of every call) per second.
+all five configurations of the benchmark in one step -- DSA input projection at
+B = 1, the o_proj sweep B = 1..16, the KDA sweep B = 1..16, wide DSA batches
+B = 32..256 and the 8-layer chain: 30 calls on 29 distinct weights of 176 MB to
+708 MB).  Inputs are resident in HBM before the timed region; every weight is
+larger than the 129 MB L2 and consecutive calls use different weights, so no
+weight is served from L2.  The metric is achieved HBM bandwidth: algorithmic
+bytes (W + x + y of every call) per second.
+
+Besides `value` the line carries: per-call times (plain launches with their
+own events, and CUDA-graph replay with programmatic dependent launch, the
+deployment's mode), one roofline per kernel family, the copy and read-only
+ceilings measured in the same run, clocks sampled during the timed region,
+the end-to-end figure through the host-buffer entry point, and the CPU oracle's
+throughput on a bounded sample.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...     # the CPU oracle on a bounded sample
@@ -49,6 +58,9 @@ WORKLOAD_TEXT = {
     "tp_sharded": "TP-G shards at B=16: DSA input projection rows 14560/G x 7168 and o_proj "
                   "7168 x 12288/G for G in {2,4,8}, seeds 0..5, tuned plan",
 }
+WORKLOAD_TEXT["baseline"] = ("all five configurations in one step: " +
+                             "; ".join(WORKLOAD_TEXT[k] for k in ("dsa_b1", "oproj_sweep", "kda_sweep",
+                                                                  "dsa_wide", "chain")))
 # Workloads whose plan is tuned by default (the verify-step tables are measured).
 TUNED_BY_DEFAULT = {"dsa_verify", "tp_sharded"}
 # Sources each kernel family is built from (a traffic record is stale once they change).
@@ -61,17 +73,19 @@ SHARED_SOURCES = ["ptx.cuh", "internal.h"]
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=synth.WORKLOADS, default="oproj_sweep")
+    ap.add_argument("--workload", choices=synth.WORKLOADS, default="baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="wall-clock budget of the oracle CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--plan", default="default", choices=("default", "tune"))
     ap.add_argument("--no-graph", action="store_true",
-                    help="skip the CUDA-graph replay (programmatic dependent launch) measurement")
+                    help="skip the CUDA-graph replay (programmatic dependent launch) measurements")
+    ap.add_argument("--no-ceiling", action="store_true",
+                    help="skip the in-run copy and read-only ceiling probes")
     ap.add_argument("--report", action="store_true",
                     help="measure every workload; one JSON line each (per-config report)")
     return ap.parse_args()
@@ -146,66 +160,105 @@ def read_traffic(kernel: str, workload: str):
 # ---------------------------------------------------------------- clocks -----
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while it runs."""
+    """SM clock and throttle reasons of the bench's GPU while it runs: a thread
+    that runs one `nvidia-smi --query-gpu` every ~150 ms (queries only; no
+    setting is touched).  Each query's output is read whole, so no sample is
+    lost to output buffering when sampling stops."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index: int):
-        self.proc = None
-        self.path = None
+        import threading
         self.device = device_index
+        self.rows = []
+        self.target = None
+        self._stop = threading.Event()
+        self._thread = None
 
-    def start(self):
+    def _query(self, target):
+        r = subprocess.run(["nvidia-smi", "-i", target, f"--query-gpu={self.QUERY}",
+                            "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
+        if r.returncode != 0:
+            return None
+        parts = [p.strip() for p in r.stdout.strip().splitlines()[0].split(",")] if r.stdout.strip() else []
+        if len(parts) < 7:
+            return None
+        try:
+            return float(parts[0]), float(parts[1]), parts[3:7]
+        except ValueError:
+            return None
+
+    def _pick_target(self):
+        candidates = []
         try:
             import torch
             uuid = str(torch.cuda.get_device_properties(self.device).uuid)
-            target = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+            candidates.append(uuid if uuid.startswith("GPU-") else f"GPU-{uuid}")
         except Exception:
-            target = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
-        fd, self.path = tempfile.mkstemp(suffix=".csv")
-        os.close(fd)
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", target, f"--query-gpu={self.QUERY}", "--format=csv,noheader",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
-        except OSError:
-            self.proc = None
+            pass
+        visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        if visible:
+            candidates.append(visible.split(",")[self.device].strip())
+        candidates.append(str(self.device))
+        for c in candidates:
+            try:
+                if self._query(c) is not None:
+                    return c
+            except (OSError, subprocess.SubprocessError):
+                continue
+        return None
+
+    def _loop(self):
+        while not self._stop.is_set():
+            try:
+                row = self._query(self.target)
+            except (OSError, subprocess.SubprocessError):
+                row = None
+            if row is not None:
+                self.rows.append(row)
+            self._stop.wait(0.15)
+
+    def start(self):
+        import threading
+        self.target = self._pick_target()
+        if self.target is None:
+            return
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((float(parts[1].split()[0]), float(parts[2].split()[0]), parts[5:9]))
-            except ValueError:
-                continue
-        os.unlink(self.path)
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=15)
+        rows = self.rows
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows),
-                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": f"nvidia-smi -i {self.target}" if self.target else "nvidia-smi unavailable"}
+        reasons = sorted({self.NAMES[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "sm_mhz_min": min(r[0] for r in rows), "reasons": reasons, "samples": len(rows),
+                "source": f"nvidia-smi -i {self.target}, every ~150 ms while the timed regions ran"}
 
 
 # ----------------------------------------------------------- cpu baseline ----
 
+def host_cores() -> int:
+    """Cores this process may run on (its CPU affinity), as the oracle's thread count."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def cpu_baseline(calls, weights, xs, seconds: float):
     """The oracle timed on this host's cores over a bounded sample of rows of
-    every call; returns bytes/s in GB/s over the sample."""
+    every call, and on one core over a sample of the DSA B = 1 call; GB/s of
+    algorithmic bytes over the sample (measured seconds reported)."""
     import oracle
-    threads = oracle.max_threads()
+    threads = host_cores()
     oracle.linear_rows(xs[0], weights[calls[0].weight_key], np.arange(4), threads)  # warm
     per_call = seconds / len(calls)
     done_bytes, done_time, rows_total = 0, 0.0, 0
@@ -223,10 +276,27 @@ def cpu_baseline(calls, weights, xs, seconds: float):
             start += idx.size
             rows = max(32, min(4 * rows, int(rows * (per_call - t_call) / max(dt, 1e-6))))
         done_time += t_call
-    return {"value": done_bytes / done_time / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"{rows_total} weight rows in total across the {len(calls)} calls "
-                      f"(all B rows of x each), ~{seconds:.0f} s of oracle work, exact integer "
-                      f"accumulation, OpenMP over outputs"}
+    out = {"value": done_bytes / done_time / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+           "seconds": done_time,
+           "sample": f"{rows_total} weight rows across the {len(calls)} calls (all B rows of x each), "
+                     f"{done_time:.2f} s of oracle work on {threads} threads (CPU affinity), exact integer "
+                     f"accumulation, OpenMP over outputs"}
+    one = next((i for i, c in enumerate(calls) if c.B == 1 and c.N == synth.DSA[0]), None)
+    if one is not None:
+        c, x, W = calls[one], xs[one], weights[calls[one].weight_key]
+        rows, t1, start, nbytes = 16, 0.0, 0, 0
+        while t1 < min(2.0, seconds / 4) and start < c.N:
+            idx = np.arange(start, min(c.N, start + rows))
+            t0 = time.perf_counter()
+            oracle.linear_rows(x, W, idx, 1)
+            dt = time.perf_counter() - t0
+            t1 += dt
+            nbytes += 2 * (idx.size * c.K + c.K + idx.size)
+            start += idx.size
+            rows = min(2 * rows, 1024)
+        out["single_core_dsa_b1"] = {"value": nbytes / t1 / 1e9, "unit": UNIT, "cores": 1, "seconds": t1,
+                                     "rows": start, "call": c.name}
+    return out
 
 
 # ------------------------------------------------------------ reference arm ---
@@ -237,26 +307,26 @@ def run_reference(args):
         return 0
     import oracle
     calls = synth.workload(args.workload)
-    threads = oracle.max_threads()
-    weights, xs = {}, []
-    for c in calls:
-        if c.weight_key not in weights:
-            weights[c.weight_key] = c.weight()
-        xs.append(c.activations())
-    # calibrate rows per call so the whole run stays within about a minute
+    threads = host_cores()
+    xs = [c.activations() for c in calls]
+    # calibrate rows per call so the whole run stays within about a minute; the
+    # sample is the first rows of each weight, generated alone (bit for bit the
+    # rows of the full weight)
     per_row = []
     for c, x in zip(calls, xs):
+        Wh = c.weight_head(64)
         t0 = time.perf_counter()
-        oracle.linear_rows(x, weights[c.weight_key], np.arange(min(c.N, 64)), threads)
-        per_row.append((time.perf_counter() - t0) / min(c.N, 64))
+        oracle.linear_rows(x, Wh, np.arange(Wh.shape[0]), threads)
+        per_row.append((time.perf_counter() - t0) / Wh.shape[0])
     step_budget = min(2.0, 60.0 / max(1, args.steps + args.warmup))
     rows = [max(1, min(c.N, int(step_budget / len(calls) / max(p, 1e-9)))) for c, p in zip(calls, per_row)]
+    heads = [c.weight_head(r) for c, r in zip(calls, rows)]
     idx = [np.arange(r) for r in rows]
     step_bytes = sum(2 * (r * c.K + c.B * c.K + c.B * r) for c, r in zip(calls, rows))
 
     def step():
-        for c, x, i in zip(calls, xs, idx):
-            oracle.linear_rows(x, weights[c.weight_key], i, threads)
+        for x, Wh, i in zip(xs, heads, idx):
+            oracle.linear_rows(x, Wh, i, threads)
 
     for _ in range(args.warmup):
         step()
@@ -271,8 +341,9 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": workload_config(args.workload, calls),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                         "sample": f"per step the first {rows} weight rows of each call "
-                                   f"(all B rows of x)"},
+                         "seconds": elapsed,
+                         "sample": f"per step the first {rows} weight rows of each call (all B rows of x), "
+                                   f"{elapsed:.2f} s of oracle work on {threads} threads (CPU affinity)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -346,8 +417,10 @@ def run_ours(args):
     args_c = [(plans[(c.N, c.K)], x_dev[i].data_ptr(), W_dev[c.weight_key].data_ptr(),
                y_dev[i].data_ptr(), c.B) for i, c in enumerate(calls)]
 
-    def one_step(ev=None):
+    def one_step(ev=None, only=None):
         for i, (p, x, W, y, B) in enumerate(args_c):
+            if only is not None and i not in only:
+                continue
             if ev is not None:
                 ev[i][0].record(stream)
             st = lib.dep_projection_run(p, x, W, y, B, sptr)
@@ -359,6 +432,24 @@ def run_ours(args):
     def barrier():
         if world > 1:
             torch.distributed.barrier()
+
+    def timed_steps(steps, lead, only=None):
+        """Device time of `steps` steps back to back, events at the two ends only;
+        the host stays at most `lead` steps ahead of the GPU."""
+        marks = [torch.cuda.Event() for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for s_ in range(steps):
+            one_step(only=only)
+            marks[s_].record(stream)
+            if s_ >= lead:
+                marks[s_ - lead].synchronize()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        return t0.elapsed_time(t1)
 
     sampler = ClockSampler(device)
     sampler.start()
@@ -374,42 +465,34 @@ def run_ours(args):
 
     # Timed region for `value`: K steps back to back, CUDA events at its two ends
     # only (a pair of events around every call costs the GPU front end a few us
-    # per call, which a decode step does not pay).  Host run-ahead is bounded
-    # with one untimed marker event per step.
-    marks = [torch.cuda.Event() for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    t_start.record(stream)
-    for s in range(args.steps):
-        one_step()
-        marks[s].record(stream)
-        if s >= lead:  # keep the host a bounded number of steps ahead of the GPU
-            marks[s - lead].synchronize()
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
+    # per call, which a decode step does not pay).
+    elapsed_ms = timed_steps(args.steps, lead)
 
     # Instrumented region: the same K steps with every call bracketed by its own
-    # events, for the per-call figures and the dominant kernel's launch duration.
+    # events, for the per-call figures and each kernel's share of the time.
     events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
                for _ in calls] for _ in range(args.steps)]
     i_start, i_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     i_start.record(stream)
-    for s in range(args.steps):
-        one_step(events[s])
-        if s >= lead_ev:
-            events[s - lead_ev][-1][1].synchronize()
+    for s_ in range(args.steps):
+        one_step(events[s_])
+        if s_ >= lead_ev:
+            events[s_ - lead_ev][-1][1].synchronize()
     i_end.record(stream)
     torch.cuda.synchronize()
     barrier()
-    clocks = sampler.stop()
     instrumented_ms = reduce_max(i_start.elapsed_time(i_end))
-    call_ms = np.array([[events[s][i][0].elapsed_time(events[s][i][1]) for i in range(len(calls))]
-                        for s in range(args.steps)])
+    call_ms = np.array([[events[s_][i][0].elapsed_time(events[s_][i][1]) for i in range(len(calls))]
+                        for s_ in range(args.steps)])
+
+    # Each kernel family's launch duration: its calls alone, K steps back to back.
+    families = {}
+    for i, t in enumerate(tactics):
+        families.setdefault(kernel_name(t), []).append(i)
+    family_ms = {k: reduce_max(timed_steps(args.steps, lead, only=set(v))) for k, v in families.items()}
+    clocks = sampler.stop()
     for p in plans.values():
         code = dep.dep_projection_device_status(p)
         if code:
@@ -417,48 +500,29 @@ def run_ours(args):
     elapsed_ms = reduce_max(elapsed_ms)
     value = whole_job_gbs(bytes_per_step, args.steps, world, elapsed_ms)
     peak, peak_src = read_peaks()
+    ceilings = None if args.no_ceiling else probe_ceilings(dep, device)
 
-    # per-kernel totals over the timed region; the dominant kernel's roofline
-    per_kernel = {}
-    for i, (c, t) in enumerate(zip(calls, tactics)):
-        k = kernel_name(t)
-        d = per_kernel.setdefault(k, {"ms": 0.0, "bytes": 0, "launches": 0})
-        d["ms"] += float(call_ms[:, i].sum())
-        d["bytes"] += c.algorithmic_bytes * args.steps
-        d["launches"] += -(-c.B // t.cols) * args.steps
-    dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
-    d = per_kernel[dom]
-    achieved_bracketed = d["bytes"] / (d["ms"] * 1e-3) / 1e9
+    rooflines = {}
+    total_call_ms = call_ms.sum() or 1.0
+    for k, idx in families.items():
+        nbytes = sum(calls[i].algorithmic_bytes for i in idx) * args.steps
+        launches = sum(-(-calls[i].B // tactics[i].cols) for i in idx) * args.steps
+        achieved = nbytes / (family_ms[k] * 1e-3) / 1e9
+        bracketed = nbytes / (float(call_ms[:, idx].sum()) * 1e-3) / 1e9
+        r = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
+             "traffic": read_traffic(k, args.workload), "kernel": k,
+             "peak_source": f"{peak_src} (HBM copy bandwidth, MEASURED_PEAKS.json)",
+             "calls": [calls[i].name for i in idx],
+             "bytes_per_launch": nbytes / launches, "us_per_launch": family_ms[k] * 1e3 / launches,
+             "duration_timing": "the family's calls alone, K steps back to back, CUDA events at the region's ends",
+             "achieved_with_per_call_events": bracketed,
+             "share_of_timed_region": float(call_ms[:, idx].sum()) / total_call_ms}
+        if ceilings:
+            r["frac_of_inrun_copy"] = achieved / ceilings["copy_gbs"]
+            r["frac_of_inrun_read"] = achieved / ceilings["read_gbs"]
+        rooflines[k] = r
+    dom = max(rooflines, key=lambda k: rooflines[k]["share_of_timed_region"])
 
-    # The dominant kernel's launch duration: its calls alone, K steps back to
-    # back on the launching stream, CUDA events at the two ends of the region.
-    dom_calls = [i for i, t in enumerate(tactics) if kernel_name(t) == dom]
-    d_start, d_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    d_start.record(stream)
-    for s in range(args.steps):
-        for i in dom_calls:
-            p, x, W, y, B = args_c[i]
-            st = lib.dep_projection_run(p, x, W, y, B, sptr)
-            if st:
-                raise dep.DepError(st, "dep_projection_run")
-        marks[s].record(stream)
-        if s >= lead:
-            marks[s - lead].synchronize()
-    d_end.record(stream)
-    torch.cuda.synchronize()
-    dom_ms = reduce_max(d_start.elapsed_time(d_end))
-    achieved = d["bytes"] / (dom_ms * 1e-3) / 1e9
-    traffic = read_traffic(dom, args.workload)
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": UNIT,
-                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
-                "peak_source": f"{peak_src} (HBM copy bandwidth)",
-                "bytes_per_launch": d["bytes"] / d["launches"],
-                "us_per_launch": dom_ms * 1e3 / d["launches"],
-                "duration_timing": "the kernel's calls alone, K steps back to back, CUDA events at the "
-                                   "region's ends",
-                "achieved_with_per_call_events": achieved_bracketed,
-                "share_of_timed_region": d["ms"] / (call_ms.sum() or 1.0)}
     per_call = []
     for i, (c, t) in enumerate(zip(calls, tactics)):
         # Event timestamps tick in about 2 us steps: the mean over the timed
@@ -473,9 +537,13 @@ def run_ours(args):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, dep, calls, plans, xs_host, W_dev, device, world)
-    graph = None
+    graph = graph_calls = None
     if not args.no_graph:
         graph = run_graph_pdl(args, dep, calls, x_dev, W_dev, y_dev, device, world, flags)
+        graph_calls = run_graph_per_call(args, dep, calls, x_dev, W_dev, y_dev, flags, peak)
+        for pc, g in zip(per_call, graph_calls):
+            pc["graph_pdl_us"] = g["us"]
+            pc["graph_pdl_frac_of_peak"] = g["frac_of_peak"]
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -489,11 +557,12 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_config(args.workload, calls),
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-            "graph_pdl": graph,
+            "roofline": rooflines[dom], "roofline_by_kernel": rooflines, "ceilings": ceilings,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "graph_pdl": graph,
             "timing": "value: K steps back to back, CUDA events at the region's ends only; per_call: "
                       "the same K steps again with every call bracketed by its own events "
-                      f"({instrumented_ms / args.steps:.4f} ms per step with those events)",
+                      f"({instrumented_ms / args.steps:.4f} ms per step with those events); graph_pdl_us: "
+                      "a CUDA graph of back-to-back launches of the call with programmatic dependent launch",
             "gpu_launches": launches_per_step * args.steps, "per_call": per_call,
             "plan": "tune" if tuned else "default", "kernel_sources": source_hash(),
             "device": torch.cuda.get_device_name(device),
@@ -504,15 +573,109 @@ def run_ours(args):
     return 0
 
 
+def probe_ceilings(dep, device):
+    """Bandwidth ceilings measured in this run: a 2 GiB device-to-device copy
+    (read + write bytes, as the copy figure of MEASURED_PEAKS.json counts them)
+    and the library's read-only streaming kernel over 2 GiB; best of 10 each,
+    CUDA events on the launching stream."""
+    import torch
+    n = 1 << 30  # BF16 elements: 2 GiB
+    src = torch.empty(n, dtype=torch.bfloat16, device=device).fill_(1.0)
+    dst = torch.empty_like(src)
+    sink = torch.zeros(1, dtype=torch.int64, device=device)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def best(fn, reps=10):
+        fn()
+        torch.cuda.synchronize()
+        out = []
+        for _ in range(reps):
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1))
+        return min(out)
+
+    copy_ms = best(lambda: dst.copy_(src))
+    read_ms = best(lambda: dep.dep_projection_probe_read(src, 2 * n, sink, stream))
+    del src, dst
+    torch.cuda.empty_cache()
+    return {"copy_gbs": 2 * (2 * n) / (copy_ms * 1e-3) / 1e9, "read_gbs": (2 * n) / (read_ms * 1e-3) / 1e9,
+            "bytes": 2 * n, "how": "device-to-device copy of 2 GiB (read + write bytes) and a read-only "
+                                   "16-byte streaming kernel over 2 GiB (dep_projection_probe_read); best of 10, "
+                                   "CUDA events"}
+
+
+def run_graph_per_call(args, dep, calls, x_dev, W_dev, y_dev, flags, peak):
+    """Per call, in the deployment's launch mode: a CUDA graph of R back-to-back
+    launches of that call on a plan with programmatic dependent launch, the
+    weight rotated over every distinct weight of its shape in the workload (so
+    no launch finds its weight in L2), replayed; time per launch."""
+    import torch
+    keys = {}
+    for c in calls:
+        keys.setdefault((c.N, c.K), set()).add(c.B)
+    plans = {k: dep.dep_projection_plan(k[0], k[1], sorted(v), flags | dep.DEP_PLAN_PDL)
+             for k, v in keys.items()}
+    by_shape = {}
+    for c in calls:
+        ws = by_shape.setdefault((c.N, c.K), [])
+        if W_dev[c.weight_key].data_ptr() not in [w.data_ptr() for w in ws]:
+            ws.append(W_dev[c.weight_key])
+    lib = dep.lib()
+    stream = torch.cuda.Stream()
+    R, reps = 16, 10
+    out = []
+    for i, c in enumerate(calls):
+        p, ws = plans[(c.N, c.K)], by_shape[(c.N, c.K)]
+        x, y = x_dev[i].data_ptr(), y_dev[i].data_ptr()
+
+        def launches(sptr):
+            for r in range(R):
+                st = lib.dep_projection_run(p, x, ws[r % len(ws)].data_ptr(), y, c.B, sptr)
+                if st:
+                    raise dep.DepError(st, "dep_projection_run")
+
+        with torch.cuda.stream(stream):
+            launches(stream.cuda_stream)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launches(stream.cuda_stream)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        cur = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        for _ in range(reps):
+            g.replay()
+        e1.record(cur)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * R)
+        gbs = c.algorithmic_bytes / (us * 1e-6) / 1e9
+        out.append({"call": c.name, "us": us, "gbs": gbs, "frac_of_peak": gbs / peak, "weights_rotated": len(ws)})
+        del g
+    for p in plans.values():
+        code = dep.dep_projection_device_status(p)
+        if code:
+            raise RuntimeError(f"a kernel reported device status {code}")
+        dep.dep_projection_plan_destroy(p)
+    return out
+
+
 def run_ahead_steps(step_ms: float, entries_per_step: int) -> int:
     """Steps the host may enqueue ahead of the GPU in a timed loop: about 20 ms
-    of queued work, and at most about 400 queued operations.  Enough that a
+    of queued work, and at most about 200 queued operations (launches with three
+    tensor maps as parameters take more room in the launch queue than plain ones).  Enough that a
     host thread descheduled for a few ms does not let the GPU run dry, few
     enough that the launch queue never fills (a full queue blocks the host
     inside a launch call, and a host woken late from that block lets the GPU
     drain in the middle of a timed call)."""
     by_time = int(np.ceil(20.0 / max(step_ms, 1e-3)))
-    by_queue = 400 // max(1, entries_per_step)
+    by_queue = 200 // max(1, entries_per_step)
     return max(2, min(by_time, by_queue))
 
 

@@ -204,6 +204,19 @@ dep_status_t dep_projection_run_host(dep_plan_t plan, const void *x_host, const 
 dep_status_t dep_projection_run_static(const void *x, const void *W, void *y, int64_t N,
                                        int64_t K, int32_t B, void *stream);
 
+/*
+ * No counterpart in the pages: a measurement aid.  Reads `bytes` of device
+ * memory at p once with a read-only streaming kernel (16-byte loads, four in
+ * flight per thread, four 512-thread blocks per SM) and XORs a fold of what it
+ * read into the 64-bit word *sink (device memory), so that timing it on
+ * `stream` gives the device's read-only bandwidth: the ceiling of a call that
+ * streams a weight and writes almost nothing (a device-to-device copy also
+ * writes as many bytes as it reads).  p 16-byte aligned, bytes a multiple of
+ * 16, sink 8-byte aligned (else MISALIGNED); INVALID_ARG for null pointers or
+ * zero bytes; CUDA if the launch fails.  Asynchronous.
+ */
+dep_status_t dep_projection_probe_read(const void *p, size_t bytes, void *sink, void *stream);
+
 /* The tactic the plan uses for a batch of B >= 1 rows. */
 dep_status_t dep_projection_plan_query(dep_plan_t plan, int32_t B, dep_tactic_t *out);
 

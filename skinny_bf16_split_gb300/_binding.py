@@ -49,7 +49,7 @@ EXPORTS = (
     "dep_projection_plan_save", "dep_projection_plan_load", "dep_projection_plan_destroy",
     "dep_projection_device_status", "dep_projection_selftest_timeout", "dep_bins_index",
     "dep_status_string", "dep_projection_version", "dep_projection_run_static",
-    "dep_projection_plan_partials", "dep_projection_plan_exchange",
+    "dep_projection_plan_partials", "dep_projection_plan_exchange", "dep_projection_probe_read",
 )
 
 
@@ -106,6 +106,7 @@ def lib():
         "dep_projection_run_static": ([vp, vp, vp, i64, i64, i32, vp], i32),
         "dep_projection_plan_partials": ([vp, vp, ctypes.c_size_t, P(ctypes.c_size_t)], i32),
         "dep_projection_plan_exchange": ([vp, vp, ctypes.c_size_t, P(ctypes.c_size_t)], i32),
+        "dep_projection_probe_read": ([vp, ctypes.c_size_t, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -280,6 +281,12 @@ def dep_projection_run_static(x, W, y, N: int | None = None, K: int | None = Non
         B = x.shape[0]
     _check(lib().dep_projection_run_static(_ptr(x), _ptr(W), _ptr(y), N, K, B, _stream(stream)),
            "dep_projection_run_static")
+
+
+def dep_projection_probe_read(p, nbytes: int, sink, stream=None) -> None:
+    """Read-only streaming pass over nbytes of device memory at p (measurement aid)."""
+    _check(lib().dep_projection_probe_read(_ptr(p), nbytes, _ptr(sink), _stream(stream)),
+           "dep_projection_probe_read")
 
 
 class Projection:

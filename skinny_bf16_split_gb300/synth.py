@@ -130,6 +130,19 @@ def normal_bf16(seed: int, tensor: int, shape, sigma: float = 1.0,
     return out[:count].reshape(shape)
 
 
+def normal_bf16_head(seed: int, tensor: int, shape, rows: int, sigma: float = 1.0) -> np.ndarray:
+    """The first `rows` rows of normal_bf16(seed, tensor, shape, sigma), bit for
+    bit, without generating the rest (the stream is counter-based: element n of
+    a row-major tensor depends only on n)."""
+    shape = tuple(int(s) for s in shape)
+    cols = int(np.prod(shape[1:])) if len(shape) > 1 else 1
+    rows = max(0, min(int(rows), shape[0]))
+    count = rows * cols
+    pairs = (count + 1) // 2
+    vals = bf16_from_f64(_normals_pairs(_key(seed, tensor), 0, pairs) * sigma) if pairs else np.empty(0, np.uint16)
+    return vals[:count].reshape((rows,) + shape[1:])
+
+
 def rms_rows_bf16(seed: int, tensor: int, shape) -> np.ndarray:
     """BF16 bits of N(0,1) rows each scaled (in float64) to unit RMS."""
     rows, cols = (int(s) for s in shape)
@@ -164,6 +177,10 @@ class Call:
 
     def weight(self) -> np.ndarray:
         return normal_bf16(self.seed, self.w_id, (self.N, self.K), sigma=0.02)
+
+    def weight_head(self, rows: int) -> np.ndarray:
+        """The first `rows` rows of weight() (for sampled CPU work)."""
+        return normal_bf16_head(self.seed, self.w_id, (self.N, self.K), rows, sigma=0.02)
 
     def activations(self) -> np.ndarray:
         if self.x_rms:
@@ -203,6 +220,10 @@ def workload(name: str) -> list[Call]:
         for s, g in enumerate((2, 4, 8)):
             calls.append(Call(f"oproj_tp{g}", OPROJ[0], OPROJ[1] // g, B=16, seed=3 + s))
         return calls
+    if name == "baseline":
+        # the five configurations of the decode-projection benchmark in one step:
+        # DSA B=1, the o_proj sweep, the KDA sweep, wide DSA batches, the chain
+        return [c for part in ("dsa_b1", "oproj_sweep", "kda_sweep", "dsa_wide", "chain") for c in workload(part)]
     if name == "chain":
         calls = []
         for layer in range(8):
@@ -214,4 +235,4 @@ def workload(name: str) -> list[Call]:
     raise KeyError(f"unknown workload {name!r}")
 
 
-WORKLOADS = ("dsa_b1", "oproj_sweep", "kda_sweep", "dsa_wide", "chain", "dsa_verify", "tp_sharded")
+WORKLOADS = ("baseline", "dsa_b1", "oproj_sweep", "kda_sweep", "dsa_wide", "chain", "dsa_verify", "tp_sharded")
