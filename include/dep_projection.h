@@ -291,6 +291,9 @@ dep_status_t dep_projection_device_status(dep_plan_t plan, void *stream, int32_t
 #define DEP_DEV_TIMEOUT_CONSUMER 2 /* a compute warp gave up waiting for a stage's data */
 #define DEP_DEV_TIMEOUT_MMA 3      /* the MMA warp gave up waiting */
 #define DEP_DEV_TIMEOUT_EPILOGUE 4 /* an epilogue warp gave up waiting for an accumulator */
+#define DEP_DEV_BOUNDS 5           /* bounds-checked (DEP_DEBUG) builds only: a kernel
+                                      computed an index past one of its buffers and
+                                      skipped that access */
 
 /*
  * Bounded-wait self-test: launches one block whose waits can never be satisfied
@@ -300,6 +303,22 @@ dep_status_t dep_projection_device_status(dep_plan_t plan, void *stream, int32_t
  * came back by itself.  Exercises the give-up path without faulting the GPU.
  */
 dep_status_t dep_projection_selftest_timeout(int32_t limit_us, int32_t *code);
+
+/*
+ * Give-up self-test of the split-K exchange, on a plan's own workspace: enqueues
+ * on `stream` one warp that publishes ("full") exchange words of two pieces,
+ * as publishers would, then runs the exchange's reducer over two pieces of
+ * which one is never published, with a wait limit of `limit_us` microseconds.
+ * The reducer gives up and records DEP_DEV_TIMEOUT_EPILOGUE in the plan's
+ * status word; the unreduced piece's flags and a nonzero word at the start of
+ * the counters are left behind.  dep_projection_device_status then reports the code and clears the
+ * counters and exchange words, after which the plan's runs give the same bits
+ * as a fresh plan's.  Exercises the give-up path without faulting the GPU.
+ * Errors: INVALID_ARG (null plan, limit outside 1 us..10 s), UNSUPPORTED
+ * (host-only plan, or a plan whose table has no tensor-core tactic and so no
+ * exchange region), CUDA.
+ */
+dep_status_t dep_projection_plan_selftest_exchange(dep_plan_t plan, int32_t limit_us, void *stream);
 
 /* The binning rule on its own: index into keys[0..n_keys) of the entry serving
  * B rows -- smallest key >= B, else the largest key; -1 if n_keys < 1.  The keys

@@ -40,6 +40,7 @@ DEP_DEV_TIMEOUT_PRODUCER = 1
 DEP_DEV_TIMEOUT_CONSUMER = 2
 DEP_DEV_TIMEOUT_MMA = 3
 DEP_DEV_TIMEOUT_EPILOGUE = 4
+DEP_DEV_BOUNDS = 5
 
 # Every symbol include/dep_projection.h declares.
 EXPORTS = (
@@ -50,6 +51,7 @@ EXPORTS = (
     "dep_projection_device_status", "dep_projection_selftest_timeout", "dep_bins_index",
     "dep_status_string", "dep_projection_version", "dep_projection_run_static",
     "dep_projection_plan_partials", "dep_projection_plan_exchange", "dep_projection_probe_read",
+    "dep_projection_plan_selftest_exchange",
 )
 
 
@@ -107,6 +109,7 @@ def lib():
         "dep_projection_plan_partials": ([vp, vp, ctypes.c_size_t, P(ctypes.c_size_t)], i32),
         "dep_projection_plan_exchange": ([vp, vp, ctypes.c_size_t, P(ctypes.c_size_t)], i32),
         "dep_projection_probe_read": ([vp, ctypes.c_size_t, vp, vp], i32),
+        "dep_projection_plan_selftest_exchange": ([vp, i32, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -281,6 +284,12 @@ def dep_projection_run_static(x, W, y, N: int | None = None, K: int | None = Non
         B = x.shape[0]
     _check(lib().dep_projection_run_static(_ptr(x), _ptr(W), _ptr(y), N, K, B, _stream(stream)),
            "dep_projection_run_static")
+
+
+def dep_projection_plan_selftest_exchange(plan, limit_us: int, stream=None) -> None:
+    """Enqueue the split-K exchange's give-up self-test on the plan's workspace."""
+    _check(lib().dep_projection_plan_selftest_exchange(plan, limit_us, _stream(stream)),
+           "dep_projection_plan_selftest_exchange")
 
 
 def dep_projection_probe_read(p, nbytes: int, sink, stream=None) -> None:

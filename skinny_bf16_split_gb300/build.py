@@ -31,18 +31,30 @@ def _flags(extra=()):
             "-I", INCLUDE, "-I", CSRC, *extra]
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every translation unit and link the library; return its path."""
-    os.makedirs(OUT_DIR, exist_ok=True)
+DEBUG_DIR = os.path.join(HERE, "_build_debug")
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile every translation unit and link the library; return its path.
+
+    debug=True builds the bounds-checked variant (-DDEP_DEBUG) into _build_debug/:
+    every kernel checks each index into y, the plan's workspace and shared
+    memory before using it, records DEP_DEV_BOUNDS in the status word and skips
+    the access if it is out of range."""
+    out_dir = DEBUG_DIR if debug else OUT_DIR
+    lib_path = os.path.join(out_dir, "libdep_projection.so")
+    if debug:
+        extra_flags = ("-DDEP_DEBUG", *extra_flags)
+    os.makedirs(out_dir, exist_ok=True)
     deps = [os.path.join(CSRC, s) for s in SOURCES + HEADERS]
     deps.append(os.path.join(INCLUDE, "dep_projection.h"))
     newest = max(os.path.getmtime(p) for p in deps)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= newest and not extra_flags:
-        return LIB
+    if not force and os.path.exists(lib_path) and os.path.getmtime(lib_path) >= newest and (debug or not extra_flags):
+        return lib_path
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, src + ".o")
+        obj = os.path.join(out_dir, src + ".o")
         cmd = [nvcc, *_flags(extra_flags), "-c", os.path.join(CSRC, src), "-o", obj]
         if src.endswith(".cpp"):
             cmd[1:1] = ["-x", "cu"]  # host-only code, still built by nvcc for one toolchain
@@ -55,15 +67,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else ()))
+                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else (), debug="--debug" in sys.argv))

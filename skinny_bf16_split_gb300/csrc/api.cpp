@@ -1051,6 +1051,22 @@ dep_status_t dep_projection_selftest_timeout(int32_t limit_us, int32_t *code)
     return DEP_OK;
 }
 
+dep_status_t dep_projection_plan_selftest_exchange(dep_plan_t plan, int32_t limit_us, void *stream)
+{
+    if (!plan || limit_us < 1 || limit_us > 10000000)
+        return DEP_ERR_INVALID_ARG;
+    if (plan->host_only)
+        return DEP_ERR_UNSUPPORTED;
+    if (plan->xch_words < 4 * 16 * 32 || plan->n_counters < 1)
+        return DEP_ERR_UNSUPPORTED;  // a plan without tensor-core tactics has no exchange region
+    if (dep::tcs_selftest_exchange(plan->xch, plan->xch_words, plan->counters, plan->status,
+                                   (uint64_t)limit_us * 1000ull, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return DEP_ERR_CUDA;
+    }
+    return DEP_OK;
+}
+
 const char *dep_status_string(dep_status_t s)
 {
     switch (s) {

@@ -12,6 +12,14 @@
 
 namespace dep {
 
+// Sizes of what one launch may index, for the bounds checks of the DEP_DEBUG
+// build (elements of y, of the split-K partials, counters and exchange words,
+// and bytes of dynamic shared memory).  Passed to every kernel; other builds
+// compile the checks away.
+struct Bounds {
+    unsigned long long y, ws, counters, xch, smem;
+};
+
 // One launch's operands and the plan-owned scratch it may use.
 struct RunArgs {
     const uint16_t *x;  // [B, K] BF16 bits, device
@@ -34,6 +42,11 @@ struct RunArgs {
     bool pdl = false;
     // The wide kernel also stores the partials its blocks reduce themselves.
     bool keep_pieces = false;
+    // What a launch of `y_rows` batch rows with `smem` bytes of shared memory may index.
+    Bounds bounds(int64_t y_rows, size_t smem) const
+    {
+        return Bounds{(unsigned long long)y_rows * (unsigned long long)N, ws_floats, n_counters, xch_words, smem};
+    }
 };
 
 // Shared memory a block of any kernel here may use (the sm_100-family opt-in maximum).
@@ -170,6 +183,8 @@ size_t tcs_xch_words(const dep_tactic_t &t, int64_t N, int64_t K);  // every pie
 size_t tcs_counters(const dep_tactic_t &t, int64_t N);               // the last 2 counters
 int tcs_blocks_per_sm(const dep_tactic_t &t);
 cudaError_t tcs_run(const dep_tactic_t &t, const RunArgs &a);       // uses the last 2 counters
+cudaError_t tcs_selftest_exchange(unsigned long long *xch, size_t xch_words, int *counters, int *status,
+                                  uint64_t limit_ns, cudaStream_t stream);
 
 // ---- tcgen05 tactic for wide batches, groups of tiles per x slice (tc_wide.cu) ----
 bool wide_valid(const dep_tactic_t &t);

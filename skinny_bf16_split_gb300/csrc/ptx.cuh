@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <stdint.h>
 
+#include "../../include/dep_projection.h"
+
 namespace dep {
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -118,6 +120,30 @@ __device__ __forceinline__ void record_status(int *status, int code)
 {
     if (status)
         atomicCAS(status, 0, code);
+}
+
+// Bounds check of the DEP_DEBUG build: an index at or past the buffer's size
+// records DEP_DEV_BOUNDS and the caller skips the access.  In other builds the
+// check is compiled away (always true).
+__device__ __forceinline__ bool dbg_ok(unsigned long long idx, unsigned long long n, int *status)
+{
+#ifdef DEP_DEBUG
+    if (idx < n)
+        return true;
+    record_status(status, DEP_DEV_BOUNDS);
+    return false;
+#else
+    (void)idx;
+    (void)n;
+    (void)status;
+    return true;
+#endif
+}
+// The same for a range [off, off + len).
+__device__ __forceinline__ bool dbg_range(unsigned long long off, unsigned long long len, unsigned long long n,
+                                          int *status)
+{
+    return dbg_ok(off + len - 1, n, status) && dbg_ok(off, n, status);
 }
 
 // ---- tcgen05 (5th-generation tensor cores, accumulators in tensor memory) ----

@@ -79,11 +79,13 @@ template <int BC, int RW>
 __global__ void __launch_bounds__(kThreads, 1)
     rows_gemv_kernel(const uint16_t *__restrict__ x, const __grid_constant__ CUtensorMap tmW, uint16_t *__restrict__ y,
                      int B, int N, int K, int KC, int stages, int *__restrict__ counters,
-                     int *__restrict__ status, uint64_t limit_ns)
+                     int *__restrict__ status, const Bounds bd, uint64_t limit_ns)
 {
     constexpr int TN = kWarps * RW;
     extern __shared__ __align__(1024) uint8_t smem[];
     const RowsLayout L(BC, TN, KC, stages, K);
+    if (!dbg_ok(L.total - 1, bd.smem, status))
+        return;  // x, the ring and the barriers must lie in the launch's shared memory
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);
     int2 *tags = reinterpret_cast<int2 *>(smem + L.tags);  // (tile, chunk) per stage; tile < 0: end
@@ -268,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < BC; ++b)
                 if (lane == i * BC + b) {
                     const int64_t n = (int64_t)row0 + warp * RW + i;
-                    if (b < B && n < N)
+                    if (b < B && n < N && dbg_ok((int64_t)b * N + n, bd.y, status))
                         y[(int64_t)b * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i][b]));
                 }
     }
@@ -365,7 +367,8 @@ cudaError_t rows_run(const dep_tactic_t &t, const RunArgs &a)
             const int32_t rows = a.B - r0 < BC ? a.B - r0 : BC;
             e = launch(rows_gemv_kernel<BC, RW>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl,
                        a.x + (size_t)r0 * a.K, tmW, a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K,
-                       t.tile_k, t.stages, a.counters + a.n_counters - 2, a.status, a.wait_limit_ns);
+                       t.tile_k, t.stages, a.counters + a.n_counters - 2, a.status, a.bounds(rows, smem),
+                       a.wait_limit_ns);
         }
     });
     return e;

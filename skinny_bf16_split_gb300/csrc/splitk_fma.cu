@@ -67,10 +67,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     splitk_fma_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       uint16_t *__restrict__ y, int B, int N, int K, int stages,
                       float *__restrict__ ws, int *__restrict__ counters, int *__restrict__ status,
-                      uint64_t limit_ns)
+                      const Bounds bd, uint64_t limit_ns)
 {
     constexpr int R = Shape<BC, TN_>::R, TN = TN_, STAGE_BYTES = Shape<BC, TN_>::STAGE_BYTES;
     extern __shared__ __align__(1024) uint8_t smem[];
+    if (!dbg_ok((size_t)stages * STAGE_BYTES + 16 * (size_t)stages - 1, bd.smem, status))
+        return;  // the ring and its barriers must lie in the launch's shared memory
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * STAGE_BYTES);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + stages);
 
@@ -218,17 +220,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t n = t * TN + row;
 
         if (whole) {
-            if (have && mb < B && n < N)
+            if (have && mb < B && n < N && dbg_ok((int64_t)mb * N + n, bd.y, status))
                 y[(int64_t)mb * N + n] = to_bf16(mine);
             continue;
         }
         const int slot = (t == first_t) ? 0 : 1;
-        if (have)
+        if (have && dbg_ok(((c * 2 + slot) * BC + mb) * TN + row, bd.ws, status))
             __stcg(&ws[((c * 2 + slot) * BC + mb) * TN + row], mine);
         __threadfence();
         __syncwarp();
         int prev = 0;
-        if (lane == 0)
+        if (lane == 0 && dbg_ok(t * kWarps + warp, bd.counters, status))
             prev = atomicAdd(&counters[t * kWarps + warp], 1);
         prev = __shfl_sync(0xFFFFFFFFu, prev, 0);
         const int64_t c0 = sk_owner(t * KTILES, U, C), c1 = sk_owner(t * KTILES + KTILES - 1, U, C);
@@ -244,17 +246,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < 4; ++i) {
                     const int64_t cc = g0 + i;
                     const int sl = (t == sk_begin(cc, U, C) / KTILES) ? 0 : 1;
-                    p[i] = cc <= c1 ? __ldcg(&ws[((cc * 2 + sl) * BC + mb) * TN + row]) : 0.0f;
+                    p[i] = cc <= c1 && dbg_ok(((cc * 2 + sl) * BC + mb) * TN + row, bd.ws, status)
+                               ? __ldcg(&ws[((cc * 2 + sl) * BC + mb) * TN + row])
+                               : 0.0f;
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (g0 + i <= c1)
                         sum = (g0 + i == c0) ? p[i] : sum + p[i];
             }
-            if (mb < B && n < N)
+            if (mb < B && n < N && dbg_ok((int64_t)mb * N + n, bd.y, status))
                 y[(int64_t)mb * N + n] = to_bf16(sum);
         }
-        if (lane == 0)
+        if (lane == 0 && dbg_ok(t * kWarps + warp, bd.counters, status))
             counters[t * kWarps + warp] = 0;  // ready for the next launch
     }
 }
@@ -324,7 +328,7 @@ cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
             return cudaErrorInvalidValue;
         e = launch(splitk_fma_kernel<BC, TN>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
                    a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, a.ws, a.counters, a.status,
-                   a.wait_limit_ns);
+                   a.bounds(rows, smem), a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }

@@ -213,7 +213,7 @@ template <int NT, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_cluster_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ CUtensorMap tmY, uint16_t *__restrict__ y, int B, int N, int K,
-                      int SW, int SX, int use_tma_y, int *__restrict__ status, uint64_t limit_ns)
+                      int SW, int SX, int use_tma_y, int *__restrict__ status, const Bounds bd, uint64_t limit_ns)
 {
     using S = ClusterShape<NT, G>;
     extern __shared__ uint8_t smem_raw[];
@@ -222,6 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = smem_raw + (base - raw);
     const uint32_t xbase = base + (uint32_t)(SW * S::W_STAGE);
     const int RING = SW * S::W_STAGE + SX * S::X_STAGE;
+    // The rings, the barriers and the TMEM slot must lie in the launch's shared
+    // memory, and the received partials and the y staging in the rings.
+    if (!dbg_ok((base - raw) + (size_t)RING + (size_t)barrier_count(SW, SX) * 8 + 8 - 1, bd.smem, status) ||
+        !dbg_ok(stage_offset(S::NCB, (int)cluster_size(), S::CB_BYTES) + stage_bytes(S::CBW) - 1, (unsigned)RING,
+                status))
+        return;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)RING);
     const uint32_t wfull0 = smem_u32(bars), wempty0 = wfull0 + 8 * SW;
     const uint32_t xfull0 = wempty0 + 8 * SW, xempty0 = xfull0 + 8 * SX;
@@ -489,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int c0 = share_begin(p, S::NCB, k), c1 = share_begin(p + 1, S::NCB, k);
                     const uint32_t pbar = peer_addr(rx_full, (uint32_t)p);
                     for (int cb = c0; cb < c1; ++cb) {
-                        if (col_b0(cb) >= B)
+                        if (col_b0(cb) >= B || !dbg_range(recv_off(rank, p, cb, c0), S::CB_BYTES, (unsigned)RING, status))
                             continue;
                         const uint32_t dst = peer_addr(base + recv_off(rank, p, cb, c0), (uint32_t)p);
 #pragma unroll 1
@@ -543,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
                                 v[j] = __uint_as_float(own[j]);
-                        } else {
+                        } else if (dbg_range(recv_off(p, rank, cb, c0), S::CB_BYTES, (unsigned)RING, status)) {
                             const float4 *src = reinterpret_cast<const float4 *>(
                                 smem + recv_off(p, rank, cb, c0) + (size_t)c16 * 128);
 #pragma unroll
@@ -554,6 +560,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 v[4 * i + 2] = f.z;
                                 v[4 * i + 3] = f.w;
                             }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                v[j] = 0.0f;  // (bounds-checked builds only: the check above failed)
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
@@ -566,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (b0 + c16 + j < B && n < N)
+                            if (b0 + c16 + j < B && n < N && dbg_ok((int64_t)(b0 + c16 + j) * N + n, bd.y, status))
                                 y[(int64_t)(b0 + c16 + j) * N + n] = to_bf16(sum[j]);
                     }
                 }
@@ -707,7 +717,8 @@ cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, tc_cluster_kernel<NT, G>, tmW, tmX, tmY, a.y + (size_t)r0 * a.N, (int)rows,
-                               (int)a.N, (int)a.K, (int)t.stages, sx, tma_y ? 1 : 0, a.status, a.wait_limit_ns);
+                               (int)a.N, (int)a.K, (int)t.stages, sx, tma_y ? 1 : 0, a.status, a.bounds(rows, smem),
+                               a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }

@@ -67,7 +67,7 @@ template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms,
-                   unsigned long long *__restrict__ xch, int *__restrict__ status,
+                   unsigned long long *__restrict__ xch, int *__restrict__ status, const Bounds bd,
                    uint64_t limit_ns)
 {
     using S = TcShape<NT>;
@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles need 1 KB alignment
     uint8_t *smem = smem_raw + (base - raw);
+    if (!dbg_ok((base - raw) + (size_t)stages * STAGE + (2 * (size_t)stages + 5) * 8 + 8 - 1, bd.smem, status))
+        return;  // the ring, the barriers and the TMEM slot must lie in the launch's shared memory
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * STAGE);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * stages;
@@ -277,24 +279,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (whole) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (j < ncols && n < N)
+                        if (j < ncols && n < N && dbg_ok((int64_t)(c0 + j) * N + n, bd.y, status))
                             y[(int64_t)(c0 + j) * N + n] = to_bf16(__uint_as_float(v[j]));
                     continue;
                 }
                 if (c != c_last) {  // publish this block's piece
-                    xch::publish16(xch + ((c * 2) * NT + c0) * kBM + row, kBM, v, ncols);
+                    const int64_t w0 = ((c * 2) * NT + c0) * kBM + row;
+                    if (dbg_range(w0, 15 * kBM + 1, bd.xch, status))
+                        xch::publish16(xch + w0, kBM, v, ncols);
                     continue;
                 }
                 float sum[16];
-                if (!xch::reduce16(xch + ((c_first * 2) * NT + c0) * kBM + row, 2 * (int64_t)NT * kBM, kBM,
-                                   (int)(c_last - c_first), ncols, v, xch + ((c * 2 + 1) * NT + c0) * kBM + row,
-                                   sum, limit_ns)) {
+                const int64_t r0 = ((c_first * 2) * NT + c0) * kBM + row, own0 = ((c * 2 + 1) * NT + c0) * kBM + row;
+                if (!dbg_range(r0, (c_last - c_first - 1) * 2 * (int64_t)NT * kBM + 15 * kBM + 1, bd.xch, status) ||
+                    !dbg_range(own0, 15 * kBM + 1, bd.xch, status)) {
+                    ok = false;
+                } else if (!xch::reduce16(xch + r0, 2 * (int64_t)NT * kBM, kBM, (int)(c_last - c_first), ncols, v,
+                                          xch + own0, sum, limit_ns)) {
                     record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
                     ok = false;
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    if (j < ncols && n < N && ok)
+                    if (j < ncols && n < N && ok && dbg_ok((int64_t)(c0 + j) * N + n, bd.y, status))
                         y[(int64_t)(c0 + j) * N + n] = to_bf16(sum[j]);
             }
             tc::fence_before();
@@ -350,7 +357,7 @@ cudaError_t run_nt(const dep_tactic_t &t, const RunArgs &a)
             return cudaErrorInvalidValue;
         e = launch(tc_gemm_kernel<NT>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
                    a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, a.xch, a.status,
-                   a.wait_limit_ns);
+                   a.bounds(rows, smem), a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }

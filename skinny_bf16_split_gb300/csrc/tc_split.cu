@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_split_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                     uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms, int S,
                     unsigned long long *__restrict__ xch, int *__restrict__ dispenser,
-                    int *__restrict__ status, uint64_t limit_ns)
+                    int *__restrict__ status, const Bounds bd, uint64_t limit_ns)
 {
     using Sh = SplitShape<NT, BM>;
     const int STAGE = atoms * Sh::ATOM;
@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles need 1 KB alignment
     uint8_t *smem = smem_raw + (base - raw);
+    if (!dbg_ok((base - raw) + split_smem_bytes(stages, STAGE) - 1024 - 1, bd.smem, status))
+        return;  // the ring, barriers, tags and TMEM slot must lie in the launch's shared memory
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * STAGE);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * stages;
@@ -334,14 +336,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (S == 1) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (c0 + j < B && mine)
+                        if (c0 + j < B && mine && dbg_ok((int64_t)(c0 + j) * N + n, bd.y, status))
                             y[(int64_t)(c0 + j) * N + n] = to_bf16(__uint_as_float(v[j]));
                     continue;
                 }
+                const int64_t tile_w = (int64_t)t * S * NT * BM + row;  // tile t's words start here
+                const int64_t own_w = tile_w + ((int64_t)piece * NT + c0) * BM;
                 unsigned long long *own = tile_x + ((int64_t)piece * NT + c0) * BM;
                 const int ncols = B - c0 < 16 ? B - c0 : 16;
                 if (piece != S - 1) {  // publish this piece
-                    if (has_row)
+                    if (has_row && dbg_range(own_w, 15 * BM + 1, bd.xch, status))
                         xch::publish16(own, BM, v, ncols);
                     continue;
                 }
@@ -349,14 +353,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;  // (lanes 16-31 of an M = 64 tile; the warp reconverges above)
                 // Reduce: pieces 0..S-2 in order, then this block's own piece.
                 float sum[16];
-                if (!xch::reduce16(tile_x + (int64_t)c0 * BM, (int64_t)NT * BM, BM, S - 1, ncols, v, own, sum,
-                                   limit_ns)) {
+                if (!dbg_range(tile_w + (int64_t)c0 * BM, (int64_t)(S - 1) * NT * BM + 15 * BM + 1, bd.xch, status)) {
+                    ok = false;
+                } else if (!xch::reduce16(tile_x + (int64_t)c0 * BM, (int64_t)NT * BM, BM, S - 1, ncols, v, own, sum,
+                                          limit_ns)) {
                     record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
                     ok = false;
                 }
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                    if (j < ncols && mine && ok)
+                    if (j < ncols && mine && ok && dbg_ok((int64_t)(c0 + j) * N + n, bd.y, status))
                         y[(int64_t)(c0 + j) * N + n] = to_bf16(sum[j]);
             }
             tc::fence_before();
@@ -424,7 +430,7 @@ cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
             return cudaErrorInvalidValue;
         e = launch(tc_split_kernel<NT, BM>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
                    a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, S, a.xch, dispenser,
-                   a.status, a.wait_limit_ns);
+                   a.status, a.bounds(rows, smem), a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }
@@ -475,7 +481,42 @@ DEP_TCS_DISPATCH(blocks_for, int, blocks_per_sm_shape, 0)
 DEP_TCS_DISPATCH(prepare_for, cudaError_t, prepare_shape, cudaErrorInvalidValue)
 #undef DEP_TCS_DISPATCH
 
+// Self-test of the exchange's give-up path, on a plan's own regions: one warp
+// publishes the words of pieces 1 and 3 of a 32-row, 16-column tile (as
+// publishers would), then reduces pieces 0 and 1 with the exchange's reducer;
+// piece 0 is never published, so the bounded wait gives up and the warp records
+// DEP_DEV_TIMEOUT_EPILOGUE.  Piece 3's "full" flags stay behind, and so does a
+// nonzero word at the start of the counters (where the split-K FMA kernel
+// counts arrivals and the wide-batch kernel keeps its flags): the state a real
+// give-up can leave a plan in.
+__global__ void selftest_exchange_kernel(unsigned long long *xch, int *counters, int *status, uint64_t limit_ns)
+{
+    const int lane = threadIdx.x & 31;
+    constexpr int64_t kCol = 32, kPiece = 16 * kCol;  // words [piece][column][row]
+    uint32_t v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        v[j] = __float_as_uint((float)(lane + j));
+    xch::publish16(xch + kPiece + lane, kCol, v, 16);      // piece 1 published
+    xch::publish16(xch + 3 * kPiece + lane, kCol, v, 16);  // piece 3: nobody reduces it
+    __syncwarp();
+    float out[16];
+    if (!xch::reduce16(xch + lane, kPiece, kCol, 2, 16, v, xch + 2 * kPiece + lane, out, limit_ns))
+        record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
+    if (lane == 0)
+        atomicExch(counters, 1);
+}
+
 }  // namespace
+
+cudaError_t tcs_selftest_exchange(unsigned long long *xch, size_t xch_words, int *counters, int *status,
+                                  uint64_t limit_ns, cudaStream_t stream)
+{
+    if (xch_words < 4 * 16 * 32)
+        return cudaErrorInvalidValue;
+    selftest_exchange_kernel<<<1, 32, 0, stream>>>(xch, counters, status, limit_ns);
+    return cudaGetLastError();
+}
 
 bool tcs_valid(const dep_tactic_t &t)
 {

@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_wide_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                    uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms,
                    float *__restrict__ ws, int *__restrict__ flags, int keep_own, int *__restrict__ status,
-                   uint64_t limit_ns)
+                   const Bounds bd, uint64_t limit_ns)
 {
     using S = WideShape<NT, G>;
     const int STAGE = atoms * S::ATOM;
@@ -175,6 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles need 1 KB alignment
     uint8_t *smem = smem_raw + (base - raw);
     const int RING = stages * STAGE;
+    if (!dbg_ok((base - raw) + (size_t)RING + (2 * (size_t)stages + 5 + kEpiWarps * kMaxStaging) * 8 + 8 - 1, bd.smem,
+                status))
+        return;  // the ring, the barriers and the TMEM slot must lie in the launch's shared memory
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)RING);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * stages;
@@ -406,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc::wait_ld();
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            if (b0 + c16 + j < B && n < N)
+                            if (b0 + c16 + j < B && n < N && dbg_ok((int64_t)(b0 + c16 + j) * N + n, bd.y, status))
                                 y[(int64_t)(b0 + c16 + j) * N + n] = to_bf16(__uint_as_float(v[j]));
                     }
                 }
@@ -426,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
                 for (int cb = 0; cb < S::NCB; ++cb) {
                     if (col_b0(cb) >= B || (cb >= my0 && cb < my1 && !keep_own))
+                        continue;
+                    if (!dbg_range((chunk(c, sl) - ws) + (size_t)cb * S::CB_FLOATS, S::CB_FLOATS, bd.ws, status))
                         continue;
                     float4 *dst = reinterpret_cast<float4 *>(chunk(c, sl) + (size_t)cb * S::CB_FLOATS);
 #pragma unroll 1
@@ -447,7 +452,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // starts at column block cb, unless that reducer is this block.
                 if (lane < S::NCB) {
                     const int64_t i = gs.reducer_index(lane, S::NCB);
-                    if (gs.cb_begin(i, S::NCB) == lane && gs.c_e + i != c) {
+                    if (gs.cb_begin(i, S::NCB) == lane && gs.c_e + i != c &&
+                        dbg_ok(flag(c, sl, lane) - flags, bd.counters, status)) {
                         __threadfence();
                         st_relaxed(flag(c, sl, lane), 1);
                     }
@@ -461,6 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (p == c)
                             continue;
                         const int *f = flag(p, slot_of(p, t, KTILES, U, C), my0);
+                        if (!dbg_ok(f - flags, bd.counters, status)) {
+                            ok = false;
+                            break;
+                        }
                         while (ld_acquire(f) == 0)
                             if (globaltimer_ns() - t0 > limit_ns) {
                                 record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
@@ -490,8 +500,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     auto issue = [&](int64_t i) {
                         const int sb = (int)(i % n_stg);
                         const uint32_t bar = stg0 + 8 * (e * kMaxStaging + sb);
+                        const float *src = copy_src(i);
                         mbar_arrive_expect_tx(bar, (uint32_t)stg_bytes);
-                        bulk_load(stg_base + (uint32_t)(sb * stg_bytes), copy_src(i), (uint32_t)stg_bytes, bar);
+                        if (dbg_range(src - ws, S::CB_FLOATS, bd.ws, status) &&
+                            dbg_range((stg_base - base) + (uint32_t)(sb * stg_bytes), stg_bytes, (uint32_t)RING, status))
+                            bulk_load(stg_base + (uint32_t)(sb * stg_bytes), src, (uint32_t)stg_bytes, bar);
                     };
                     int64_t issued = 0, used = 0;
                     if (ok && lane == 0) {
@@ -555,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             break;
 #pragma unroll
                         for (int j = 0; j < S::CBW; ++j)
-                            if (b0 + j < B && n < N)
+                            if (b0 + j < B && n < N && dbg_ok((int64_t)(b0 + j) * N + n, bd.y, status))
                                 y[(int64_t)(b0 + j) * N + n] = to_bf16(sum[j]);
                     }
                     if (!ok && lane == 0) {
@@ -646,7 +659,7 @@ cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
             return cudaErrorInvalidValue;
         e = launch(tc_wide_kernel<NT, G>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
                    a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, a.ws, a.counters,
-                   a.keep_pieces ? 1 : 0, a.status, a.wait_limit_ns);
+                   a.keep_pieces ? 1 : 0, a.status, a.bounds(rows, smem), a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }

@@ -811,3 +811,44 @@ def test_tcs_batches_wider_than_the_mma(dep, orc, B, NT, splits, BM):
         assert dep.dep_projection_device_status(plan) == 0
     finally:
         dep.dep_projection_plan_destroy(plan)
+
+
+def test_exchange_give_up_is_reported_and_cleared(dep, orc):
+    """The split-K exchange's bounded wait, made to run out without faulting
+    anything: the self-test leaves published exchange words and a counter
+    behind and has the reducer wait for a piece nobody publishes.  The give-up
+    comes back as DEP_DEV_TIMEOUT_EPILOGUE; reading the status clears the
+    exchange region and the counters; afterwards the K-piece tensor-core
+    kernel, the split-K FMA kernel and the wide-batch stream-K kernel give the
+    bits of a fresh plan (a stale flag or counter would change them)."""
+    N, K, B = 7168, 4096, 16
+    x = synth.normal_bf16(51, 2, (B, K))
+    W = synth.normal_bf16(52, 1, (N, K), sigma=0.02)
+    sms = sm_count()
+    fma = fma_tactic(dep, 8, sms)
+    wide = dep.dep_tactic_t(max_rows=64, kind=dep.DEP_KIND_TC_WIDE, ctas=sms, tile_n=256, tile_k=64, stages=4,
+                            cols=64)
+
+    def all_runs(plan):
+        return [run(dep, plan, x, W, N), run(dep, plan, x, W, N, fma), run(dep, plan, x, W, N, wide)]
+
+    fresh = dep.dep_projection_plan(N, K, [B])
+    plan = dep.dep_projection_plan(N, K, [B])
+    try:
+        dep.dep_projection_plan_set(fresh, wide)
+        dep.dep_projection_plan_set(plan, wide)
+        assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC_SPLIT
+        want = all_runs(fresh)
+        assert dep.dep_projection_device_status(fresh) == 0
+        ok, worst, idx = within_tolerance(want[0], orc.linear(x, W))
+        assert ok, (worst, idx)
+        dep.dep_projection_plan_selftest_exchange(plan, 2000)  # 2 ms limit
+        assert dep.dep_projection_device_status(plan) == dep.DEP_DEV_TIMEOUT_EPILOGUE
+        words = dep.dep_projection_plan_exchange(plan, 4 * 16 * 32)
+        assert not words.any()  # flags and values cleared
+        for got, ref in zip(all_runs(plan), want):
+            np.testing.assert_array_equal(got, ref)
+        assert dep.dep_projection_device_status(plan) == 0
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+        dep.dep_projection_plan_destroy(fresh)
