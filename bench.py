@@ -141,10 +141,14 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def read_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if taken on the
-    current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
+def read_traffic(kernel: str):
+    """DRAM bytes (read + written) per algorithmic byte of a kernel, from the
+    committed record of one ncu capture of it (profiles/traffic_<kernel>.txt),
+    and the capture it came from; None when there is no record or the record
+    was taken on other kernel sources.  A roofline's `traffic` is this ratio
+    times its bytes per launch: DRAM traffic grows in proportion to the weight
+    streamed, so a capture of one call scales to the family's launches."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}.txt")
     try:
         fields = dict(line.split(":", 1) for line in open(path) if ":" in line)
     except OSError:
@@ -152,7 +156,7 @@ def read_traffic(kernel: str, workload: str):
     if fields.get("source_sha", "").strip() != source_hash(kernel_family(kernel)):
         return None
     try:
-        return float(fields["dram_bytes_per_launch"])
+        return float(fields["dram_bytes_per_algorithmic_byte"]), fields.get("capture", "").strip()
     except (KeyError, ValueError):
         return None
 
@@ -509,8 +513,13 @@ def run_ours(args):
         launches = sum(-(-calls[i].B // tactics[i].cols) for i in idx) * args.steps
         achieved = nbytes / (family_ms[k] * 1e-3) / 1e9
         bracketed = nbytes / (float(call_ms[:, idx].sum()) * 1e-3) / 1e9
+        tr = read_traffic(k)
         r = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": UNIT, "frac": achieved / peak,
-             "traffic": read_traffic(k, args.workload), "kernel": k,
+             "traffic": tr[0] * nbytes / launches if tr else None,
+             "traffic_source": f"ncu dram__bytes_read.sum + dram__bytes_write.sum of {tr[1]}, as a ratio to "
+                               f"that call's algorithmic bytes ({tr[0]:.4f}), times this family's bytes per "
+                               f"launch" if tr else "no ncu record on the current kernel sources",
+             "kernel": k,
              "peak_source": f"{peak_src} (HBM copy bandwidth, MEASURED_PEAKS.json)",
              "calls": [calls[i].name for i in idx],
              "bytes_per_launch": nbytes / launches, "us_per_launch": family_ms[k] * 1e3 / launches,
