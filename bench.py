@@ -375,7 +375,8 @@ def kernel_name(t) -> str:
     if t.kind == dep.DEP_KIND_TC_WIDE:
         return f"tc_wide_n{t.cols}_g{t.tile_n // 128}"
     if t.kind == dep.DEP_KIND_TC_CLUSTER:
-        return f"tc_cluster_n{t.cols}_g{t.tile_n // 128}_k{t.splits}"
+        g = "1.5" if t.tile_n == 192 else str(t.tile_n // 128)  # 192 rows: a 128-row and a 64-row tile
+        return f"tc_cluster_n{t.cols}_g{g}_k{t.splits}"
     return f"tc_gemm_n{t.cols}"
 
 

@@ -81,9 +81,11 @@ typedef enum {
                                  that share them, each a part of the columns, adding
                                  the blocks' FP32 partials in block order */
 #define DEP_KIND_TC_CLUSTER 6 /* tcgen05 MMA for wide batches: a thread-block cluster
-                                 of `splits` = k CTAs per group of tile_n / 128 = 2 or
-                                 4 weight tiles (one MMA per tile, the same x
-                                 operand), CTA rank r streaming K piece r; the K
+                                 of `splits` = k CTAs per group of weight tiles --
+                                 tile_n = 256 or 512 rows (2 or 4 tiles of 128), or
+                                 192 rows (a 128-row and a 64-row tile) -- one MMA
+                                 per tile with the same x operand, CTA rank r
+                                 streaming K piece r; the K
                                  pieces are added in rank order through distributed
                                  shared memory (no global workspace); `stages` =
                                  weight stages (x has its own 2-4 stage ring);
@@ -96,7 +98,8 @@ typedef struct {
     int32_t ctas;     /* persistent blocks launched (FMA/TC/TC_WIDE: work split
                          evenly, stream-K; ROWS/TC_SPLIT: work items taken
                          dynamically) */
-    int32_t tile_n;   /* weight rows per tile (TC_WIDE: per group, 256 or 512) */
+    int32_t tile_n;   /* weight rows per tile (TC_WIDE: per group, 256 or 512;
+                         TC_CLUSTER: per group, 192, 256 or 512) */
     int32_t tile_k;   /* reduction columns per pipeline stage */
     int32_t stages;   /* pipeline depth (shared-memory stages) */
     int32_t cols;     /* batch rows per pass (FMA/ROWS: x rows held; TC: MMA N) */

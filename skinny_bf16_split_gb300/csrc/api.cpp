@@ -270,8 +270,17 @@ dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
     // kernel; o_proj 7168 x 12288 B = 64..256 (k = 4): 37.2 / 41.0 / 49.9 us; KDA
     // 49376 x 7168 B = 128 (four-tile groups) / 256 (k = 2): 119.6 / 152.6 us.
     if (cols >= 64) {
-        const int64_t t2 = (N + 255) / 256, t4 = (N + 511) / 512;
+        const int64_t t2 = (N + 255) / 256, t3 = (N + 191) / 192, t4 = (N + 511) / 512;
         const int32_t sw = cols == 256 ? 4 : (cols == 128 ? 6 : 5);
+        if (cols == 256 && 2 * t3 <= sm_count && 8 * t3 > 3 * (int64_t)sm_count) {
+            // 256 rows: groups of 192 rows (a 128-row and a 64-row tile) in clusters
+            // of two where those nearly fill the SMs (DSA: 76 groups, 152 CTAs;
+            // 49.4 us against 50.6 us for 57 groups of two tiles on 114 CTAs)
+            dep_tactic_t t = cluster_tactic(rows, cols, 2, 2, 5, (int32_t)t3 * 2);
+            t.tile_n = 192;
+            if (dep::cluster_valid(t))
+                return t;
+        }
         if (2 * t2 <= sm_count) {
             const int32_t k = (int32_t)std::min<int64_t>(4, sm_count / t2);
             const dep_tactic_t t = cluster_tactic(rows, cols, 2, k, sw, (int32_t)t2 * k);
@@ -589,17 +598,20 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
                 for (int32_t st : {2, 3, 4, 5, 6})
                     if (cols * g <= 512)
                         c.push_back(wide_tactic(rows, cols, g, st, sm_count, tk));
-    // A cluster of k CTAs per group of 2 or 4 tiles: k = 1..4, as many clusters
-    // as groups (at most one wave of the SMs).
+    // A cluster of k CTAs per group of 2 or 4 tiles (or a 128-row and a 64-row
+    // tile, 192 rows): k = 1..4, as many clusters as groups (at most one wave of
+    // the SMs).
     if (cols >= 32)
-        for (int32_t g : {2, 4})
+        for (int32_t grows : {256, 192, 512})
             for (int32_t k : {1, 2, 3, 4})
                 for (int32_t st : {3, 4, 5, 6}) {
-                    if (cols * g > 512)
+                    if (cols * (grows == 192 ? 2 : grows / 128) > 512 || (grows == 192 && cols < 64))
                         continue;
-                    const int64_t groups = (N + 128 * g - 1) / (128 * g);
+                    const int64_t groups = (N + grows - 1) / grows;
                     const int32_t clusters = (int32_t)std::max<int64_t>(1, std::min<int64_t>(groups, sm_count / k));
-                    c.push_back(cluster_tactic(rows, cols, g, k, st, clusters * k));
+                    dep_tactic_t t = cluster_tactic(rows, cols, 2, k, st, clusters * k);
+                    t.tile_n = grows;
+                    c.push_back(t);
                 }
     // K pieces keep every piece's partial: leave out tactics whose exchange words
     // would take more than 64 MB.

@@ -17,10 +17,13 @@
 // Design (sm_103a, one CTA per SM, clusters of k CTAs, no multicast):
 //  * Cluster j takes groups j, j + C, j + 2C, ... (C clusters); CTA rank r of a
 //    cluster streams K piece r (64-column k-tiles [r KT / k, (r+1) KT / k)) of
-//    the group: G weight boxes [128 x 64] per k-tile against one x box
-//    [NT x 64], one M = 128 MMA per tile with the same x descriptor (swap-AB;
-//    MMA N = the batch padded to NT).  The group's accumulator is G x NT TMEM
-//    columns (tile g at column g NT), two buffers where they fit.
+//    the group: a weight box [tile rows x 64] per tile and k-tile against one
+//    x box [NT x 64], one MMA per tile with the same x descriptor (swap-AB; MMA
+//    N = the batch padded to NT).  A group is 2 or 4 tiles of 128 rows (MMA
+//    M = 128), or one of 128 and one of 64 rows (M = 64; 192 rows, so that
+//    the groups of a 14560-row weight fill 152 SMs in clusters of two).  The
+//    group's accumulator is one NT-column TMEM block per tile (tile g at
+//    column g NT), two buffers where they fit.
 //  * The weight and x have rings of their own, each filled by its own producer
 //    warp: the weight ring is as deep as shared memory allows (its latency is
 //    HBM's), the x ring only a few stages (x is read from L2).
@@ -57,19 +60,27 @@ constexpr int kColBlocks = 8;   // column blocks per warp chunk (at most)
 constexpr int kMaxCluster = 8;  // portable cluster size
 constexpr int kMaxXStages = 4;
 
+// G = 2 or 4: that many 128-row tiles per group.  G = 3 stands for one and a
+// half: a 128-row tile and a 64-row tile (MMA M = 64), 192 rows per group.
 template <int NT, int G>
 struct ClusterShape {
-    static constexpr int ROWS = G * kBM;               // weight rows per group
-    static constexpr int ACC = G * NT;                 // TMEM columns of one accumulator
+    static constexpr int TILES = G == 3 ? 2 : G;       // MMA tiles per group
+    static constexpr int ROWS = G == 3 ? 192 : G * kBM;  // weight rows per group
+    static constexpr int ACC = TILES * NT;             // TMEM columns of one accumulator
     static constexpr int BUFS = 2 * ACC <= 512 ? 2 : 1;
     static constexpr uint32_t TMEM_COLS = BUFS * ACC;  // a power of two >= 64
     static constexpr int HALF = ACC / 2;               // accumulator columns per epilogue warp
     static constexpr int CBW = HALF / kColBlocks >= 16 ? HALF / kColBlocks : 16;  // columns per block
     static constexpr int NCB = HALF / CBW;             // column blocks per warp chunk
     static constexpr int CB_BYTES = 32 * CBW * 4;      // one column block of a warp chunk (FP32)
-    static constexpr int W_STAGE = G * kWBytes;
+    static constexpr int W_STAGE = G == 3 ? kWBytes + kWBytes / 2 : G * kWBytes;
     static constexpr int X_STAGE = NT * kBK * 2;
-    static_assert(ACC <= 512 && NT >= 32 && NT <= 256 && (G == 2 || G == 4), "shape");
+    // weight rows a column block of the eight warp chunks covers (G = 3: the
+    // 64-row tile has 16 rows per TMEM lane quadrant)
+    static constexpr int CB_ROWS = G == 3 ? 192 : 256;
+    // rows of tile g, and whether TMEM lane `lane` of a quadrant holds one of them
+    __host__ __device__ static constexpr int tile_rows(int g) { return G == 3 && g == 1 ? 64 : kBM; }
+    static_assert(ACC <= 512 && NT >= 32 && NT <= 256 && (G == 2 || G == 3 || G == 4), "shape");
     static_assert(CBW % 16 == 0 && NT % CBW == 0 && NCB <= kColBlocks, "column blocks");
 };
 
@@ -211,8 +222,9 @@ __device__ __forceinline__ void cluster_sync()
 
 template <int NT, int G>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_cluster_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                      const __grid_constant__ CUtensorMap tmY, uint16_t *__restrict__ y, int B, int N, int K,
+    tc_cluster_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmW64,
+                      const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmY,
+                      const __grid_constant__ CUtensorMap tmY64, uint16_t *__restrict__ y, int B, int N, int K,
                       int SW, int SX, int use_tma_y, int *__restrict__ status, const Bounds bd, uint64_t limit_ns)
 {
     using S = ClusterShape<NT, G>;
@@ -305,9 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(wfull0 + 8 * s, (uint32_t)S::W_STAGE);
-                    for (int g = 0; g < G; ++g)
-                        tma_load_2d(base + (uint32_t)(s * S::W_STAGE + g * kWBytes), &tmW, kt * kBK,
-                                    (int)(t * S::ROWS) + g * kBM, wfull0 + 8 * s, pol);
+                    for (int g = 0; g < S::TILES; ++g)
+                        tma_load_2d(base + (uint32_t)(s * S::W_STAGE + g * kWBytes), S::tile_rows(g) == kBM ? &tmW : &tmW64,
+                                    kt * kBK, (int)(t * S::ROWS) + g * kBM, wfull0 + 8 * s, pol);
                     ++issued;
                     if (++s == SW) {
                         s = 0;
@@ -373,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, NT);
+            constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, NT), idesc64 = tc::idesc_bf16_f32(64, NT);
             int sw = 0, sx = 0, buf = 0;
             uint32_t phw = 0, phx = 0, acce_ph = 0;
             bool ok = true;
@@ -404,9 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t off = (uint64_t)((j * kUmmaK * 2) >> 4);
                         const uint32_t acc = (kt != kt0 || j > 0) ? 1u : 0u;
 #pragma unroll
-                        for (int g = 0; g < G; ++g)
+                        for (int g = 0; g < S::TILES; ++g)
                             tc::mma_bf16(d + (uint32_t)(g * NT), tc::desc_sw128(wa + (uint32_t)(g * kWBytes)) + off,
-                                         bd + off, idesc, acc);
+                                         bd + off, S::tile_rows(g) == kBM ? idesc : idesc64, acc);
                     }
                     tc::commit(wempty0 + 8 * sw);  // the stages are free once these MMAs finish
                     tc::commit(xempty0 + 8 * sx);
@@ -435,12 +447,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e = warp - 2;         // chunk index within a piece
         const int q = warp & 3;         // TMEM lane quadrant this warp may access
         const int h = e >> 2;           // accumulator column half
-        const int row = 32 * q + lane;  // row within a tile
         const int ms = max_share(S::NCB, k);
         // Column block cb of this warp: accumulator columns h HALF + cb CBW ..,
         // tile col / NT, batch rows from col % NT.
         auto col_tile = [&](int cb) { return (h * S::HALF + cb * S::CBW) / NT; };
         auto col_b0 = [&](int cb) { return (h * S::HALF + cb * S::CBW) % NT; };
+        // The weight row of this lane in tile g, and whether the lane holds one: a
+        // 128-row tile has row 32 q + lane in TMEM lane quadrant q; the 64-row
+        // (M = 64) tile has rows 16 q .. 16 q + 15 in lanes 0-15 of quadrant q.
+        auto tile_row = [&](int g) { return S::tile_rows(g) == kBM ? 32 * q + lane : 16 * q + lane; };
+        auto lane_has_row = [&](int g) { return S::tile_rows(g) == kBM || lane < 16; };
         // Where sender `from` puts column block cb (of a share starting at cb0)
         // in the receiving CTA: [sender slot][warp][block of the share][lane][CBW].
         auto recv_off = [&](int from, int to, int cb, int cb0) -> uint32_t {
@@ -474,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) {
                         uint32_t nb = 0;
                         for (int cb = share_begin(rank, S::NCB, k); cb < share_begin(rank + 1, S::NCB, k); ++cb)
-                            nb += col_b0(cb) < B ? (uint32_t)(kEpiWarps * S::CB_BYTES) : 0u;
+                            nb += col_b0(cb) < B ? (uint32_t)(S::CB_ROWS * S::CBW * 4) : 0u;
                         mbar_arrive_expect_tx(rx_full, nb * (uint32_t)(k - 1));
                     }
                     __syncwarp();
@@ -498,17 +514,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (col_b0(cb) >= B || !dbg_range(recv_off(rank, p, cb, c0), S::CB_BYTES, (unsigned)RING, status))
                             continue;
                         const uint32_t dst = peer_addr(base + recv_off(rank, p, cb, c0), (uint32_t)p);
+                        const bool has = lane_has_row(col_tile(cb));  // lanes without a row send nothing
 #pragma unroll 1
                         for (int c16 = 0; c16 < S::CBW; c16 += 16) {
                             __syncwarp();  // tcgen05.ld is warp-collective: every lane, converged
                             uint32_t v[16];
                             tc::ld16(tq + (uint32_t)(cb * S::CBW + c16), v);
                             tc::wait_ld();
+                            if (has) {
 #pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                st_async_peer_v4(dst + (uint32_t)(((c16 / 4 + i) * 32 + lane) * 16),
-                                                 __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]), pbar);
+                                for (int i = 0; i < 4; ++i)
+                                    st_async_peer_v4(dst + (uint32_t)(((c16 / 4 + i) * 32 + lane) * 16),
+                                                     __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]),
+                                                     pbar);
+                            }
                         }
                     }
                 }
@@ -526,8 +546,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int b0 = col_b0(cb);  // the same for every epilogue warp
                 if (b0 >= B)
                     continue;
-                const int64_t n = t * S::ROWS + (int64_t)col_tile(cb) * kBM + row;
-                // y staging buffer of this column block: [h][batch row j][128 rows]
+                const int g = col_tile(cb);
+                const bool has = lane_has_row(g);
+                const int rt = tile_row(g), pitch = S::tile_rows(g);
+                const int64_t n = t * S::ROWS + (int64_t)g * kBM + rt;
+                // y staging buffer of this column block: [h][batch row j][tile rows]
                 uint16_t *sy = reinterpret_cast<uint16_t *>(smem + (stg - base) +
                                                             (size_t)(stg_i & 1) * (stage_bytes(S::CBW) / 2));
                 if (use_tma_y) {
@@ -570,10 +593,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             sum[j] = p == 0 ? v[j] : sum[j] + v[j];
                     }
                     if (use_tma_y) {
+                        if (has) {
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            sy[((size_t)h * S::CBW + c16 + j) * kBM + 32 * q + lane] = to_bf16(sum[j]);
-                    } else {
+                            for (int j = 0; j < 16; ++j)
+                                sy[(size_t)h * S::CBW * kBM + (size_t)(c16 + j) * pitch + rt] = to_bf16(sum[j]);
+                        }
+                    } else if (has) {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             if (b0 + c16 + j < B && n < N && dbg_ok((int64_t)(b0 + c16 + j) * N + n, bd.y, status))
@@ -584,11 +609,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_proxy_async_smem();
                     epi_sync();
                     if (elected) {
-                        // two boxes [CBW batch rows x 128 weight rows], one per column half;
+                        // two boxes [CBW batch rows x tile rows], one per column half;
                         // rows past N and batch rows past B are clipped by the store
-                        for (int hh = 0; hh < 2; ++hh)
-                            tma_store_2d(&tmY, smem_u32(sy) + (uint32_t)(hh * S::CBW * kBM * 2),
-                                         (int)(t * S::ROWS) + ((hh * S::HALF + cb * S::CBW) / NT) * kBM, b0);
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int gg = (hh * S::HALF + cb * S::CBW) / NT;
+                            tma_store_2d(S::tile_rows(gg) == kBM ? &tmY : &tmY64,
+                                         smem_u32(sy) + (uint32_t)(hh * S::CBW * kBM * 2), (int)(t * S::ROWS) + gg * kBM,
+                                         b0);
+                        }
                         bulk_commit();
                     }
                     ++stg_i;
@@ -677,9 +705,10 @@ cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
     cudaError_t e = prepare<NT, G>();
     if (e != cudaSuccess)
         return e;
-    CUtensorMap tmW, tmX, tmY;
+    CUtensorMap tmW, tmW64, tmX, tmY, tmY64;
     if (encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B) !=
-        CUDA_SUCCESS)
+            CUDA_SUCCESS ||
+        encode_bf16_2d(&tmW64, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, 64, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     // y goes out in bulk tensor stores when its rows are 16-byte multiples (a
     // tensor map's row pitch must be), else by plain stores.
@@ -697,10 +726,12 @@ cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
             return cudaErrorInvalidValue;
         if (tma_y) {
             if (encode_bf16_2d(&tmY, a.y + (size_t)r0 * a.N, (uint64_t)a.N, (uint64_t)rows, kBM, S::CBW,
+                               CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS ||
+                encode_bf16_2d(&tmY64, a.y + (size_t)r0 * a.N, (uint64_t)a.N, (uint64_t)rows, 64, S::CBW,
                                CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
                 return cudaErrorInvalidValue;
         } else {
-            tmY = tmX;  // not used
+            tmY = tmY64 = tmX;  // not used
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(clusters * k));
@@ -716,7 +747,8 @@ cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
         attr[1].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        e = cudaLaunchKernelEx(&cfg, tc_cluster_kernel<NT, G>, tmW, tmX, tmY, a.y + (size_t)r0 * a.N, (int)rows,
+        e = cudaLaunchKernelEx(&cfg, tc_cluster_kernel<NT, G>, tmW, tmW64, tmX, tmY, tmY64, a.y + (size_t)r0 * a.N,
+                               (int)rows,
                                (int)a.N, (int)a.K, (int)t.stages, sx, tma_y ? 1 : 0, a.status, a.bounds(rows, smem),
                                a.wait_limit_ns);
         if (e != cudaSuccess)
@@ -731,17 +763,19 @@ cudaError_t prepare_shape(const dep_tactic_t &)
     return prepare<NT, G>();
 }
 
-#define DEP_CLUSTER_DISPATCH(NAME, RET, FN, BAD)                                \
-    RET NAME(const dep_tactic_t &t)                                             \
-    {                                                                           \
-        const int g = t.tile_n / kBM;                                           \
-        switch (t.cols) {                                                       \
-        case 32: return g == 4 ? FN<32, 4>(t) : g == 2 ? FN<32, 2>(t) : BAD;    \
-        case 64: return g == 4 ? FN<64, 4>(t) : g == 2 ? FN<64, 2>(t) : BAD;    \
-        case 128: return g == 4 ? FN<128, 4>(t) : g == 2 ? FN<128, 2>(t) : BAD; \
-        case 256: return g == 2 ? FN<256, 2>(t) : BAD;                          \
-        default: return BAD;                                                    \
-        }                                                                       \
+// The instantiation of a tactic: MMA width (cols) x group (tile_n = 256, 192 or
+// 512 weight rows: G = 2, 3 (a 128-row and a 64-row tile) or 4).
+#define DEP_CLUSTER_DISPATCH(NAME, RET, FN, BAD)                                             \
+    RET NAME(const dep_tactic_t &t)                                                          \
+    {                                                                                        \
+        const int g = t.tile_n == 192 ? 3 : t.tile_n / kBM;                                  \
+        switch (t.cols) {                                                                    \
+        case 32: return g == 4 ? FN<32, 4>(t) : g == 2 ? FN<32, 2>(t) : BAD;                 \
+        case 64: return g == 4 ? FN<64, 4>(t) : g == 3 ? FN<64, 3>(t) : g == 2 ? FN<64, 2>(t) : BAD;     \
+        case 128: return g == 4 ? FN<128, 4>(t) : g == 3 ? FN<128, 3>(t) : g == 2 ? FN<128, 2>(t) : BAD; \
+        case 256: return g == 3 ? FN<256, 3>(t) : g == 2 ? FN<256, 2>(t) : BAD;             \
+        default: return BAD;                                                                 \
+        }                                                                                    \
     }
 
 DEP_CLUSTER_DISPATCH(valid_for, bool, valid_shape, false)
@@ -752,7 +786,8 @@ DEP_CLUSTER_DISPATCH(prepare_for, cudaError_t, prepare_shape, cudaErrorInvalidVa
 
 bool cluster_valid(const dep_tactic_t &t)
 {
-    if (t.kind != DEP_KIND_TC_CLUSTER || t.tile_k != kBK || (t.tile_n != 2 * kBM && t.tile_n != 4 * kBM))
+    if (t.kind != DEP_KIND_TC_CLUSTER || t.tile_k != kBK ||
+        (t.tile_n != 2 * kBM && t.tile_n != 4 * kBM && t.tile_n != 192))
         return false;
     if (t.splits < 1 || t.splits > kMaxCluster || t.ctas < t.splits || t.ctas % t.splits)
         return false;  // whole clusters of 1..8 CTAs
@@ -764,12 +799,12 @@ bool cluster_valid(const dep_tactic_t &t)
 cudaError_t cluster_prepare_device()
 {
     for (int32_t cols : {32, 64, 128, 256})
-        for (int32_t g : {2, 4}) {
-            if (cols * g > 512)
+        for (int32_t rows : {256, 192, 512}) {
+            if (cols * (rows == 192 ? 2 : rows / kBM) > 512 || (rows == 192 && cols == 32))
                 continue;
             dep_tactic_t t{};
             t.cols = cols;
-            t.tile_n = g * kBM;
+            t.tile_n = rows;
             const cudaError_t e = prepare_for(t);
             if (e != cudaSuccess)
                 return e;
@@ -779,12 +814,12 @@ cudaError_t cluster_prepare_device()
 
 cudaError_t cluster_run(const dep_tactic_t &t, const RunArgs &a)
 {
-    const int g = t.tile_n / kBM;
+    const int g = t.tile_n == 192 ? 3 : t.tile_n / kBM;
     switch (t.cols) {
     case 32: return g == 4 ? run_shape<32, 4>(t, a) : run_shape<32, 2>(t, a);
-    case 64: return g == 4 ? run_shape<64, 4>(t, a) : run_shape<64, 2>(t, a);
-    case 128: return g == 4 ? run_shape<128, 4>(t, a) : run_shape<128, 2>(t, a);
-    case 256: return run_shape<256, 2>(t, a);
+    case 64: return g == 4 ? run_shape<64, 4>(t, a) : g == 3 ? run_shape<64, 3>(t, a) : run_shape<64, 2>(t, a);
+    case 128: return g == 4 ? run_shape<128, 4>(t, a) : g == 3 ? run_shape<128, 3>(t, a) : run_shape<128, 2>(t, a);
+    case 256: return g == 3 ? run_shape<256, 3>(t, a) : run_shape<256, 2>(t, a);
     default: return cudaErrorInvalidValue;
     }
 }

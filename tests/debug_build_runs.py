@@ -47,6 +47,8 @@ def main():
                             cols=128, splits=2)),
             ("cluster-3", T(max_rows=256, kind=dep.DEP_KIND_TC_CLUSTER, ctas=3 * g2, tile_n=256, tile_k=64,
                             stages=4, cols=256, splits=3)),
+            ("cluster-192", T(max_rows=512, kind=dep.DEP_KIND_TC_CLUSTER, ctas=2 * -(-N // 192), tile_n=192,
+                              tile_k=64, stages=5, cols=256, splits=2)),
         ]
 
     for N, K, B in [(333, 1000, 5), (97, 264, 33), (1000, 3000, 100), (1024, 2048, 255)]:

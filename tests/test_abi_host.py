@@ -85,9 +85,12 @@ def test_default_batches_when_none_given(dep):
         # 114 tiles of 128 rows nearly fill 152 SMs: whole tiles, one per block
         assert all((t.kind, t.splits) == (dep.DEP_KIND_TC_SPLIT, 1) for t in table if 2 < t.max_rows <= 16)
         assert all((t.kind, t.ctas) == (dep.DEP_KIND_TC, 114) for t in table if t.max_rows == 32)
-        # 64 rows and more: 57 groups of two tiles, a cluster of two CTAs each
-        wide = [t for t in table if t.max_rows >= 64]
+        # 64 and 128 rows: 57 groups of two tiles, a cluster of two CTAs each; 256
+        # rows: 76 groups of 192 rows (a 128-row and a 64-row tile), 152 CTAs
+        wide = [t for t in table if 64 <= t.max_rows <= 128]
         assert all((t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, 256, 2, 114) for t in wide)
+        t = table[-1]
+        assert (t.max_rows, t.kind, t.tile_n, t.splits, t.ctas) == (256, dep.DEP_KIND_TC_CLUSTER, 192, 2, 152)
     finally:
         dep.dep_projection_plan_destroy(plan)
 
@@ -109,6 +112,9 @@ def test_default_rule_wide_batches(dep, N, sms, expect):
         if expect is not None:
             for b in (64, 128, 256):
                 t = table[b]
+                if b == 256 and N == 14560:  # 76 groups of 192 rows fill the SMs
+                    assert (t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, 192, 2, 152), t
+                    continue
                 assert (t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, *expect), (b, t)
         else:
             assert (table[256].kind, table[256].splits, table[256].ctas) == (dep.DEP_KIND_TC_CLUSTER, 2, 152)

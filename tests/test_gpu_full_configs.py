@@ -55,7 +55,7 @@ def weights():
     return get
 
 
-@pytest.mark.parametrize("workload", list(synth.WORKLOADS))
+@pytest.mark.parametrize("workload", [w for w in synth.WORKLOADS if w != "baseline"])  # its parts, one by one
 def test_workload_full_size(dep, orc, weights, workload):
     calls = synth.workload(workload)
     batches = {}
@@ -91,3 +91,30 @@ def test_workload_full_size(dep, orc, weights, workload):
     finally:
         for p in plans.values():
             dep.dep_projection_plan_destroy(p)
+
+
+@pytest.mark.slow
+def test_dsa_b1_every_output_against_the_oracle(dep, orc):
+    """DSA packed input projection at B = 1 (x with unit-RMS rows), the benchmark's
+    first configuration at full size: all 14,560 outputs of the default plan's
+    call against the exact oracle's, element by element (about half a minute of
+    oracle work on the host's cores), and run to run bit for bit."""
+    c = synth.workload("dsa_b1")[0]
+    W, x = c.weight(), c.activations()
+    plan = dep.dep_projection_plan(c.N, c.K, [1])
+    try:
+        Wd, xd = to_dev(W), to_dev(x)
+        y1, y2 = empty_out(1, c.N), empty_out(1, c.N)
+        dep.dep_projection_run(plan, xd, Wd, y1, 1)
+        dep.dep_projection_run(plan, xd, Wd, y2, 1)
+        torch.cuda.synchronize()
+        assert dep.dep_projection_device_status(plan) == 0
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+    got = to_host(y1)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    ref = orc.linear(x, W)
+    ok, worst, idx = within_tolerance(got, ref)
+    assert ok, (worst, idx)
+    # the default tactic at one row is the whole-row kernel, whose order the FP32 mirror restates
+    np.testing.assert_array_equal(got, orc.mirror_fma(x, W, 1, 64))

@@ -229,9 +229,10 @@ def test_wide_determinism_and_graph_replay(dep, NT, G, B):
 def cluster_stages(NT, G, k, want=5):
     """Deepest weight ring (at most `want`) that fits with two or more x stages
     and holds the peers' partials and the y staging once idle (the kernel's own
-    rule)."""
-    ws, xs = G * 16384, NT * 128
-    half = G * NT // 2
+    rule).  G = 3 stands for a 128-row and a 64-row tile (192 rows)."""
+    tiles = 2 if G == 3 else G
+    ws, xs = (24576 if G == 3 else G * 16384), NT * 128
+    half = tiles * NT // 2
     cbw = max(16, half // 8)
     ncb = half // cbw
     recv = (k - 1) * 8 * -(-ncb // k) * 32 * cbw * 4
@@ -247,18 +248,26 @@ def cluster_stages(NT, G, k, want=5):
 
 def cluster_tactic(dep, NT, G, k, clusters, stages, max_rows=None):
     return dep.dep_tactic_t(max_rows=max_rows or NT, kind=dep.DEP_KIND_TC_CLUSTER, ctas=clusters * k,
-                            tile_n=128 * G, tile_k=64, stages=stages, cols=NT, splits=k)
+                            tile_n=192 if G == 3 else 128 * G, tile_k=64, stages=stages, cols=NT, splits=k)
+
+
+def group_rows(G):
+    return 192 if G == 3 else 128 * G
+
+
+CLUSTER_KINDS = KINDS + [(64, 3), (128, 3), (256, 3)]  # G = 3: a 128-row and a 64-row tile
 
 
 @pytest.mark.parametrize("N,K", [(256, 64), (333, 1000), (97, 264), (1000, 3000)])
-@pytest.mark.parametrize("NT,G", KINDS)
+@pytest.mark.parametrize("NT,G", CLUSTER_KINDS)
 def test_cluster_parity_vs_oracle(dep, orc, plans, N, K, NT, G):
-    """Every MMA width and group size; clusters of 1-4 CTAs (fewer where K has
-    fewer 64-column k-tiles); one cluster, 3 clusters and one per group (clusters
-    looping over several groups); partial, full and multi-pass batches."""
+    """Every MMA width and group size (two or four 128-row tiles, or a 128-row
+    and a 64-row tile); clusters of 1-4 CTAs (fewer where K has fewer 64-column
+    k-tiles); one cluster, 3 clusters and one per group (clusters looping over
+    several groups); partial, full and multi-pass batches."""
     plan = plans(N, K)
     W = synth.normal_bf16(N + NT + G + 7, 1, (N, K), sigma=0.02)
-    groups = -(-N // (128 * G))
+    groups = -(-N // group_rows(G))
     for B in sorted({min(NT, 5), NT - 3, NT, NT + 7}):
         x = synth.normal_bf16(B + NT + 1, 2, (B, K))
         ref = orc.linear(x, W)
@@ -312,9 +321,9 @@ def test_cluster_small_integers_exact_and_negation(dep, orc, plans):
     W = np.vectorize(exact_bf16)(rng.integers(-8, 9, (N, K))).astype(np.uint16)
     plan = plans(N, K)
     ref = orc.linear(x, W)
-    for NT, G in ((256, 2), (128, 4)):
+    for NT, G in ((256, 2), (128, 4), (256, 3)):
         for k in (1, 2, 3, 4):
-            t = cluster_tactic(dep, NT, G, k, -(-N // (128 * G)), cluster_stages(NT, G, k))
+            t = cluster_tactic(dep, NT, G, k, -(-N // group_rows(G)), cluster_stages(NT, G, k))
             np.testing.assert_array_equal(run(dep, plan, x, W, N, t), ref)
     xn = synth.normal_bf16(31, 2, (B, K))
     Wn = synth.normal_bf16(31, 1, (N, K), sigma=0.02)
@@ -325,14 +334,14 @@ def test_cluster_small_integers_exact_and_negation(dep, orc, plans):
     np.testing.assert_array_equal(yn[nz], y[nz] ^ np.uint16(0x8000))
 
 
-@pytest.mark.parametrize("NT,G,k,B", [(256, 2, 2, 256), (128, 2, 2, 128), (64, 4, 4, 64)])
+@pytest.mark.parametrize("NT,G,k,B", [(256, 2, 2, 256), (128, 2, 2, 128), (64, 4, 4, 64), (256, 3, 2, 256)])
 def test_cluster_determinism_and_graph_replay(dep, NT, G, k, B):
     """Repeated runs and CUDA-graph replays give identical bits; the bounded
     waits all complete (device status 0)."""
     N, K = 14560, 7168
     plan = dep.dep_projection_plan(N, K, [B])
     try:
-        T = -(-N // (128 * G))
+        T = -(-N // group_rows(G))
         dep.dep_projection_plan_set(plan, cluster_tactic(dep, NT, G, k, T, cluster_stages(NT, G, k), max_rows=B))
         x = to_dev(synth.normal_bf16(B, 2, (B, K)))
         W = to_dev(synth.normal_bf16(5, 1, (N, K), 0.02))
