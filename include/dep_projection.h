@@ -158,7 +158,10 @@ dep_status_t dep_projection_run(dep_plan_t plan, const void *x, const void *W, v
 /*
  * The same with an explicit tactic instead of the table's (tests and tuning).
  * Errors as dep_projection_run, plus INVALID_ARG for a tactic this build does
- * not implement or whose split-K workspace exceeds the plan's.
+ * not implement or whose split-K workspace exceeds the plan's, and UNSUPPORTED
+ * for a grid the device cannot hold at once in a kind whose blocks wait on one
+ * another (DEP_KIND_TC, DEP_KIND_TC_SPLIT, DEP_KIND_TC_WIDE: at most
+ * (blocks resident per SM) x (SM count) blocks).
  */
 dep_status_t dep_projection_run_tactic(dep_plan_t plan, const dep_tactic_t *tactic,
                                        const void *x, const void *W, void *y,
@@ -228,7 +231,8 @@ dep_status_t dep_projection_plan_table(dep_plan_t plan, dep_tactic_t *out, int32
                                        int32_t *n);
 
 /* Replace (or insert) the table entry with key tactic->max_rows.  The tactic is
- * validated (INVALID_ARG if not); if it needs more workspace, counters or
+ * validated (INVALID_ARG if not; UNSUPPORTED, as for dep_projection_run_tactic,
+ * for a grid the device cannot hold at once); if it needs more workspace, counters or
  * staging than the plan owns, the plan's device block is re-allocated (after a
  * device synchronisation; OOM leaves the plan unchanged). */
 dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic);
@@ -271,7 +275,7 @@ dep_status_t dep_projection_plan_workspace(dep_plan_t plan, size_t *bytes);
  * written in format 2 (eight fields per entry); format 1 files (seven fields,
  * no K pieces) still load.  Load checks the
  * shape (INVALID_ARG if it differs) and the SM count (UNSUPPORTED if the file
- * was made for another GPU).  Errors: IO for unreadable or malformed files.
+ * was made for another GPU, or holds a grid this device cannot hold at once).  Errors: IO for unreadable or malformed files.
  */
 dep_status_t dep_projection_plan_save(dep_plan_t plan, const char *path);
 dep_status_t dep_projection_plan_load(const char *path, int64_t N, int64_t K,

@@ -110,6 +110,32 @@ int64_t effective_ctas(const dep_tactic_t &t, int64_t N, int64_t K)
     return U < t.ctas ? U : t.ctas;
 }
 
+// Kinds whose blocks wait on one another (the stream-K fix-up, the K-piece
+// reducer, the wide reduce-scatter) need every block of a launch resident at
+// once: a block that waits on one still queued behind it would only give up.
+// False when the launch's grid exceeds the blocks the device holds together.
+bool grid_resident(const dep_tactic_t &t, int64_t N, int64_t K, int sm_count)
+{
+    int64_t grid = 0;
+    int per_sm = 0;
+    switch (t.kind) {
+    case DEP_KIND_TC:
+        grid = std::min<int64_t>(t.ctas, dep::tc_units(t, N, K));
+        per_sm = dep::tc_blocks_per_sm(t);
+        break;
+    case DEP_KIND_TC_SPLIT:
+        grid = std::min<int64_t>(t.ctas, dep::tcs_items(t, N, K));
+        per_sm = dep::tcs_blocks_per_sm(t);
+        break;
+    case DEP_KIND_TC_WIDE:
+        grid = std::min<int64_t>(t.ctas, dep::wide_units(t, N, K));
+        per_sm = dep::wide_blocks_per_sm(t);
+        break;
+    default: return true;  // no waits between blocks, or (clusters) waits only inside a co-scheduled cluster
+    }
+    return grid <= (int64_t)per_sm * sm_count;
+}
+
 // Split-K partial floats a launch of tactic t on an [N,K] weight may write.
 size_t tactic_ws_floats(const dep_tactic_t &t, int64_t N, int64_t K)
 {
@@ -789,6 +815,8 @@ dep_status_t dep_projection_run_tactic(dep_plan_t plan, const dep_tactic_t *tact
 {
     if (!tactic || !tactic_valid(*tactic))
         return DEP_ERR_INVALID_ARG;
+    if (plan && !plan->host_only && !grid_resident(*tactic, plan->N, plan->K, plan->sm_count))
+        return DEP_ERR_UNSUPPORTED;
     return run_impl(plan, tactic, x, W, y, B, stream);
 }
 
@@ -871,6 +899,8 @@ dep_status_t dep_projection_plan_set(dep_plan_t plan, const dep_tactic_t *tactic
 {
     if (!plan || !tactic || !tactic_valid(*tactic))
         return DEP_ERR_INVALID_ARG;
+    if (!plan->host_only && !grid_resident(*tactic, plan->N, plan->K, plan->sm_count))
+        return DEP_ERR_UNSUPPORTED;
     const std::vector<dep_tactic_t> old = plan->table;
     bool replaced = false;
     for (auto &t : plan->table)
@@ -993,7 +1023,10 @@ dep_status_t dep_projection_plan_load(const char *path, int64_t N, int64_t K, de
     dep_status_t st = make_plan(N, K, keys.data(), (int32_t)keys.size(), false, 0, &p);
     if (st != DEP_OK)
         return st;
-    if (p->sm_count != sms) {
+    bool resident = true;
+    for (const auto &t : table)
+        resident = resident && grid_resident(t, N, K, p->sm_count);
+    if (p->sm_count != sms || !resident) {
         dep_projection_plan_destroy(p);
         return DEP_ERR_UNSUPPORTED;
     }

@@ -66,6 +66,12 @@ cudaError_t set_smem_attr(Kernel kernel, std::atomic<uint64_t> &devices)
     if (bit && (devices.load(std::memory_order_acquire) & bit))
         return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynamicSmem);
+    // All of the unified L1 as shared memory: no kernel here reads through L1,
+    // and a block of the next grid in the stream (programmatic dependent launch)
+    // can then sit beside a running block whenever the two rings fit together.
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess && bit)
         devices.fetch_or(bit, std::memory_order_release);
     return e;
@@ -182,6 +188,7 @@ bool tcs_valid(const dep_tactic_t &t);
 size_t tcs_xch_words(const dep_tactic_t &t, int64_t N, int64_t K);  // every piece's exchange word
 size_t tcs_counters(const dep_tactic_t &t, int64_t N);               // the last 2 counters
 int tcs_blocks_per_sm(const dep_tactic_t &t);
+int64_t tcs_items(const dep_tactic_t &t, int64_t N, int64_t K);      // (tile, piece) items of a launch
 cudaError_t tcs_run(const dep_tactic_t &t, const RunArgs &a);       // uses the last 2 counters
 cudaError_t tcs_selftest_exchange(unsigned long long *xch, size_t xch_words, int *counters, int *status,
                                   uint64_t limit_ns, cudaStream_t stream);

@@ -228,6 +228,41 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Issue H consecutive 16-column K steps of one stage into accumulator d, fully
+// unrolled with constant descriptor offsets: step i reads slice i / 4 (A at
+// ad + i / 4 slices of A_BYTES, B likewise) at K offset 16 (i % 4) inside the
+// slice's 128-byte rows (2 descriptor units of 16 bytes per step).  ad and bd
+// are the descriptors of the first step.  One thread issues a tcgen05.mma only
+// every ~45 cycles at best, and address arithmetic between the instructions
+// adds to that, so the loop carries none.
+template <int H, int A_BYTES, int B_BYTES>
+__device__ __forceinline__ void mma_steps(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t &accumulate)
+{
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+        const uint64_t ka = (uint64_t)(((i / 4) * A_BYTES) >> 4) + 2 * (i % 4);
+        const uint64_t kb = (uint64_t)(((i / 4) * B_BYTES) >> 4) + 2 * (i % 4);
+        mma_bf16(d, ad + ka, bd + kb, idesc, accumulate);
+        accumulate = 1;
+    }
+}
+
+// The K steps [k0, k0 + n) of a stage whose slices start at a0 (A) and b0 (B),
+// n in {2, 4, 8, 16}; k0 % 4 == 0 unless n == 2 (then the steps stay in one slice).
+template <int A_BYTES, int B_BYTES>
+__device__ __forceinline__ void mma_stage(uint32_t d, uint32_t a0, uint32_t b0, int k0, int n, uint32_t idesc,
+                                          uint32_t &accumulate)
+{
+    const uint64_t ad = desc_sw128(a0 + (uint32_t)((k0 / 4) * A_BYTES)) + 2 * (k0 % 4);
+    const uint64_t bd = desc_sw128(b0 + (uint32_t)((k0 / 4) * B_BYTES)) + 2 * (k0 % 4);
+    switch (n) {
+    case 16: mma_steps<16, A_BYTES, B_BYTES>(d, ad, bd, idesc, accumulate); break;
+    case 8: mma_steps<8, A_BYTES, B_BYTES>(d, ad, bd, idesc, accumulate); break;
+    case 4: mma_steps<4, A_BYTES, B_BYTES>(d, ad, bd, idesc, accumulate); break;
+    default: mma_steps<2, A_BYTES, B_BYTES>(d, ad, bd, idesc, accumulate); break;
+    }
+}
+
 }  // namespace tc
 
 }  // namespace dep

@@ -15,10 +15,16 @@
 //  * Warp 0: TMA producer.  Per stage, tile_k / 64 weight slices [128 x 64] and
 //    activation slices [NT x 64] land in a shared-memory ring in the 128-byte
 //    swizzle layout (wider stages give each weight row longer contiguous reads).
-//  * Warp 1: allocates TMEM (two accumulators of NT columns), one thread issues
+//  * Warp 1: allocates TMEM (two accumulator buffers), one thread issues
 //    tcgen05.mma (4 per 64-column slice, K = 16 each) and releases each stage with
-//    tcgen05.commit; at the end of a segment it commits the accumulator.
-//  * Warps 2-5: epilogue.  Each owns the 32 TMEM lanes (= weight rows) of its
+//    tcgen05.commit; at the end of a segment it commits the accumulator.  One
+//    thread issues an MMA only about every 67 cycles, whatever its M and N (up
+//    to N = 128): too little work per instruction at N <= 32 to drain a full
+//    ring quickly.  There warp 2 issues too: issuer i takes a fixed half of
+//    every stage's K steps into its own accumulator, and the epilogue adds the
+//    two in issuer order (FP32, deterministic; the K-piece kernel uses the same
+//    rule, so the two kernels' sums of one tile agree bit for bit).
+//  * Warps 3-6: epilogue.  Each owns the 32 TMEM lanes (= weight rows) of its
 //    quadrant, reads its accumulator with tcgen05.ld, frees it for the MMA of
 //    the next-but-one segment, and either stores BF16 y (segment = whole tile)
 //    or exchanges FP32 partials for the split-K reduction through flagged
@@ -45,7 +51,7 @@ namespace {
 constexpr int kBM = 128;          // weight rows per tile (MMA M)
 constexpr int kBK = 64;           // columns per stage: one 128-byte swizzle row
 constexpr int kUmmaK = 16;        // K of one kind::f16 MMA
-constexpr int kThreads = 192;     // warp 0 TMA, warp 1 MMA/TMEM, warps 2-5 epilogue
+constexpr int kThreads = 224;     // warp 0 TMA, warps 1-2 MMA (warp 1 owns TMEM), warps 3-6 epilogue
 constexpr int kEpiWarps = 4;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB weight tile per stage
 
@@ -55,7 +61,8 @@ template <int NT>
 struct TcShape {
     static constexpr int B_BYTES = NT * kBK * 2;     // one activation slice (a multiple of 1024)
     static constexpr int ATOM = kABytes + B_BYTES;   // bytes per 64-column slice pair
-    static constexpr uint32_t TMEM_COLS = 2 * NT < 32 ? 32 : 2 * NT;
+    static constexpr int ISSUERS = NT <= 32 ? 2 : 1;  // MMA issuers, one accumulator each per buffer
+    static constexpr uint32_t TMEM_COLS = 2 * ISSUERS * NT < 32 ? 32 : 2 * ISSUERS * NT;
 };
 
 __device__ __forceinline__ uint16_t to_bf16(float v)
@@ -96,13 +103,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, S::ISSUERS);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(accf0 + 8 * b, S::ISSUERS);
             mbar_init(acce0 + 8 * b, kEpiWarps);
         }
-        mbar_init(done, 1);
+        mbar_init(done, S::ISSUERS);
         *abort_flag = 0;
         fence_mbar_init();
         griddep_launch_dependents();
@@ -183,10 +190,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     record_status(status, DEP_DEV_TIMEOUT_PRODUCER);
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+    } else if (warp == 1 || warp == 2) {
+        // ---------------- MMA issuers ----------------
+        // Issuer mi takes K steps [mi H, (mi + 1) H) of every stage (H = the
+        // stage's steps / issuers) into its own accumulator of each buffer.
+        const int mi = warp - 1;
+        if (lane == 0 && mi < S::ISSUERS) {
             constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, NT);
+            const int H = atoms * (kBK / kUmmaK) / S::ISSUERS;
             int s = 0;
             uint32_t ph = 0, acce_ph = 0;
             int buf = 0;
@@ -203,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 acce_ph ^= 1u << buf;
                 tc::fence_after();
-                const uint32_t d = tmem + (uint32_t)(buf * NT);
+                const uint32_t d = tmem + (uint32_t)((buf * S::ISSUERS + mi) * NT);
                 uint32_t accumulate = 0;
                 for (; u < seg_end; ++u) {
                     if (*abort_flag) {
@@ -218,18 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc::fence_after();
                     const uint32_t st = base + (uint32_t)(s * STAGE);
-                    for (int a = 0; a < atoms; ++a) {
-                        const uint64_t ad = tc::desc_sw128(st + (uint32_t)(a * kABytes));
-                        const uint64_t bd = tc::desc_sw128(st + (uint32_t)(atoms * kABytes + a * S::B_BYTES));
-#pragma unroll
-                        for (int j = 0; j < kBK / kUmmaK; ++j) {
-                            // advance along K inside the 128-byte swizzle row: 32 bytes per step
-                            const uint64_t off = (uint64_t)((j * kUmmaK * 2) >> 4);
-                            tc::mma_bf16(d, ad + off, bd + off, idesc, accumulate);
-                            accumulate = 1;
-                        }
-                    }
-                    tc::commit(empty0 + 8 * s);  // the stage is free once these MMAs finish
+                    tc::mma_stage<kABytes, S::B_BYTES>(d, st, st + (uint32_t)(atoms * kABytes), mi * H, H, idesc,
+                                                       accumulate);
+                    tc::commit(empty0 + 8 * s);  // the stage is free once every issuer's MMAs finish
                     if (++s == stages) {
                         s = 0;
                         ph ^= 1u;
@@ -237,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!ok)
                     break;
-                tc::commit(accf0 + 8 * buf);  // the accumulator is final
+                tc::commit(accf0 + 8 * buf);  // the accumulator is final once every issuer's MMAs finish
                 buf ^= 1;
             }
             tc::commit(done);  // TMEM is freed at the end: wait for every MMA
@@ -263,7 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             accf_ph ^= 1u << buf;
             tc::fence_after();
             const int64_t n = t * kBM + row;
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NT);
+            // buffer buf's accumulators: issuer 0's, then issuer 1's (NT columns each)
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * S::ISSUERS * NT);
             // Pieces of tile t: the segments of blocks c_first..c_last, in block order.
             // Exchange words: [block][slot][b][row]; slot 0 published, slot 1 own.
             const int64_t c_first = sk_owner(t * KTILES, U, C);
@@ -272,9 +275,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int c0 = 0; c0 < NT && c0 < B; c0 += 16) {
                 __syncwarp();  // tcgen05.ld is warp-collective: every lane, converged
-                uint32_t v[16];
+                uint32_t v[16], v1[16];
                 tc::ld16(taddr + (uint32_t)c0, v);
+                if (S::ISSUERS == 2)
+                    tc::ld16(taddr + (uint32_t)(NT + c0), v1);
                 tc::wait_ld();
+                if (S::ISSUERS == 2) {  // the block's partial: issuer 0's half of K, then issuer 1's
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+                }
                 const int ncols = B - c0 < 16 ? B - c0 : 16;
                 if (whole) {
 #pragma unroll

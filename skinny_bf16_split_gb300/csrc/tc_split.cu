@@ -15,9 +15,16 @@
 //    counter for the next launch.
 //  * Swap-AB MMAs as in the stream-K kernel: M = BM = 128 (or 64) weight rows,
 //    N = the batch padded to NT, K = 16 per instruction; 128-byte-swizzled TMA
-//    stages of tile_k / 64 slices; accumulators in TMEM, two buffers of NT
-//    columns.  The first stages are issued by thread 0 right after the barrier
-//    set-up, while warp 1 allocates TMEM.
+//    stages of tile_k / 64 slices; accumulators in TMEM, two buffers.  The first
+//    stages are issued by thread 0 right after the barrier set-up, while warp 1
+//    allocates TMEM.
+//  * One thread issues a tcgen05.mma about every 67 cycles whatever its M and
+//    N (up to N = 128), which at N <= 64 is less work per instruction than the
+//    tensor pipe can do: a block with one issuer consumes about 60 weight bytes
+//    per cycle, barely ahead of its share of HBM, and drains a prefetched ring
+//    slowly.  For NT <= 32 two warps issue: each takes a fixed half of every
+//    stage's 16-column K steps into its own accumulator, and the epilogue adds
+//    the two in issuer order (FP32), so the result stays deterministic.
 //  * Pieces are exchanged through the plan's exchange region, one 64-bit word
 //    per (tile, piece, b, row): the FP32 partial in the low half and a "full"
 //    flag in the high half, written by one single-copy-atomic store (no fence,
@@ -33,9 +40,10 @@
 //    held by a running block (or was run earlier by the same block), and the
 //    earliest pending reduction never waits on a later one.
 //  * Warp roles: warp 0 TMA producer (takes the items), warp 1 TMEM owner and
-//    MMA issuer, warps 2-5 epilogue.  The producer tags each stage with its item
-//    and first/last flags; the MMA issuer passes the item of each finished
-//    accumulator to the epilogue through a tag slot and its own mbarrier.
+//    MMA issuer 0, warp 2 MMA issuer 1 (NT <= 32), warps 3-6 epilogue.  The
+//    producer tags each stage with its item and first/last flags; issuer 0
+//    passes the item of each finished accumulator to the epilogue through a tag
+//    slot and its own mbarrier.
 //  * Every wait is bounded in time; on a give-up the block records a code, lets
 //    every role finish, waits for its MMAs and copies, and frees TMEM.
 #include <cuda_bf16.h>
@@ -49,7 +57,7 @@ namespace {
 
 constexpr int kBK = 64;       // columns per slice: one 128-byte swizzle row
 constexpr int kUmmaK = 16;    // K of one kind::f16 MMA
-constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA/TMEM, warps 2-5 epilogue
+constexpr int kThreads = 224; // warp 0 TMA, warps 1-2 MMA (warp 1 owns TMEM), warps 3-6 epilogue
 constexpr int kEpiWarps = 4;
 constexpr int kMaxSplits = 64;
 
@@ -59,7 +67,10 @@ struct SplitShape {
     static constexpr int A_BYTES = BM * kBK * 2;  // one weight slice: 8 or 16 KB
     static constexpr int B_BYTES = NT * kBK * 2;
     static constexpr int ATOM = A_BYTES + B_BYTES;
-    static constexpr uint32_t TMEM_COLS = 2 * NT < 32 ? 32 : 2 * NT;
+    // MMA issuers, each with its own accumulator per buffer: two at N <= 32,
+    // the same rule as the stream-K kernel, whose results these must equal.
+    static constexpr int ISSUERS = NT <= 32 ? 2 : 1;
+    static constexpr uint32_t TMEM_COLS = 2 * ISSUERS * NT < 32 ? 32 : 2 * ISSUERS * NT;
 };
 
 // Shared memory after the 1 KB-aligned ring: full[stages], empty[stages],
@@ -139,14 +150,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmX);
         for (int s = 0; s < stages; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, Sh::ISSUERS);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(accf0 + 8 * b, Sh::ISSUERS);
             mbar_init(acce0 + 8 * b, kEpiWarps);
             mbar_init(tagb0 + 8 * b, 1);
         }
-        mbar_init(done, 1);
+        mbar_init(done, Sh::ISSUERS);
         *abort_flag = 0;
         fence_mbar_init();
         griddep_launch_dependents();
@@ -232,10 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *finished = 0;
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
+    } else if (warp == 1 || warp == 2) {
+        // ---------------- MMA issuers ----------------
+        // Issuer mi takes K steps [mi H, (mi + 1) H) of every stage (H = the
+        // stage's steps / issuers) into its own accumulator of each buffer.
+        const int mi = warp - 1;
+        if (lane == 0 && mi < Sh::ISSUERS) {
             constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, NT);
+            const int H = atoms * (kBK / kUmmaK) / Sh::ISSUERS;
             int s = 0, buf = 0;
             uint32_t ph = 0, acce_ph = 0;
             uint32_t accumulate = 0;
@@ -259,33 +274,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::fence_after();
                     accumulate = 0;
                 }
-                if (tag.x < 0) {  // hand the end marker to the epilogue
-                    acc_item[buf] = -1;
-                    mbar_arrive(tagb0 + 8 * buf);
+                if (tag.x < 0) {  // issuer 0 hands the end marker to the epilogue
+                    if (mi == 0) {
+                        acc_item[buf] = -1;
+                        mbar_arrive(tagb0 + 8 * buf);
+                    }
                     break;
                 }
-                const uint32_t d = tmem + (uint32_t)(buf * NT);
+                const uint32_t d = tmem + (uint32_t)((buf * Sh::ISSUERS + mi) * NT);
                 const uint32_t st = base + (uint32_t)(s * STAGE);
-                for (int a = 0; a < atoms; ++a) {
-                    const uint64_t ad = tc::desc_sw128(st + (uint32_t)(a * Sh::A_BYTES));
-                    const uint64_t bd = tc::desc_sw128(st + (uint32_t)(atoms * Sh::A_BYTES + a * Sh::B_BYTES));
-#pragma unroll
-                    for (int j = 0; j < kBK / kUmmaK; ++j) {
-                        // advance along K inside the 128-byte swizzle row: 32 bytes per step
-                        const uint64_t off = (uint64_t)((j * kUmmaK * 2) >> 4);
-                        tc::mma_bf16(d, ad + off, bd + off, idesc, accumulate);
-                        accumulate = 1;
-                    }
-                }
-                tc::commit(empty0 + 8 * s);  // the stage is free once these MMAs finish
+                tc::mma_stage<Sh::A_BYTES, Sh::B_BYTES>(d, st, st + (uint32_t)(atoms * Sh::A_BYTES), mi * H, H, idesc,
+                                                        accumulate);
+                tc::commit(empty0 + 8 * s);  // the stage is free once both issuers' MMAs finish
                 if (++s == stages) {
                     s = 0;
                     ph ^= 1u;
                 }
                 if (tag.y & 2) {  // the item's last k-tile: publish the accumulator
-                    acc_item[buf] = tag.x;
-                    tc::commit(accf0 + 8 * buf);
-                    mbar_arrive(tagb0 + 8 * buf);
+                    if (mi == 0)
+                        acc_item[buf] = tag.x;
+                    tc::commit(accf0 + 8 * buf);  // complete once both issuers' MMAs finish
+                    if (mi == 0)
+                        mbar_arrive(tagb0 + 8 * buf);
                     buf ^= 1;
                 }
             }
@@ -323,16 +333,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = item / S, piece = item % S;
             const int64_t n = (int64_t)t * BM + row;
             const bool mine = has_row && n < N;  // this lane's output row exists
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * NT);
+            // buffer buf's accumulators: issuer 0's, then issuer 1's (NT columns each)
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * Sh::ISSUERS * NT);
             // tile t's exchange words, [piece][b][row]
             unsigned long long *tile_x = xch + (int64_t)t * S * NT * BM + row;
             bool ok = true;
 #pragma unroll 1
             for (int c0 = 0; c0 < NT && c0 < B; c0 += 16) {
                 __syncwarp();  // tcgen05.ld is warp-collective: every lane, converged
-                uint32_t v[16];
+                uint32_t v[16], v1[16];
                 tc::ld16(taddr + (uint32_t)c0, v);
+                if (Sh::ISSUERS == 2)
+                    tc::ld16(taddr + (uint32_t)(NT + c0), v1);
                 tc::wait_ld();
+                if (Sh::ISSUERS == 2) {  // the block's partial: issuer 0's half of K, then issuer 1's
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+                }
                 if (S == 1) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
@@ -539,6 +557,11 @@ size_t tcs_xch_words(const dep_tactic_t &t, int64_t N, int64_t K)
 size_t tcs_counters(const dep_tactic_t &, int64_t)
 {
     return 2;  // the item counter pair at the end
+}
+
+int64_t tcs_items(const dep_tactic_t &t, int64_t N, int64_t K)
+{
+    return tiles_of(t, N) * effective_splits(t, K);
 }
 
 int tcs_blocks_per_sm(const dep_tactic_t &t)

@@ -145,11 +145,14 @@ def test_wide_fixup_bitexact_from_partials(dep, plans, NT, G, B, N, K):
     assert checked > 0
 
 
-@pytest.mark.parametrize("NT,G,B", [(256, 2, 256), (128, 2, 77), (64, 4, 64), (32, 4, 9)])
+@pytest.mark.parametrize("NT,G,B", [(256, 2, 256), (128, 2, 77), (64, 4, 64), (64, 2, 40)])
 def test_wide_whole_groups_equal_one_tile_kernel(dep, plans, NT, G, B):
     """With one block per group (no split) every output is its tile's TMEM
     accumulator rounded once, from the same MMAs in the same order as the
-    stream-K tensor-core kernel with one block per 128-row tile: equal bits."""
+    stream-K tensor-core kernel with one block per 128-row tile: equal bits.
+    (At N <= 32 the one-tile kernel splits every stage's K steps between two
+    MMA issuers and adds their two accumulators at the end, which the group
+    kernels do not, so the comparison is made at N >= 64.)"""
     N, K = 1500, 2048
     plan = plans(N, K)
     x = synth.normal_bf16(70, 2, (B, K))
