@@ -621,8 +621,10 @@ def probe_ceilings(dep, device):
 def run_graph_per_call(args, dep, calls, x_dev, W_dev, y_dev, flags, peak):
     """Per call, in the deployment's launch mode: a CUDA graph of R back-to-back
     launches of that call on a plan with programmatic dependent launch, the
-    weight rotated over every distinct weight of its shape in the workload (so
-    no launch finds its weight in L2), replayed; time per launch."""
+    weight rotated over every distinct weight of its shape in the workload,
+    plus copies of them until the rotation spans at least three L2 sizes (so no
+    launch finds its weight in L2, however small the weight), replayed; time
+    per launch."""
     import torch
     keys = {}
     for c in calls:
@@ -634,6 +636,10 @@ def run_graph_per_call(args, dep, calls, x_dev, W_dev, y_dev, flags, peak):
         ws = by_shape.setdefault((c.N, c.K), [])
         if W_dev[c.weight_key].data_ptr() not in [w.data_ptr() for w in ws]:
             ws.append(W_dev[c.weight_key])
+    l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    for (N, K), ws in by_shape.items():
+        need = min(16, -(-3 * l2 // (N * K * 2)))
+        ws += [ws[i % len(ws)].clone() for i in range(max(0, need - len(ws)))]
     lib = dep.lib()
     stream = torch.cuda.Stream()
     R, reps = 16, 10
@@ -666,7 +672,8 @@ def run_graph_per_call(args, dep, calls, x_dev, W_dev, y_dev, flags, peak):
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / (reps * R)
         gbs = c.algorithmic_bytes / (us * 1e-6) / 1e9
-        out.append({"call": c.name, "us": us, "gbs": gbs, "frac_of_peak": gbs / peak, "weights_rotated": len(ws)})
+        out.append({"call": c.name, "us": us, "gbs": gbs, "frac_of_peak": gbs / peak,
+                    "weights_rotated": min(R, len(ws))})
         del g
     for p in plans.values():
         code = dep.dep_projection_device_status(p)

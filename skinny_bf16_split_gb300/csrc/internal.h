@@ -224,5 +224,10 @@ cudaError_t stage_copy(const uint16_t *src, uint16_t *dst, size_t n, bool after_
 // elements read as zero.
 CUresult encode_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
                         uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+// The same matrix as {64, outer, inner / 64} column blocks (inner % 64 == 0):
+// one box {64, box_rows, blocks} equals `blocks` 2-D boxes {64, box_rows} with
+// the 128-byte swizzle, side by side in shared memory.
+CUresult encode_bf16_3d_blocks(CUtensorMap *map, const void *base, uint64_t inner, uint64_t outer,
+                               uint32_t box_rows, uint32_t blocks);
 
 }  // namespace dep

@@ -73,7 +73,7 @@ __device__ __forceinline__ uint16_t to_bf16(float v)
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                   uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms,
+                   uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms, int tma3,
                    unsigned long long *__restrict__ xch, int *__restrict__ status, const Bounds bd,
                    uint64_t limit_ns)
 {
@@ -138,18 +138,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t u = cur.u;
                 const uint32_t st = base + (uint32_t)(i * STAGE);
                 mbar_arrive_expect_tx(full0 + 8 * (int)i, STAGE);
-                for (int a = 0; a < atoms; ++a)
-                    tma_load_2d(st + (uint32_t)(a * kABytes), &tmW, (int)(u % KTILES) * KG + a * kBK,
-                                (int)(u / KTILES) * kBM, full0 + 8 * (int)i, pol_w);
+                if (tma3)  // the stage's slices in one copy (column-block view of W)
+                    tma_load_3d(st, &tmW, 0, (int)(u / KTILES) * kBM, (int)(u % KTILES) * atoms, full0 + 8 * (int)i,
+                                pol_w);
+                else
+                    for (int a = 0; a < atoms; ++a)
+                        tma_load_2d(st + (uint32_t)(a * kABytes), &tmW, (int)(u % KTILES) * KG + a * kBK,
+                                    (int)(u / KTILES) * kBM, full0 + 8 * (int)i, pol_w);
             }
             griddep_wait();
             UnitCursor cx(order);
             for (int64_t i = 0; i < pre; ++i, cx.next()) {
                 const int64_t u = cx.u;
                 const uint32_t xs = base + (uint32_t)(i * STAGE) + (uint32_t)(atoms * kABytes);
-                for (int a = 0; a < atoms; ++a)
-                    tma_load_2d(xs + (uint32_t)(a * S::B_BYTES), &tmX, (int)(u % KTILES) * KG + a * kBK, 0,
-                                full0 + 8 * (int)i, pol_x);
+                if (tma3)
+                    tma_load_3d(xs, &tmX, 0, 0, (int)(u % KTILES) * atoms, full0 + 8 * (int)i, pol_x);
+                else
+                    for (int a = 0; a < atoms; ++a)
+                        tma_load_2d(xs + (uint32_t)(a * S::B_BYTES), &tmX, (int)(u % KTILES) * KG + a * kBK, 0,
+                                    full0 + 8 * (int)i, pol_x);
             }
             int s = (int)(pre % stages);
             uint32_t ph = pre == stages ? 1u : 0u;
@@ -166,12 +173,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t st = base + (uint32_t)(s * STAGE);
                 mbar_arrive_expect_tx(full0 + 8 * s, STAGE);
                 const int t = (int)(u / KTILES), kg = (int)(u % KTILES);
-                for (int a = 0; a < atoms; ++a)
-                    tma_load_2d(st + (uint32_t)(a * kABytes), &tmW, kg * KG + a * kBK, t * kBM, full0 + 8 * s,
-                                pol_w);
-                for (int a = 0; a < atoms; ++a)
-                    tma_load_2d(st + (uint32_t)(atoms * kABytes + a * S::B_BYTES), &tmX, kg * KG + a * kBK, 0,
-                                full0 + 8 * s, pol_x);
+                if (tma3) {
+                    tma_load_3d(st, &tmW, 0, t * kBM, kg * atoms, full0 + 8 * s, pol_w);
+                    tma_load_3d(st + (uint32_t)(atoms * kABytes), &tmX, 0, 0, kg * atoms, full0 + 8 * s, pol_x);
+                } else {
+                    for (int a = 0; a < atoms; ++a)
+                        tma_load_2d(st + (uint32_t)(a * kABytes), &tmW, kg * KG + a * kBK, t * kBM, full0 + 8 * s,
+                                    pol_w);
+                    for (int a = 0; a < atoms; ++a)
+                        tma_load_2d(st + (uint32_t)(atoms * kABytes + a * S::B_BYTES), &tmX, kg * KG + a * kBK, 0,
+                                    full0 + 8 * s, pol_x);
+                }
                 ++issued;
                 if (++s == stages) {
                     s = 0;
@@ -352,21 +364,27 @@ cudaError_t run_nt(const dep_tactic_t &t, const RunArgs &a)
     cudaError_t e = prepare<NT>();
     if (e != cudaSuccess)
         return e;
-    CUtensorMap tmW, tmX;
-    if (encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, kBM,
-                       CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
     const int atoms = t.tile_k / kBK;
+    // One copy per stage (a column-block view) when K is a multiple of 64; else
+    // one per 64-column slice, whose tensor map zero-fills past column K.
+    const int tma3 = a.K % kBK == 0;
+    CUtensorMap tmW, tmX;
+    if ((tma3 ? encode_bf16_3d_blocks(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBM, (uint32_t)atoms)
+              : encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
     const int64_t T = (a.N + kBM - 1) / kBM, KT = (a.K + t.tile_k - 1) / t.tile_k, U = T * KT;
     const int grid = (int)(U < t.ctas ? U : t.ctas);
     const size_t smem = smem_bytes<NT>(t.stages, atoms);
     for (int32_t r0 = 0; r0 < a.B; r0 += NT) {
         const int32_t rows = a.B - r0 < NT ? a.B - r0 : NT;
-        if (encode_bf16_2d(&tmX, a.x + (size_t)r0 * a.K, (uint64_t)a.K, (uint64_t)rows, kBK, NT,
-                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        const uint16_t *xr = a.x + (size_t)r0 * a.K;
+        if ((tma3 ? encode_bf16_3d_blocks(&tmX, xr, (uint64_t)a.K, (uint64_t)rows, NT, (uint32_t)atoms)
+                  : encode_bf16_2d(&tmX, xr, (uint64_t)a.K, (uint64_t)rows, kBK, NT, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            CUDA_SUCCESS)
             return cudaErrorInvalidValue;
         e = launch(tc_gemm_kernel<NT>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
-                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, a.xch, a.status,
+                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, tma3, a.xch, a.status,
                    a.bounds(rows, smem), a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;

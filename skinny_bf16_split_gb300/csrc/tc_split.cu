@@ -95,7 +95,7 @@ __device__ __forceinline__ uint16_t to_bf16(float v)
 template <int NT, int BM>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_split_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms, int S,
+                    uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms, int S, int tma3,
                     unsigned long long *__restrict__ xch, int *__restrict__ dispenser,
                     int *__restrict__ status, const Bounds bd, uint64_t limit_ns)
 {
@@ -135,14 +135,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int flags = (kt == piece_begin(item % S, KT, S) ? 1 : 0) | (kt == kt_end - 1 ? 2 : 0);
         tags[st] = make_int2(item, flags);
         mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)STAGE);
-        for (int a = 0; a < atoms; ++a)
-            tma_load_2d(stage_addr(st) + (uint32_t)(a * Sh::A_BYTES), &tmW, kt * KG + a * kBK, tile * BM,
-                        full0 + 8 * st, pol_w);
+        if (tma3)  // the stage's slices in one copy (column-block view of W)
+            tma_load_3d(stage_addr(st), &tmW, 0, tile * BM, kt * atoms, full0 + 8 * st, pol_w);
+        else
+            for (int a = 0; a < atoms; ++a)
+                tma_load_2d(stage_addr(st) + (uint32_t)(a * Sh::A_BYTES), &tmW, kt * KG + a * kBK, tile * BM,
+                            full0 + 8 * st, pol_w);
     };
     auto issue_x = [&](int st, int k_tile) {
         const uint32_t xs = stage_addr(st) + (uint32_t)(atoms * Sh::A_BYTES);
-        for (int a = 0; a < atoms; ++a)
-            tma_load_2d(xs + (uint32_t)(a * Sh::B_BYTES), &tmX, k_tile * KG + a * kBK, 0, full0 + 8 * st, pol_x);
+        if (tma3)
+            tma_load_3d(xs, &tmX, 0, 0, k_tile * atoms, full0 + 8 * st, pol_x);
+        else
+            for (int a = 0; a < atoms; ++a)
+                tma_load_2d(xs + (uint32_t)(a * Sh::B_BYTES), &tmX, k_tile * KG + a * kBK, 0, full0 + 8 * st,
+                            pol_x);
     };
 
     if (threadIdx.x == 0) {
@@ -431,11 +438,15 @@ cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
     cudaError_t e = prepare<NT, BM>();
     if (e != cudaSuccess)
         return e;
+    const int atoms = t.tile_k / kBK;
+    // One copy per stage (a column-block view) when K is a multiple of 64; else
+    // one per 64-column slice, whose tensor map zero-fills past column K.
+    const int tma3 = a.K % kBK == 0;
     CUtensorMap tmW, tmX;
-    if (encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, BM, CU_TENSOR_MAP_SWIZZLE_128B) !=
+    if ((tma3 ? encode_bf16_3d_blocks(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, BM, (uint32_t)atoms)
+              : encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, BM, CU_TENSOR_MAP_SWIZZLE_128B)) !=
         CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    const int atoms = t.tile_k / kBK;
     const int S = (int)effective_splits(t, a.K);
     const int64_t items = tiles_of(t, a.N) * S;
     const int grid = (int)(items < t.ctas ? items : t.ctas);
@@ -443,11 +454,13 @@ cudaError_t run_shape(const dep_tactic_t &t, const RunArgs &a)
     int *dispenser = a.counters + a.n_counters - 2;
     for (int32_t r0 = 0; r0 < a.B; r0 += NT) {
         const int32_t rows = a.B - r0 < NT ? a.B - r0 : NT;
-        if (encode_bf16_2d(&tmX, a.x + (size_t)r0 * a.K, (uint64_t)a.K, (uint64_t)rows, kBK, NT,
-                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+        const uint16_t *xr = a.x + (size_t)r0 * a.K;
+        if ((tma3 ? encode_bf16_3d_blocks(&tmX, xr, (uint64_t)a.K, (uint64_t)rows, NT, (uint32_t)atoms)
+                  : encode_bf16_2d(&tmX, xr, (uint64_t)a.K, (uint64_t)rows, kBK, NT, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            CUDA_SUCCESS)
             return cudaErrorInvalidValue;
         e = launch(tc_split_kernel<NT, BM>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
-                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, S, a.xch, dispenser,
+                   a.y + (size_t)r0 * a.N, rows, (int)a.N, (int)a.K, t.stages, atoms, S, tma3, a.xch, dispenser,
                    a.status, a.bounds(rows, smem), a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
