@@ -45,8 +45,10 @@ __device__ __forceinline__ void publish16(unsigned long long *p, int64_t col_str
 // Reduce 16 batch columns of one row: out[j] = ((p_0 + p_1) + ...) + own[j] in
 // FP32, where p_i is read from piece i's word at base + i * piece_stride +
 // j * col_stride (i < np, j < ncols), waiting for its flag at most limit_ns.
-// Own values are kept (flag clear) at own_word + j * col_stride.  Returns false
-// if a wait gave up (out is then incomplete).
+// Own values are kept (flag clear) at own_word + j * col_stride.  PB pieces'
+// words are in flight at a time (one L2 round trip per PB pieces once they are
+// published).  Returns false if a wait gave up (out is then incomplete).
+template <int PB = 2>
 __device__ __forceinline__ bool reduce16(unsigned long long *base, int64_t piece_stride, int64_t col_stride,
                                          int np, int ncols, const uint32_t (&own)[16],
                                          unsigned long long *own_word, float (&out)[16], uint64_t limit_ns)
@@ -56,11 +58,11 @@ __device__ __forceinline__ bool reduce16(unsigned long long *base, int64_t piece
         if (j < ncols)
             store(own_word + j * col_stride, (unsigned long long)own[j]);
     bool ok = true;
-    for (int p0 = 0; p0 < np; p0 += 2) {  // two pieces' words in flight at a time
-        unsigned long long w[2][16];
-        unsigned long long *src[2];
+    for (int p0 = 0; p0 < np; p0 += PB) {
+        unsigned long long w[PB][16];
+        unsigned long long *src[PB];
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < PB; ++i) {
             src[i] = base + (int64_t)(p0 + i) * piece_stride;
 #pragma unroll
             for (int j = 0; j < 16; ++j)
@@ -70,7 +72,7 @@ __device__ __forceinline__ bool reduce16(unsigned long long *base, int64_t piece
         for (;;) {
             bool all = true;
 #pragma unroll
-            for (int i = 0; i < 2; ++i)
+            for (int i = 0; i < PB; ++i)
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     if (!(w[i][j] & kFull)) {
@@ -88,7 +90,7 @@ __device__ __forceinline__ bool reduce16(unsigned long long *base, int64_t piece
             }
         }
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < PB; ++i)
 #pragma unroll
             for (int j = 0; j < 16; ++j)
                 if (p0 + i < np) {

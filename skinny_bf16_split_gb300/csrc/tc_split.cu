@@ -380,8 +380,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float sum[16];
                 if (!dbg_range(tile_w + (int64_t)c0 * BM, (int64_t)(S - 1) * NT * BM + 15 * BM + 1, bd.xch, status)) {
                     ok = false;
-                } else if (!xch::reduce16(tile_x + (int64_t)c0 * BM, (int64_t)NT * BM, BM, S - 1, ncols, v, own, sum,
-                                          limit_ns)) {
+                } else if (!(S > 3 ? xch::reduce16<4>(tile_x + (int64_t)c0 * BM, (int64_t)NT * BM, BM, S - 1, ncols, v,
+                                                      own, sum, limit_ns)
+                                   : xch::reduce16<2>(tile_x + (int64_t)c0 * BM, (int64_t)NT * BM, BM, S - 1, ncols, v,
+                                                      own, sum, limit_ns))) {
                     record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
                     ok = false;
                 }
