@@ -82,6 +82,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--plan", default="default", choices=("default", "tune"))
+    ap.add_argument("--launch", default="pdl", choices=("plain", "pdl"),
+                    help="timed region's launches: stream launches on plans with programmatic dependent "
+                         "launch (each call streams its first weight stages while the previous one "
+                         "finishes; the default), or plain stream launches")
     ap.add_argument("--no-graph", action="store_true",
                     help="skip the CUDA-graph replay (programmatic dependent launch) measurements")
     ap.add_argument("--no-ceiling", action="store_true",
@@ -412,7 +416,19 @@ def run_ours(args):
         plans.setdefault((c.N, c.K), set()).add(c.B)
     tuned = args.plan == "tune" or args.workload in TUNED_BY_DEFAULT
     flags = dep.DEP_PLAN_TUNE if tuned else dep.DEP_PLAN_DEFAULT
-    plans = {k: dep.dep_projection_plan(k[0], k[1], sorted(v), flags) for k, v in plans.items()}
+    run_flags = flags | (dep.DEP_PLAN_PDL if args.launch == "pdl" else 0)
+    plans = {k: dep.dep_projection_plan(k[0], k[1], sorted(v), run_flags) for k, v in plans.items()}
+    # The same tables on plans without programmatic dependent launch (a saved and
+    # reloaded table), for the plain-launch figure reported beside `value`.
+    plain_plans = None
+    if args.launch == "pdl":
+        import tempfile
+        plain_plans = {}
+        with tempfile.TemporaryDirectory() as td:
+            for k, p in plans.items():
+                path = os.path.join(td, f"plan_{k[0]}_{k[1]}.txt")
+                dep.dep_projection_plan_save(p, path)
+                plain_plans[k] = dep.dep_projection_plan_load(path, k[0], k[1])
     tactics = [dep.dep_projection_plan_query(plans[(c.N, c.K)], c.B) for c in calls]
     launches_per_step = sum(-(-c.B // t.cols) for c, t in zip(calls, tactics))
     stream = torch.cuda.current_stream()
@@ -421,9 +437,10 @@ def run_ours(args):
     lib = dep.lib()
     args_c = [(plans[(c.N, c.K)], x_dev[i].data_ptr(), W_dev[c.weight_key].data_ptr(),
                y_dev[i].data_ptr(), c.B) for i, c in enumerate(calls)]
+    args_plain = None if plain_plans is None else [(plain_plans[(c.N, c.K)],) + a[1:] for c, a in zip(calls, args_c)]
 
-    def one_step(ev=None, only=None):
-        for i, (p, x, W, y, B) in enumerate(args_c):
+    def one_step(ev=None, only=None, plain=False):
+        for i, (p, x, W, y, B) in enumerate(args_plain if plain else args_c):
             if only is not None and i not in only:
                 continue
             if ev is not None:
@@ -438,7 +455,7 @@ def run_ours(args):
         if world > 1:
             torch.distributed.barrier()
 
-    def timed_steps(steps, lead, only=None):
+    def timed_steps(steps, lead, only=None, plain=False):
         """Device time of `steps` steps back to back, events at the two ends only;
         the host stays at most `lead` steps ahead of the GPU."""
         marks = [torch.cuda.Event() for _ in range(steps)]
@@ -447,7 +464,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         t0.record(stream)
         for s_ in range(steps):
-            one_step(only=only)
+            one_step(only=only, plain=plain)
             marks[s_].record(stream)
             if s_ >= lead:
                 marks[s_ - lead].synchronize()
@@ -472,6 +489,11 @@ def run_ours(args):
     # only (a pair of events around every call costs the GPU front end a few us
     # per call, which a decode step does not pay).
     elapsed_ms = timed_steps(args.steps, lead)
+    plain_ms = None
+    if args_plain is not None:
+        for _ in range(min(3, args.warmup)):
+            one_step(plain=True)
+        plain_ms = timed_steps(args.steps, lead, plain=True)
 
     # Instrumented region: the same K steps with every call bracketed by its own
     # events, for the per-call figures and each kernel's share of the time.
@@ -498,7 +520,7 @@ def run_ours(args):
         families.setdefault(kernel_name(t), []).append(i)
     family_ms = {k: reduce_max(timed_steps(args.steps, lead, only=set(v))) for k, v in families.items()}
     clocks = sampler.stop()
-    for p in plans.values():
+    for p in list(plans.values()) + list((plain_plans or {}).values()):
         code = dep.dep_projection_device_status(p)
         if code:
             raise RuntimeError(f"a kernel reported device status {code}")
@@ -559,8 +581,15 @@ def run_ours(args):
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = cpu_baseline(calls, weights, xs_host, args.cpu_seconds)
 
-    for p in plans.values():
+    for p in list(plans.values()) + list((plain_plans or {}).values()):
         dep.dep_projection_plan_destroy(p)
+    plain_value = None
+    if plain_ms is not None:
+        plain_ms = reduce_max(plain_ms)
+        plain_value = {"value": whole_job_gbs(bytes_per_step, args.steps, world, plain_ms), "unit": UNIT,
+                       "ms_per_step": plain_ms / args.steps,
+                       "how": "the same K steps as `value`, plain stream launches (the same tactic tables "
+                              "on plans without programmatic dependent launch)"}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -574,7 +603,11 @@ def run_ours(args):
                       f"({instrumented_ms / args.steps:.4f} ms per step with those events); graph_pdl_us: "
                       "a CUDA graph of back-to-back launches of the call with programmatic dependent launch",
             "gpu_launches": launches_per_step * args.steps, "per_call": per_call,
-            "plan": "tune" if tuned else "default", "kernel_sources": source_hash(),
+            "plan": "tune" if tuned else "default",
+            "launch": ("stream launches on plans with programmatic dependent launch (DEP_PLAN_PDL)"
+                       if args.launch == "pdl" else "plain stream launches"),
+            "plain_launches": plain_value,
+            "kernel_sources": source_hash(),
             "device": torch.cuda.get_device_name(device),
         }
         print(json.dumps(line), flush=True)

@@ -61,8 +61,9 @@ def test_workload_full_size(dep, orc, weights, workload):
     batches = {}
     for c in calls:
         batches.setdefault((c.N, c.K), set()).add(c.B)
-    from bench import TUNED_BY_DEFAULT  # the launch configuration the bench times
-    flags = dep.DEP_PLAN_TUNE if workload in TUNED_BY_DEFAULT else dep.DEP_PLAN_DEFAULT
+    from bench import TUNED_BY_DEFAULT  # the launch configuration the bench times: tuned where it
+    # tunes, programmatic dependent launch, calls back to back on one stream
+    flags = (dep.DEP_PLAN_TUNE if workload in TUNED_BY_DEFAULT else dep.DEP_PLAN_DEFAULT) | dep.DEP_PLAN_PDL
     plans = {k: dep.dep_projection_plan(k[0], k[1], sorted(v), flags) for k, v in batches.items()}
     try:
         for i, c in enumerate(calls):
