@@ -374,8 +374,8 @@ def kernel_name(t) -> str:
         return f"splitk_fma_c{t.cols}"
     if t.kind == dep.DEP_KIND_ROWS:
         return f"rows_gemv_c{t.cols}"
-    if t.kind == dep.DEP_KIND_TC_SPLIT:
-        return f"tc_split_n{t.cols}"
+    if t.kind == dep.DEP_KIND_TC_SPLIT:  # 64-row tiles are another instantiation (MMA M = 64)
+        return f"tc_split_n{t.cols}" + ("_m64" if t.tile_n == 64 else "")
     if t.kind == dep.DEP_KIND_TC_WIDE:
         return f"tc_wide_n{t.cols}_g{t.tile_n // 128}"
     if t.kind == dep.DEP_KIND_TC_CLUSTER:

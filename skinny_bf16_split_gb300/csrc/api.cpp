@@ -273,7 +273,22 @@ dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
             return t;
     }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
-    const int64_t tiles = (N + 127) / 128;
+    const int64_t tiles = (N + 127) / 128, t64 = (N + 63) / 64;
+    // Up to 32 batch rows on long weight rows (K >= 3072) whose 64-row tiles fit
+    // on the SMs: 64-row K-piece tiles in as few pieces as fill the SMs (o_proj:
+    // 112 tiles, one piece each, no exchange).  Measured on GB300 per call (CUDA
+    // graph + PDL, weights rotated past L2), o_proj 7168 x 12288: B = 32 29.9 us
+    // against 33.4 us for the stream-K kernel; B = 4 / 16 28.4 / 28.6 us against
+    // 28.7 / 29.2 us for 128-row tiles in two pieces.  On shorter rows 128-row
+    // tiles win: they drain a prefetched ring with half the MMA instructions.
+    if (cols <= 32 && t64 <= sm_count && K >= 3072) {
+        const int32_t splits = (int32_t)std::min<int64_t>(64, std::max<int64_t>(1, sm_count / t64));
+        for (int32_t st : {6, 5, 4, 3}) {
+            const dep_tactic_t t = tcs_tactic(rows, cols, st, sm_count, 256, splits, 64);
+            if (dep::tcs_valid(t))
+                return t;
+        }
+    }
     // Widest stage (most contiguous bytes per weight row) that still leaves a
     // ring of at least three stages.
     if (cols == 16) {
@@ -295,7 +310,11 @@ dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
     // 7168 B = 128 / 256: 44.6 / 50.0 us against 45.4 / 61.0 us for the one-tile
     // kernel; o_proj 7168 x 12288 B = 64..256 (k = 4): 37.2 / 41.0 / 49.9 us; KDA
     // 49376 x 7168 B = 128 (four-tile groups) / 256 (k = 2): 119.6 / 152.6 us.
-    if (cols >= 64) {
+    // At 64 rows on a weight whose 128-row tiles nearly fill the SMs (DSA: 114
+    // tiles), one tile per block of the stream-K kernel, no K split, measured
+    // faster than clusters of two (36.6 against 38.1 us per call, CUDA graph + PDL).
+    const bool one_tile_each = tiles <= sm_count && 4 * tiles >= 3 * (int64_t)sm_count;
+    if (cols >= 64 && !(cols == 64 && one_tile_each)) {
         const int64_t t2 = (N + 255) / 256, t3 = (N + 191) / 192, t4 = (N + 511) / 512;
         const int32_t sw = cols == 256 ? 4 : (cols == 128 ? 6 : 5);
         if (cols == 256 && 2 * t3 <= sm_count && 8 * t3 > 3 * (int64_t)sm_count) {
@@ -322,7 +341,7 @@ dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
                 return t;
         }
     }
-    const int32_t ctas = (tiles <= sm_count && 4 * tiles >= 3 * (int64_t)sm_count) ? (int32_t)tiles : sm_count;
+    const int32_t ctas = one_tile_each ? (int32_t)tiles : sm_count;
     // 64-column stages for the widest batches.
     for (int32_t tk : {256, 128}) {
         for (int32_t st : {6, 5, 4, 3}) {

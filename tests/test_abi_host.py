@@ -58,8 +58,8 @@ def test_default_table_follows_split_rule(dep):
                               dep.DEP_KIND_TC_SPLIT)
             if t.max_rows <= 2:  # the smallest batches: warp split-K over whole rows
                 assert t.kind == dep.DEP_KIND_ROWS
-            else:  # 56 tiles of 128 rows on 152 SMs: two K pieces per tile
-                assert (t.kind, t.tile_n, t.splits, t.cols) == (dep.DEP_KIND_TC_SPLIT, 128, 2, 16)
+            else:  # long rows, 112 tiles of 64 rows on 152 SMs: one tile per block, one piece
+                assert (t.kind, t.tile_n, t.splits, t.cols) == (dep.DEP_KIND_TC_SPLIT, 64, 1, 16)
         for B, key in [(1, 1), (3, 4), (5, 8), (16, 16), (17, 16), (1000, 16)]:
             assert dep.dep_projection_plan_query(plan, B).max_rows == key
     finally:
@@ -84,10 +84,11 @@ def test_default_batches_when_none_given(dep):
         assert [t.max_rows for t in table] == [1, 2, 4, 8, 16, 32, 64, 128, 256]
         # 114 tiles of 128 rows nearly fill 152 SMs: whole tiles, one per block
         assert all((t.kind, t.splits) == (dep.DEP_KIND_TC_SPLIT, 1) for t in table if 2 < t.max_rows <= 16)
-        assert all((t.kind, t.ctas) == (dep.DEP_KIND_TC, 114) for t in table if t.max_rows == 32)
-        # 64 and 128 rows: 57 groups of two tiles, a cluster of two CTAs each; 256
-        # rows: 76 groups of 192 rows (a 128-row and a 64-row tile), 152 CTAs
-        wide = [t for t in table if 64 <= t.max_rows <= 128]
+        # 32 and 64 rows: one 128-row tile per block (114 tiles), no K split
+        assert all((t.kind, t.ctas) == (dep.DEP_KIND_TC, 114) for t in table if t.max_rows in (32, 64))
+        # 128 rows: 57 groups of two tiles, a cluster of two CTAs each; 256 rows:
+        # 76 groups of 192 rows (a 128-row and a 64-row tile), 152 CTAs
+        wide = [t for t in table if t.max_rows == 128]
         assert all((t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, 256, 2, 114) for t in wide)
         t = table[-1]
         assert (t.max_rows, t.kind, t.tile_n, t.splits, t.ctas) == (256, dep.DEP_KIND_TC_CLUSTER, 192, 2, 152)
@@ -105,7 +106,9 @@ def test_default_rule_wide_batches(dep, N, sms, expect):
     """The default rule for 64-256 rows: a cluster of k = SMs / groups (at most
     4) CTAs per group of two 128-row tiles while the groups fit on the SMs in
     clusters of two; otherwise clusters of two at 256 rows, groups of four tiles
-    one CTA each at 128 rows if they fit, the one-tile stream-K kernel else."""
+    one CTA each at 128 rows if they fit, the one-tile stream-K kernel else.  At
+    64 rows, where the 128-row tiles nearly fill the SMs, one tile per block of
+    the stream-K kernel."""
     plan = dep.dep_projection_plan_host(N, 7168, [64, 128, 256], sms)
     try:
         table = {t.max_rows: t for t in dep.dep_projection_plan_table(plan)}
@@ -114,6 +117,9 @@ def test_default_rule_wide_batches(dep, N, sms, expect):
                 t = table[b]
                 if b == 256 and N == 14560:  # 76 groups of 192 rows fill the SMs
                     assert (t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, 192, 2, 152), t
+                    continue
+                if b == 64 and 4 * -(-N // 128) >= 3 * sms:  # 128-row tiles nearly fill the SMs
+                    assert (t.kind, t.ctas) == (dep.DEP_KIND_TC, -(-N // 128)), t
                     continue
                 assert (t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, *expect), (b, t)
         else:

@@ -369,8 +369,8 @@ def test_tc_parity_vs_oracle(dep, orc, plan_cache, N, K, NT, tile_k):
 @pytest.mark.parametrize("which", ["default", "stream-k"])
 def test_tc_determinism_and_graph_replay(dep, plan_cache, B, which):
     """The tensor-core kernels' split-K combinations are order-fixed: repeated
-    runs and CUDA-graph replays give identical bits (the default plan takes K
-    pieces for this 56-tile weight up to 16 rows and clusters of CTAs past them;
+    runs and CUDA-graph replays give identical bits (the default plan takes the
+    K-piece kernel for this weight up to 16 rows and clusters of CTAs past them;
     the stream-K kernel is installed explicitly)."""
     N, K = 7168, 4096
     x, W = to_dev(synth.normal_bf16(B, 2, (B, K))), to_dev(synth.normal_bf16(5, 1, (N, K), 0.02))
@@ -828,6 +828,7 @@ def test_exchange_give_up_is_reported_and_cleared(dep, orc):
     fma = fma_tactic(dep, 8, sms)
     wide = dep.dep_tactic_t(max_rows=64, kind=dep.DEP_KIND_TC_WIDE, ctas=sms, tile_n=256, tile_k=64, stages=4,
                             cols=64)
+    pieces = tcs_tactic(dep, 16, sms, 2, 3, 256, max_rows=B)  # 128-row tiles in two K pieces: exchanged
 
     def all_runs(plan):
         return [run(dep, plan, x, W, N), run(dep, plan, x, W, N, fma), run(dep, plan, x, W, N, wide)]
@@ -835,8 +836,9 @@ def test_exchange_give_up_is_reported_and_cleared(dep, orc):
     fresh = dep.dep_projection_plan(N, K, [B])
     plan = dep.dep_projection_plan(N, K, [B])
     try:
-        dep.dep_projection_plan_set(fresh, wide)
-        dep.dep_projection_plan_set(plan, wide)
+        for p_ in (fresh, plan):
+            dep.dep_projection_plan_set(p_, wide)
+            dep.dep_projection_plan_set(p_, pieces)
         assert dep.dep_projection_plan_query(plan, B).kind == dep.DEP_KIND_TC_SPLIT
         want = all_runs(fresh)
         assert dep.dep_projection_device_status(fresh) == 0
