@@ -27,6 +27,7 @@ the line reports the total bytes of all ranks over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -73,7 +74,7 @@ SHARED_SOURCES = ["ptx.cuh", "internal.h"]
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=synth.WORKLOADS, default="baseline")
@@ -167,26 +168,70 @@ def read_traffic(kernel: str):
 
 # ---------------------------------------------------------------- clocks -----
 
+class _Nvml:
+    """The driver's management library called in-process through ctypes: SM
+    clock, maximum SM clock and the clock event reasons of one GPU (queries
+    only).  In-process calls replace spawning `nvidia-smi` every 150 ms, which
+    now and then stalled the launching thread for 40-70 ms and let the GPU run
+    dry in the middle of a timed region."""
+
+    CLOCK_SM = 1  # nvmlClockType_t
+    REASON_BITS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+                   ("sw_power_cap", 0x4))
+
+    def __init__(self, uuid: str):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.handle = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.handle)) != 0:
+            raise OSError(f"no NVML device {uuid}")
+        name = "nvmlDeviceGetCurrentClocksEventReasons"
+        self.reasons_fn = getattr(self.lib, name, None) or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def query(self):
+        ct = self.ct
+        sm, mx, mask = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if (self.lib.nvmlDeviceGetClockInfo(self.handle, self.CLOCK_SM, ct.byref(sm)) != 0 or
+                self.lib.nvmlDeviceGetMaxClockInfo(self.handle, self.CLOCK_SM, ct.byref(mx)) != 0 or
+                self.reasons_fn(self.handle, ct.byref(mask)) != 0):
+            return None
+        return float(sm.value), float(mx.value), ["Active" if mask.value & bit else "Not Active"
+                                                  for _, bit in self.REASON_BITS]
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
     """SM clock and throttle reasons of the bench's GPU while it runs: a thread
-    that runs one `nvidia-smi --query-gpu` every ~150 ms (queries only; no
-    setting is touched).  Each query's output is read whole, so no sample is
-    lost to output buffering when sampling stops."""
+    that queries them every ~0.5 s (queries only; no setting is touched), through
+    NVML in-process where the driver's library loads, else through one
+    `nvidia-smi --query-gpu` per sample (each output read whole, so no sample is
+    lost to output buffering when sampling stops)."""
 
     QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
              "clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    # Every management query can delay the GPU now and then (a 40-250 ms stall in
+    # about one run in eight at 150 ms, none without sampling): sample sparingly.
+    INTERVAL_S = 0.5
 
     def __init__(self, device_index: int):
         import threading
         self.device = device_index
         self.rows = []
         self.target = None
+        self.nvml = None
         self._stop = threading.Event()
         self._thread = None
 
     def _query(self, target):
+        if self.nvml is not None:
+            return self.nvml.query()
         r = subprocess.run(["nvidia-smi", "-i", target, f"--query-gpu={self.QUERY}",
                             "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=10)
         if r.returncode != 0:
@@ -199,14 +244,26 @@ class ClockSampler:
         except ValueError:
             return None
 
-    def _pick_target(self):
-        candidates = []
+    def _uuid(self):
         try:
             import torch
             uuid = str(torch.cuda.get_device_properties(self.device).uuid)
-            candidates.append(uuid if uuid.startswith("GPU-") else f"GPU-{uuid}")
+            return uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
         except Exception:
-            pass
+            return None
+
+    def _pick_target(self):
+        uuid = self._uuid()
+        if uuid:
+            try:
+                nv = _Nvml(uuid)
+                if nv.query() is not None:
+                    self.nvml = nv
+                    return uuid
+                nv.close()
+            except (OSError, AttributeError):
+                pass
+        candidates = [uuid] if uuid else []
         visible = os.environ.get("CUDA_VISIBLE_DEVICES", "")
         if visible:
             candidates.append(visible.split(",")[self.device].strip())
@@ -227,7 +284,7 @@ class ClockSampler:
                 row = None
             if row is not None:
                 self.rows.append(row)
-            self._stop.wait(0.15)
+            self._stop.wait(self.INTERVAL_S)
 
     def start(self):
         import threading
@@ -241,14 +298,17 @@ class ClockSampler:
         if self._thread is not None:
             self._stop.set()
             self._thread.join(timeout=15)
+        if self.nvml is not None:
+            self.nvml.close()
+        how = "NVML in-process" if self.nvml is not None else f"nvidia-smi -i {self.target}"
         rows = self.rows
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "source": f"nvidia-smi -i {self.target}" if self.target else "nvidia-smi unavailable"}
+                    "source": how if self.target else "NVML and nvidia-smi unavailable"}
         reasons = sorted({self.NAMES[i] for _, _, r in rows for i, v in enumerate(r) if v == "Active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
                 "sm_mhz_min": min(r[0] for r in rows), "reasons": reasons, "samples": len(rows),
-                "source": f"nvidia-smi -i {self.target}, every ~150 ms while the timed regions ran"}
+                "source": f"{how} ({self.target}), every ~{self.INTERVAL_S * 1e3:.0f} ms while the timed regions ran"}
 
 
 # ----------------------------------------------------------- cpu baseline ----
@@ -455,22 +515,42 @@ def run_ours(args):
         if world > 1:
             torch.distributed.barrier()
 
-    def timed_steps(steps, lead, only=None, plain=False):
+    host_wait_ms = {}
+    step_ms_stats = {}
+
+    def timed_steps(steps, lead, only=None, plain=False, tag=None):
         """Device time of `steps` steps back to back, events at the two ends only;
-        the host stays at most `lead` steps ahead of the GPU."""
-        marks = [torch.cuda.Event() for _ in range(steps)]
+        the host stays at most `lead` steps ahead of the GPU.  The Python garbage
+        collector is off meanwhile.  With `tag`, the time the host spent waiting
+        for the GPU is kept: close to the device time when the GPU set the pace,
+        far below it when the host could not keep the queue filled."""
+        marks = [torch.cuda.Event(enable_timing=bool(tag)) for _ in range(steps)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
+        gc_was = gc.isenabled()
+        gc.disable()
+        waited = 0.0
         t0.record(stream)
         for s_ in range(steps):
             one_step(only=only, plain=plain)
             marks[s_].record(stream)
             if s_ >= lead:
+                h = time.perf_counter()
                 marks[s_ - lead].synchronize()
+                waited += time.perf_counter() - h
         t1.record(stream)
         torch.cuda.synchronize()
+        if gc_was:
+            gc.enable()
         barrier()
+        if tag:
+            host_wait_ms[tag] = waited * 1e3
+            per = np.diff([0.0] + [t0.elapsed_time(m) for m in marks])
+            med = float(np.median(per))
+            step_ms_stats[tag] = {"median": round(med, 4), "max": round(float(per.max()), 3),
+                                  "steps_over_1.5x_median": int((per > 1.5 * med).sum()),
+                                  "ms_in_those": round(float(per[per > 1.5 * med].sum()), 3)}
         return t0.elapsed_time(t1)
 
     sampler = ClockSampler(device)
@@ -488,12 +568,12 @@ def run_ours(args):
     # Timed region for `value`: K steps back to back, CUDA events at its two ends
     # only (a pair of events around every call costs the GPU front end a few us
     # per call, which a decode step does not pay).
-    elapsed_ms = timed_steps(args.steps, lead)
+    elapsed_ms = timed_steps(args.steps, lead, tag="value")
     plain_ms = None
     if args_plain is not None:
         for _ in range(min(3, args.warmup)):
             one_step(plain=True)
-        plain_ms = timed_steps(args.steps, lead, plain=True)
+        plain_ms = timed_steps(args.steps, lead, plain=True, tag="plain")
 
     # Instrumented region: the same K steps with every call bracketed by its own
     # events, for the per-call figures and each kernel's share of the time.
@@ -518,7 +598,7 @@ def run_ours(args):
     families = {}
     for i, t in enumerate(tactics):
         families.setdefault(kernel_name(t), []).append(i)
-    family_ms = {k: reduce_max(timed_steps(args.steps, lead, only=set(v))) for k, v in families.items()}
+    family_ms = {k: reduce_max(timed_steps(args.steps, lead, only=set(v), tag=f"family:{k}")) for k, v in families.items()}
     clocks = sampler.stop()
     for p in list(plans.values()) + list((plain_plans or {}).values()):
         code = dep.dep_projection_device_status(p)
@@ -598,6 +678,8 @@ def run_ours(args):
             "config": workload_config(args.workload, calls),
             "roofline": rooflines[dom], "roofline_by_kernel": rooflines, "ceilings": ceilings,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "graph_pdl": graph,
+            "host_wait_ms": {k: round(v, 3) for k, v in host_wait_ms.items()},
+            "step_ms": step_ms_stats,
             "timing": "value: K steps back to back, CUDA events at the region's ends only; per_call: "
                       "the same K steps again with every call bracketed by its own events "
                       f"({instrumented_ms / args.steps:.4f} ms per step with those events); graph_pdl_us: "
