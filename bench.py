@@ -524,13 +524,16 @@ def run_ours(args):
         collector is off meanwhile.  With `tag`, the time the host spent waiting
         for the GPU is kept: close to the device time when the GPU set the pace,
         far below it when the host could not keep the queue filled."""
-        marks = [torch.cuda.Event(enable_timing=bool(tag)) for _ in range(steps)]
+        # Plain (non-timing) marks: a timing event between two calls would cut the
+        # programmatic dependent launch between them.
+        marks = [torch.cuda.Event() for _ in range(steps)]
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
         gc_was = gc.isenabled()
         gc.disable()
         waited = 0.0
+        done_at = []  # host time at which each step was seen complete
         t0.record(stream)
         for s_ in range(steps):
             one_step(only=only, plain=plain)
@@ -538,7 +541,8 @@ def run_ours(args):
             if s_ >= lead:
                 h = time.perf_counter()
                 marks[s_ - lead].synchronize()
-                waited += time.perf_counter() - h
+                done_at.append(time.perf_counter())
+                waited += done_at[-1] - h
         t1.record(stream)
         torch.cuda.synchronize()
         if gc_was:
@@ -546,7 +550,9 @@ def run_ours(args):
         barrier()
         if tag:
             host_wait_ms[tag] = waited * 1e3
-            per = np.diff([0.0] + [t0.elapsed_time(m) for m in marks])
+            # Steps seen complete one after another by the host (the GPU sets the
+            # pace, so these are the steps' own durations, plus host jitter).
+            per = np.diff(np.array(done_at) * 1e3) if len(done_at) > 2 else np.zeros(1)
             med = float(np.median(per))
             step_ms_stats[tag] = {"median": round(med, 4), "max": round(float(per.max()), 3),
                                   "steps_over_1.5x_median": int((per > 1.5 * med).sum()),
