@@ -854,3 +854,56 @@ def test_exchange_give_up_is_reported_and_cleared(dep, orc):
     finally:
         dep.dep_projection_plan_destroy(plan)
         dep.dep_projection_plan_destroy(fresh)
+
+
+@pytest.mark.parametrize("kind,NT,tile_n,tile_k,B", [("split", 16, 128, 256, 16), ("split", 16, 64, 256, 5),
+                                                     ("split", 32, 64, 128, 20), ("gemm", 16, 128, 128, 9),
+                                                     ("gemm", 64, 128, 128, 64)])
+def test_stage_copy_forms_agree_bitwise(dep, kind, NT, tile_n, tile_k, B):
+    """A K that is a multiple of 64 loads each stage with one copy of a column-block
+    view of W and x; any other K loads it slice by slice through 2-D maps that
+    zero-fill past column K.  The same product with 8 zero columns appended to x
+    and W (K = 4104) takes the second form and only adds zero products to each
+    accumulator, so with one piece per tile the two give identical bits."""
+    N, K, pad = 1000, 4096, 8
+    x = synth.normal_bf16(90 + NT, 2, (B, K))
+    W = synth.normal_bf16(91, 1, (N, K), sigma=0.02)
+    xp = np.concatenate([x, np.zeros((B, pad), np.uint16)], axis=1)
+    Wp = np.concatenate([W, np.zeros((N, pad), np.uint16)], axis=1)
+    tiles = -(-N // tile_n)
+    if kind == "split":
+        t = tcs_tactic(dep, NT, sm_count(), 1, 2, tile_k, max_rows=B, tile_n=tile_n)
+    else:
+        t = tc_tactic(dep, NT, tiles, 2, tile_k)
+        t.max_rows = B
+    got = []
+    for k_, xx, ww in ((K, x, W), (K + pad, xp, Wp)):
+        plan = tcs_plan(dep, N, k_, [t])
+        try:
+            got.append(run(dep, plan, xx, ww, N, t))
+            assert dep.dep_projection_device_status(plan) == 0
+        finally:
+            dep.dep_projection_plan_destroy(plan)
+    np.testing.assert_array_equal(got[0], got[1])
+
+
+def test_grid_larger_than_the_device_holds_is_refused(dep):
+    """Kinds whose blocks wait on one another need the whole grid resident: a
+    tactic asking for more blocks than the device holds at once is refused by
+    plan_set and run_tactic, and the plan keeps its table."""
+    N, K = 7168, 4096
+    plan = dep.dep_projection_plan(N, K, [16])
+    try:
+        before = dep.dep_projection_plan_query(plan, 16).as_dict()
+        too_many = tc_tactic(dep, 16, 8 * sm_count(), 4, 64)  # 448 tiles x 64 units: enough units
+        too_many.max_rows = 16
+        with pytest.raises(dep.DepError) as e:
+            dep.dep_projection_plan_set(plan, too_many)
+        assert e.value.status == dep.DEP_ERR_UNSUPPORTED
+        assert dep.dep_projection_plan_query(plan, 16).as_dict() == before
+        x, W = synth.normal_bf16(1, 2, (16, K)), synth.normal_bf16(2, 1, (N, K), sigma=0.02)
+        with pytest.raises(dep.DepError) as e:
+            run(dep, plan, x, W, N, too_many)
+        assert e.value.status == dep.DEP_ERR_UNSUPPORTED
+    finally:
+        dep.dep_projection_plan_destroy(plan)
