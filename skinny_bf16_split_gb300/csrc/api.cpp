@@ -863,7 +863,7 @@ dep_status_t dep_projection_run_host(dep_plan_t plan, const void *x_host, const 
     if (mapped) {
         const dep_tactic_t *t = lookup(plan, B);
         if (dep::stage_copy(static_cast<const uint16_t *>(ax.devicePointer), plan->x_stage, (size_t)B * plan->K,
-                            false, s) != cudaSuccess) {
+                            true, s) != cudaSuccess) {
             cudaGetLastError();
             return DEP_ERR_CUDA;
         }

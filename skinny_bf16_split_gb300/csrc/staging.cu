@@ -3,12 +3,15 @@
 // When the caller's host buffers are pinned (mapped into the device's address
 // space), x is gathered into the plan's device staging area and y written back
 // by two small kernels instead of two memcpys.  Chained by programmatic
-// dependent launch: the gather triggers its dependents at once, so the
-// projection kernel launches early and streams its first weight stages while x
-// is still arriving (it reads x only after its griddepcontrol.wait); the
-// write-back kernel launches early the same way and waits for the projection
-// before it reads y.  Plain loads and stores of mapped host memory; 16-byte
-// vectors where both sides allow it, 2-byte elements for the rest.
+// dependent launch: each copy triggers its dependents at once and waits for
+// the preceding grid before it reads (so a source written by earlier work in
+// the stream is complete, and the staging area is no longer read by an earlier
+// projection); the projection kernel launches early and streams its first
+// weight stages while x is still arriving (it reads x only after its
+// griddepcontrol.wait); the next call's gather launches early the same way, so
+// no launch gap separates the calls.  Plain loads and stores of mapped host
+// memory; 16-byte vectors where both sides allow it, 2-byte elements for the
+// rest.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -45,9 +48,10 @@ int copy_grid(size_t n)
 
 cudaError_t stage_copy(const uint16_t *src, uint16_t *dst, size_t n, bool after_preceding, cudaStream_t stream)
 {
-    // The gather (after_preceding = false) is an ordinary launch: it waits for
-    // all earlier work in the stream.  The write-back is launched with the
-    // programmatic attribute and waits for the projection itself.
+    // With after_preceding the copy is launched with the programmatic attribute
+    // and waits for the preceding grid itself (a preceding kernel that does not
+    // trigger its dependents, or a copy, still orders it as a plain launch
+    // would); without, it is an ordinary launch.
     return launch(stage_copy_kernel, dim3(copy_grid(n)), dim3(kStageThreads), 0, stream, after_preceding, src, dst,
                   n, after_preceding ? 1 : 0);
 }

@@ -272,6 +272,30 @@ def test_run_host_end_to_end(dep, orc, plan_cache, monkeypatch, B, N, memory):
     assert dep.dep_projection_device_status(plan) == 0
 
 
+@pytest.mark.parametrize("B", [4, 16])
+def test_run_host_chain_through_pinned_buffers(dep, plan_cache, B):
+    """Calls chained through the host buffers with no synchronisation between
+    them: each call's pinned output is the next call's pinned input.  The
+    zero-copy gather of a call, launched with the programmatic attribute, must
+    still see the write-back of the call before it (it reads only after the
+    preceding grid has completed): the chain gives the bits of the same chain
+    run one synchronised call at a time."""
+    N = K = 2048
+    plan = get_plan(dep, plan_cache, N, K)
+    W = synth.normal_bf16(130, 1, (N, K), sigma=0.02)
+    Wd = to_dev(W)
+    bufs = [torch.empty((B, K), dtype=torch.bfloat16).pin_memory() for _ in range(7)]
+    bufs[0].copy_(torch.from_numpy(synth.normal_bf16(131, 2, (B, K)).view(np.int16)).view(torch.bfloat16))
+    for i in range(6):
+        dep.dep_projection_run_host(plan, bufs[i], Wd, bufs[i + 1], B)
+    torch.cuda.synchronize()
+    x = bufs[0].view(torch.int16).numpy().view(np.uint16).copy()
+    for i in range(6):
+        x = run(dep, plan, x, W, N)
+        np.testing.assert_array_equal(bufs[i + 1].view(torch.int16).numpy().view(np.uint16), x)
+    assert dep.dep_projection_device_status(plan) == 0
+
+
 def test_run_host_captured_in_a_graph(dep, plan_cache):
     """The host-buffer entry point with pinned buffers inside a CUDA graph: the
     zero-copy gather, the projection and the write-back (chained by programmatic
