@@ -42,6 +42,10 @@ def main():
                            cols=16, splits=3)),
             ("k-pieces-64", T(max_rows=16, kind=dep.DEP_KIND_TC_SPLIT, ctas=sms, tile_n=64, tile_k=64, stages=3,
                               cols=16, splits=5)),
+            ("k-pieces-64-whole", T(max_rows=16, kind=dep.DEP_KIND_TC_SPLIT, ctas=sms, tile_n=64, tile_k=256,
+                                    stages=5, cols=16, splits=1)),
+            ("k-pieces-5", T(max_rows=16, kind=dep.DEP_KIND_TC_SPLIT, ctas=sms, tile_n=128, tile_k=256, stages=3,
+                             cols=16, splits=5)),
             ("wide", T(max_rows=64, kind=dep.DEP_KIND_TC_WIDE, ctas=sms, tile_n=256, tile_k=64, stages=4, cols=64)),
             ("cluster-2", T(max_rows=128, kind=dep.DEP_KIND_TC_CLUSTER, ctas=2 * g2, tile_n=256, tile_k=64, stages=5,
                             cols=128, splits=2)),
@@ -51,7 +55,10 @@ def main():
                               tile_k=64, stages=5, cols=256, splits=2)),
         ]
 
-    for N, K, B in [(333, 1000, 5), (97, 264, 33), (1000, 3000, 100), (1024, 2048, 255)]:
+    # K = 2048 and 1088 (multiples of 64) take the one-copy column-block stage
+    # loads, 1088 with a last 256-column stage past the end; the others the
+    # per-slice 2-D loads.
+    for N, K, B in [(333, 1000, 5), (97, 264, 33), (1000, 3000, 100), (1024, 2048, 255), (333, 1088, 16)]:
         x = synth.normal_bf16(N + B, 2, (B, K))
         W = synth.normal_bf16(N + K, 1, (N, K), sigma=0.02)
         ref = oracle.linear(x, W)
