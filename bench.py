@@ -689,7 +689,8 @@ def run_ours(args):
             "timing": "value: K steps back to back, CUDA events at the region's ends only; per_call: "
                       "the same K steps again with every call bracketed by its own events "
                       f"({instrumented_ms / args.steps:.4f} ms per step with those events); graph_pdl_us: "
-                      "a CUDA graph of back-to-back launches of the call with programmatic dependent launch",
+                      "the median of 50 replays of a CUDA graph of back-to-back launches of the call with "
+                      "programmatic dependent launch, at least four distinct weights spanning four L2 sizes rotated",
             "gpu_launches": launches_per_step * args.steps, "per_call": per_call,
             "plan": "tune" if tuned else "default",
             "launch": ("stream launches on plans with programmatic dependent launch (DEP_PLAN_PDL)"
@@ -742,10 +743,11 @@ def probe_ceilings(dep, device):
 def run_graph_per_call(args, dep, calls, x_dev, W_dev, y_dev, flags, peak):
     """Per call, in the deployment's launch mode: a CUDA graph of R back-to-back
     launches of that call on a plan with programmatic dependent launch, the
-    weight rotated over every distinct weight of its shape in the workload,
-    plus copies of them until the rotation spans at least three L2 sizes (so no
-    launch finds its weight in L2, however small the weight), replayed; time
-    per launch."""
+    weight rotated over every distinct weight of its shape in the workload plus
+    copies of them, so that at least four distinct weights spanning at least
+    four L2 sizes rotate (no launch finds its weight in L2, however small the
+    weight); R covers every weight of the rotation (16 at least).  50 replays,
+    each timed on its own; the median replay time per launch."""
     import torch
     keys = {}
     for c in calls:
@@ -759,14 +761,15 @@ def run_graph_per_call(args, dep, calls, x_dev, W_dev, y_dev, flags, peak):
             ws.append(W_dev[c.weight_key])
     l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
     for (N, K), ws in by_shape.items():
-        need = min(16, -(-3 * l2 // (N * K * 2)))
+        need = min(32, max(4, -(-4 * l2 // (N * K * 2))))
         ws += [ws[i % len(ws)].clone() for i in range(max(0, need - len(ws)))]
     lib = dep.lib()
     stream = torch.cuda.Stream()
-    R, reps = 16, 10
+    reps = 50
     out = []
     for i, c in enumerate(calls):
         p, ws = plans[(c.N, c.K)], by_shape[(c.N, c.K)]
+        R = max(16, len(ws))
         x, y = x_dev[i].data_ptr(), y_dev[i].data_ptr()
 
         def launches(sptr):
@@ -785,16 +788,17 @@ def run_graph_per_call(args, dep, calls, x_dev, W_dev, y_dev, flags, peak):
             g.replay()
         torch.cuda.synchronize()
         cur = torch.cuda.current_stream()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(cur)
-        for _ in range(reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        ev[0].record(cur)
+        for r in range(reps):
             g.replay()
-        e1.record(cur)
+            ev[r + 1].record(cur)
         torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (reps * R)
+        per = sorted(ev[r].elapsed_time(ev[r + 1]) for r in range(reps))
+        us = per[reps // 2] * 1e3 / R
         gbs = c.algorithmic_bytes / (us * 1e-6) / 1e9
         out.append({"call": c.name, "us": us, "gbs": gbs, "frac_of_peak": gbs / peak,
-                    "weights_rotated": min(R, len(ws))})
+                    "weights_rotated": min(R, len(ws)), "launches_per_replay": R, "replays": reps})
         del g
     for p in plans.values():
         code = dep.dep_projection_device_status(p)
