@@ -18,6 +18,16 @@
 //    stages of tile_k / 64 slices; accumulators in TMEM, two buffers.  The first
 //    stages are issued by thread 0 right after the barrier set-up, while warp 1
 //    allocates TMEM.
+//  * 64-row tiles at NT <= 32 take slices in pairs when a stage has an even
+//    number of them: an M = 64 MMA costs as long as an M = 128 one, so one
+//    M = 128, N = 2 NT instruction reads slice 2j as A rows 0-63 and slice 2j+1
+//    (the next 8 KB) as rows 64-127, against x slices 2j and 2j+1 as B rows
+//    0..NT-1 and NT..2NT-1.  Lanes 0-63 / columns [0, NT) of D collect the even
+//    slices, lanes 64-127 / columns [NT, 2 NT) the odd ones (the two other
+//    blocks of D are never read).  The epilogue warps of lane quadrants 2-3
+//    hand their sums to those of quadrants 0-1 through shared memory, and a
+//    row's partial is (even slices) + (odd slices), each issuer 0's plus issuer
+//    1's, in FP32: half the instructions per weight byte, same determinism.
 //  * One thread issues a tcgen05.mma about every 67 cycles whatever its M and
 //    N (up to N = 128), which at N <= 64 is less work per instruction than the
 //    tensor pipe can do: a block with one issuer consumes about 60 weight bytes
@@ -70,15 +80,26 @@ struct SplitShape {
     // MMA issuers, each with its own accumulator per buffer: two at N <= 32,
     // the same rule as the stream-K kernel, whose results these must equal.
     static constexpr int ISSUERS = NT <= 32 ? 2 : 1;
-    static constexpr uint32_t TMEM_COLS = 2 * ISSUERS * NT < 32 ? 32 : 2 * ISSUERS * NT;
+    // 64-row tiles at N <= 32 issue slice pairs (when a stage has an even number
+    // of slices): one M = 128, N = 2 NT instruction covers two slices, the even
+    // one in TMEM lanes 0-63 / columns [0, NT), the odd one in lanes 64-127 /
+    // columns [NT, 2 NT).  An M = 64 instruction takes as long as an M = 128
+    // one, so this halves the instructions per weight byte.
+    static constexpr bool PAIRABLE = BM == 64 && NT <= 32;
+    static constexpr int ACC_MAX = PAIRABLE ? 2 * NT : NT;  // accumulator columns
+    static constexpr uint32_t TMEM_COLS = 2 * ISSUERS * ACC_MAX < 32 ? 32 : 2 * ISSUERS * ACC_MAX;
+    // The odd slices' sums pass from the warps reading TMEM lanes 64-127 to the
+    // warps owning the rows: [buffer][lane quadrant pair][column][lane] floats.
+    static constexpr int XFER_BYTES = PAIRABLE ? 2 * 2 * NT * 32 * 4 : 0;
 };
 
-// Shared memory after the 1 KB-aligned ring: full[stages], empty[stages],
-// accf[2], acce[2], tagb[2], done; then the stage tags, the accumulator items,
-// the TMEM address and the abort flag.
-__host__ __device__ inline size_t split_smem_bytes(int stages, int stage_bytes)
+// Shared memory after the 1 KB-aligned ring: the slice-pair hand-off area;
+// full[stages], empty[stages], accf[2], acce[2], tagb[2], done, hand[2][2];
+// then the stage tags, the accumulator items, the TMEM address and the abort flag.
+__host__ __device__ inline size_t split_smem_bytes(int stages, int stage_bytes, int xfer_bytes)
 {
-    return 1024 + (size_t)stages * stage_bytes + (size_t)(2 * stages + 7) * 8 + (size_t)stages * 8 + 16;
+    return 1024 + (size_t)stages * stage_bytes + (size_t)xfer_bytes + (size_t)(2 * stages + 11) * 8 +
+           (size_t)stages * 8 + 16;
 }
 
 __device__ __forceinline__ int piece_begin(int p, int KT, int S)
@@ -106,22 +127,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle tiles need 1 KB alignment
     uint8_t *smem = smem_raw + (base - raw);
-    if (!dbg_ok((base - raw) + split_smem_bytes(stages, STAGE) - 1024 - 1, bd.smem, status))
+    if (!dbg_ok((base - raw) + split_smem_bytes(stages, STAGE, Sh::XFER_BYTES) - 1024 - 1, bd.smem, status))
         return;  // the ring, barriers, tags and TMEM slot must lie in the launch's shared memory
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * STAGE);
+    float *xfer = reinterpret_cast<float *>(smem + (size_t)stages * STAGE);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)stages * STAGE + Sh::XFER_BYTES);
     const uint32_t full0 = smem_u32(bars);
     const uint32_t empty0 = full0 + 8 * stages;
     const uint32_t accf0 = empty0 + 8 * stages;  // accumulator final, 2 buffers
     const uint32_t acce0 = accf0 + 16;           // accumulator drained, 2 buffers
     const uint32_t tagb0 = acce0 + 16;           // accumulator's item published, 2 buffers
     const uint32_t done = tagb0 + 16;            // all MMAs complete
-    int2 *tags = reinterpret_cast<int2 *>(bars + 2 * stages + 7);  // (item, flags); item < 0: end
+    const uint32_t hand0 = done + 8;             // odd-slice sums handed over, [buffer][quadrant pair]
+    int2 *tags = reinterpret_cast<int2 *>(bars + 2 * stages + 11);  // (item, flags); item < 0: end
     volatile int *acc_item = reinterpret_cast<volatile int *>(tags + stages);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tags + stages) + 2;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int T = (N + BM - 1) / BM, KT = (K + KG - 1) / KG, I = T * S;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool pair = Sh::PAIRABLE && (atoms & 1) == 0;  // slice-pair MMAs
+    const int ACC = pair ? 2 * NT : NT;                   // columns of one accumulator
     int *grab = dispenser, *finished = dispenser + 1;
 
     // Producer state; the producer is thread 0 (warp 0, lane 0).
@@ -165,6 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tagb0 + 8 * b, 1);
         }
         mbar_init(done, Sh::ISSUERS);
+        for (int h = 0; h < 4; ++h)
+            mbar_init(hand0 + 8 * h, 32);
         *abort_flag = 0;
         fence_mbar_init();
         griddep_launch_dependents();
@@ -256,8 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stage's steps / issuers) into its own accumulator of each buffer.
         const int mi = warp - 1;
         if (lane == 0 && mi < Sh::ISSUERS) {
-            constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, NT);
-            const int H = atoms * (kBK / kUmmaK) / Sh::ISSUERS;
+            constexpr uint32_t idesc1 = tc::idesc_bf16_f32(BM, NT);
+            constexpr uint32_t idesc2 = Sh::PAIRABLE ? tc::idesc_bf16_f32(128, 2 * NT) : idesc1;
+            const uint32_t idesc = pair ? idesc2 : idesc1;
+            // K steps of a stage: 4 per slice, or per slice pair
+            const int H = (pair ? atoms / 2 : atoms) * (kBK / kUmmaK) / Sh::ISSUERS;
             int s = 0, buf = 0;
             uint32_t ph = 0, acce_ph = 0;
             uint32_t accumulate = 0;
@@ -288,10 +318,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     break;
                 }
-                const uint32_t d = tmem + (uint32_t)((buf * Sh::ISSUERS + mi) * NT);
+                const uint32_t d = tmem + (uint32_t)((buf * Sh::ISSUERS + mi) * ACC);
                 const uint32_t st = base + (uint32_t)(s * STAGE);
-                tc::mma_stage<Sh::A_BYTES, Sh::B_BYTES>(d, st, st + (uint32_t)(atoms * Sh::A_BYTES), mi * H, H, idesc,
-                                                        accumulate);
+                if (pair)  // step i: slices 2 (i / 4) and 2 (i / 4) + 1 at K offset 16 (i % 4)
+                    tc::mma_stage<2 * Sh::A_BYTES, 2 * Sh::B_BYTES>(d, st, st + (uint32_t)(atoms * Sh::A_BYTES), mi * H,
+                                                                    H, idesc, accumulate);
+                else
+                    tc::mma_stage<Sh::A_BYTES, Sh::B_BYTES>(d, st, st + (uint32_t)(atoms * Sh::A_BYTES), mi * H, H,
+                                                            idesc, accumulate);
                 tc::commit(empty0 + 8 * s);  // the stage is free once both issuers' MMAs finish
                 if (++s == stages) {
                     s = 0;
@@ -315,10 +349,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         griddep_wait();  // the exchange words and y may still be in use by the preceding grid
         const int q = warp & 3;  // TMEM lane quadrant this warp may access
         // M = 128: tile row r is TMEM lane r.  M = 64: rows 16q..16q+15 are lanes
-        // 0-15 of quadrant q (lanes 16-31 hold nothing of this MMA).
-        const int row = BM == 128 ? 32 * q + lane : 16 * q + lane;
-        const bool has_row = BM == 128 || lane < 16;
-        uint32_t tag_ph = 0, accf_ph = 0;
+        // 0-15 of quadrant q (lanes 16-31 hold nothing of this MMA).  Slice pairs:
+        // row r is lane r (even slices) and lane 64 + r (odd slices); quadrants 0-1
+        // own the rows, quadrants 2-3 hand their sums to them.
+        const bool odd = pair && q >= 2;
+        const int row = pair ? 32 * (q & 1) + lane : (BM == 128 ? 32 * q + lane : 16 * q + lane);
+        const bool has_row = pair ? !odd : (BM == 128 || lane < 16);
+        uint32_t tag_ph = 0, accf_ph = 0, hand_ph = 0;
         int buf = 0;
         for (;;) {
             if (!mbar_wait(tagb0 + 8 * buf, (tag_ph >> buf) & 1u, limit_ns)) {
@@ -340,8 +377,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int t = item / S, piece = item % S;
             const int64_t n = (int64_t)t * BM + row;
             const bool mine = has_row && n < N;  // this lane's output row exists
-            // buffer buf's accumulators: issuer 0's, then issuer 1's (NT columns each)
-            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * Sh::ISSUERS * NT);
+            // buffer buf's accumulators: issuer 0's, then issuer 1's (ACC columns each)
+            const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * Sh::ISSUERS * ACC);
+            float *hand = xfer + (size_t)(2 * buf + (q & 1)) * NT * 32 + lane;  // [column][lane]
+            const uint32_t hand_bar = hand0 + 8 * (uint32_t)(2 * buf + (q & 1));
+            if (odd) {
+                // Columns [NT, 2 NT) of lanes 64-127: the odd slices' sums, issuer
+                // 0's plus issuer 1's, handed to the warp that owns these rows.
+#pragma unroll 1
+                for (int c0 = 0; c0 < NT && c0 < B; c0 += 16) {
+                    __syncwarp();
+                    uint32_t v[16], v1[16];
+                    tc::ld16(taddr + (uint32_t)(NT + c0), v);
+                    tc::ld16(taddr + (uint32_t)(ACC + NT + c0), v1);
+                    tc::wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        hand[(c0 + j) * 32] = __uint_as_float(v[j]) + __uint_as_float(v1[j]);
+                }
+                mbar_arrive(hand_bar);
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(acce0 + 8 * buf);
+                buf ^= 1;
+                continue;
+            }
+            if (pair) {
+                if (!mbar_wait(hand_bar, (hand_ph >> buf) & 1u, limit_ns)) {
+                    record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
+                    *abort_flag = 1;
+                    break;
+                }
+                hand_ph ^= 1u << buf;
+            }
             // tile t's exchange words, [piece][b][row]
             unsigned long long *tile_x = xch + (int64_t)t * S * NT * BM + row;
             bool ok = true;
@@ -351,12 +420,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[16], v1[16];
                 tc::ld16(taddr + (uint32_t)c0, v);
                 if (Sh::ISSUERS == 2)
-                    tc::ld16(taddr + (uint32_t)(NT + c0), v1);
+                    tc::ld16(taddr + (uint32_t)(ACC + c0), v1);
                 tc::wait_ld();
                 if (Sh::ISSUERS == 2) {  // the block's partial: issuer 0's half of K, then issuer 1's
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
                         v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+                }
+                if (pair) {  // (even slices) + (odd slices), each issuer 0 + issuer 1
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) + hand[(c0 + j) * 32]);
                 }
                 if (S == 1) {
 #pragma unroll
@@ -412,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int NT, int BM>
 size_t smem_bytes(int stages, int atoms)
 {
-    return split_smem_bytes(stages, atoms * SplitShape<NT, BM>::ATOM);
+    return split_smem_bytes(stages, atoms * SplitShape<NT, BM>::ATOM, SplitShape<NT, BM>::XFER_BYTES);
 }
 
 template <int NT, int BM>
