@@ -175,12 +175,15 @@ dep_status_t dep_projection_run_tactic(dep_plan_t plan, const dep_tactic_t *tact
  * the plan's largest table key (the staging capacity).  Errors as
  * dep_projection_run.
  *   - Pinned host buffers (mapped into the device's address space, 16-byte
- *     aligned): two small kernels read x_host and write y_host directly
- *     (zero-copy), chained to the projection by programmatic dependent launch,
- *     so the projection streams its first weight stages while x arrives and
- *     consecutive calls leave no launch gap.  Stream order holds as for
- *     memcpys: each copy reads only after the preceding work in the stream has
- *     completed, so one call's y_host may be the next call's x_host.
+ *     aligned): a small kernel reads x_host directly (zero-copy) into the
+ *     staging buffer, chained to the projection by programmatic dependent
+ *     launch, so the projection streams its first weight stages while x
+ *     arrives and consecutive calls leave no launch gap.  The projection
+ *     stores y straight into y_host, except the cluster kind
+ *     (DEP_KIND_TC_CLUSTER), whose y a second small kernel copies back.
+ *     Stream order holds as for memcpys: each copy reads only after the
+ *     preceding work in the stream has completed, so one call's y_host may be
+ *     the next call's x_host.
  *   - Any other host memory: cudaMemcpyAsync both ways.
  *   Both give the same bits as dep_projection_run.  The environment variable
  *   DEP_STAGING=copy forces the copy path (for comparisons).

@@ -870,11 +870,17 @@ dep_status_t dep_projection_run_host(dep_plan_t plan, const void *x_host, const 
         }
         // The projection may start while the gather runs: it streams W first and
         // reads x only after waiting for the gather (the gather does not write W).
-        dep_status_t st = run_impl(plan, t, plan->x_stage, W, plan->y_stage, B, stream, true);
+        // Kernels that store y with plain stores write it straight into the
+        // mapped y_host (one kernel and one dependent-launch hop fewer per call);
+        // the cluster kernel stores y by bulk tensor copies from shared memory
+        // into device memory, and a copy kernel takes it back.
+        const bool direct = t && t->kind != DEP_KIND_TC_CLUSTER;
+        dep_status_t st = run_impl(plan, t, plan->x_stage, W, direct ? ay.devicePointer : plan->y_stage, B, stream,
+                                   true);
         if (st != DEP_OK)
             return st;
-        if (dep::stage_copy(plan->y_stage, static_cast<uint16_t *>(ay.devicePointer), (size_t)B * plan->N, true,
-                            s) != cudaSuccess) {
+        if (!direct && dep::stage_copy(plan->y_stage, static_cast<uint16_t *>(ay.devicePointer), (size_t)B * plan->N,
+                                       true, s) != cudaSuccess) {
             cudaGetLastError();
             return DEP_ERR_CUDA;
         }

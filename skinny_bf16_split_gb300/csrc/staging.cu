@@ -1,8 +1,10 @@
 // staging.cu -- zero-copy staging of x and y for the host-buffer entry point.
 //
 // When the caller's host buffers are pinned (mapped into the device's address
-// space), x is gathered into the plan's device staging area and y written back
-// by two small kernels instead of two memcpys.  Chained by programmatic
+// space), x is gathered into the plan's device staging area by a small kernel
+// instead of a memcpy; the projection stores y into the mapped buffer itself,
+// or (the cluster kind, whose y leaves by bulk tensor stores) writes the staging
+// area and the same kernel copies y back.  Chained by programmatic
 // dependent launch: each copy triggers its dependents at once and waits for
 // the preceding grid before it reads (so a source written by earlier work in
 // the stream is complete, and the staging area is no longer read by an earlier

@@ -244,12 +244,14 @@ def test_argument_errors_on_device(dep, plan_cache):
     assert e.value.status == dep.DEP_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("B,N", [(5, 640), (1, 333), (16, 7168), (40, 1001)])
+@pytest.mark.parametrize("B,N", [(5, 640), (1, 333), (16, 7168), (40, 1001), (255, 14561)])
 @pytest.mark.parametrize("memory", ["pinned", "pageable", "pinned-copy"])
 def test_run_host_end_to_end(dep, orc, plan_cache, monkeypatch, B, N, memory):
     """The host-buffer entry point gives the device entry point's bits: pinned
-    buffers through the zero-copy staging kernels (chained by programmatic
-    dependent launch, N odd included: a 2-byte tail), pageable buffers and
+    buffers through the zero-copy gather, y stored by the projection or (the
+    cluster kind, B = 40 and 255) copied back by the staging kernel, chained by
+    programmatic dependent launch (N odd included: a 2-byte tail; B = 255: a
+    7.4 MB y, several 16-byte vectors per copying thread), pageable buffers and
     DEP_STAGING=copy through memcpys.  Ten calls back to back, one sync."""
     K = 2048
     plan = get_plan(dep, plan_cache, N, K)
@@ -272,14 +274,16 @@ def test_run_host_end_to_end(dep, orc, plan_cache, monkeypatch, B, N, memory):
     assert dep.dep_projection_device_status(plan) == 0
 
 
-@pytest.mark.parametrize("B", [4, 16])
+@pytest.mark.parametrize("B", [4, 16, 64])
 def test_run_host_chain_through_pinned_buffers(dep, plan_cache, B):
     """Calls chained through the host buffers with no synchronisation between
     them: each call's pinned output is the next call's pinned input.  The
     zero-copy gather of a call, launched with the programmatic attribute, must
-    still see the write-back of the call before it (it reads only after the
-    preceding grid has completed): the chain gives the bits of the same chain
-    run one synchronised call at a time."""
+    still see the y of the call before it, stored into the pinned buffer by the
+    projection itself (B = 4, 16) or copied back by the staging kernel (B = 64,
+    the cluster kind); it reads only after the preceding grid has completed.
+    The chain gives the bits of the same chain run one synchronised call at a
+    time."""
     N = K = 2048
     plan = get_plan(dep, plan_cache, N, K)
     W = synth.normal_bf16(130, 1, (N, K), sigma=0.02)
@@ -298,9 +302,10 @@ def test_run_host_chain_through_pinned_buffers(dep, plan_cache, B):
 
 def test_run_host_captured_in_a_graph(dep, plan_cache):
     """The host-buffer entry point with pinned buffers inside a CUDA graph: the
-    zero-copy gather, the projection and the write-back (chained by programmatic
-    dependent launch) replay with new inputs written into the same pinned
-    buffers, and every replay gives the device entry point's bits."""
+    zero-copy gather and the projection that stores y into the pinned buffer
+    (chained by programmatic dependent launch) replay with new inputs written
+    into the same pinned buffers, and every replay gives the device entry
+    point's bits."""
     N, K, B = 7168, 4096, 8
     plan = get_plan(dep, plan_cache, N, K)
     W = synth.normal_bf16(120, 1, (N, K), sigma=0.02)
