@@ -90,6 +90,14 @@ typedef enum {
                                  shared memory (no global workspace); `stages` =
                                  weight stages (x has its own 2-4 stage ring);
                                  `ctas` = a multiple of k; tile_k = 64 */
+#define DEP_KIND_TC_XM 7      /* tcgen05 MMA for wide batches with x on the MMA's M
+                                 side: blocks of 128 batch rows (cols = 128 or 256:
+                                 one or two per pass) against tiles of tile_n weight
+                                 rows (MMA N, a multiple of 16 up to 256), dealt out
+                                 statically over `ctas` blocks; each block sums its
+                                 tiles' whole K (no split, no workspace); `stages`
+                                 = weight stages of tile_k = 64, 128 or 256 columns
+                                 (x has its own ring of 64-column slices) */
 
 /* One table entry: the tactic that serves batches of up to max_rows rows. */
 typedef struct {
@@ -99,10 +107,11 @@ typedef struct {
                          evenly, stream-K; ROWS/TC_SPLIT: work items taken
                          dynamically) */
     int32_t tile_n;   /* weight rows per tile (TC_WIDE: per group, 256 or 512;
-                         TC_CLUSTER: per group, 192, 256 or 512) */
+                         TC_CLUSTER: per group, 192, 256 or 512; TC_XM: MMA N) */
     int32_t tile_k;   /* reduction columns per pipeline stage */
     int32_t stages;   /* pipeline depth (shared-memory stages) */
-    int32_t cols;     /* batch rows per pass (FMA/ROWS: x rows held; TC: MMA N) */
+    int32_t cols;     /* batch rows per pass (FMA/ROWS: x rows held; TC: MMA N;
+                         TC_XM: 128 or 256, MMA M = 128 per block of rows) */
     int32_t splits;   /* TC_SPLIT: K pieces per tile, 1..64 (capped at the tile's
                          k-tiles, ceil(K / tile_k)); 0 for the other kinds */
 } dep_tactic_t;

@@ -80,6 +80,8 @@ bool tactic_valid(const dep_tactic_t &t)
         return dep::wide_valid(t);
     if (t.kind == DEP_KIND_TC_CLUSTER)
         return dep::cluster_valid(t);
+    if (t.kind == DEP_KIND_TC_XM)
+        return dep::xm_valid(t);
     if (t.splits != 0)
         return false;  // only the K-piece tactic has pieces
     if (t.kind == DEP_KIND_SPLITK_FMA)
@@ -106,6 +108,7 @@ int64_t effective_ctas(const dep_tactic_t &t, int64_t N, int64_t K)
     const int64_t U = t.kind == DEP_KIND_SPLITK_FMA ? dep::fma_units(t, N, K)
                       : t.kind == DEP_KIND_TC       ? dep::tc_units(t, N, K)
                       : t.kind == DEP_KIND_TC_WIDE  ? dep::wide_units(t, N, K)
+                      : t.kind == DEP_KIND_TC_XM    ? dep::xm_tiles(t, N)
                                                     : dep::rows_tiles(t, N);
     return U < t.ctas ? U : t.ctas;
 }
@@ -159,6 +162,7 @@ size_t tactic_counters(const dep_tactic_t &t, int64_t N, int64_t K)
     case DEP_KIND_TC: return 0;  // the exchange words need no counters
     case DEP_KIND_TC_WIDE: return (size_t)effective_ctas(t, N, K) * dep::wide_flags_per_cta(t);  // flags
     case DEP_KIND_TC_CLUSTER: return 0;  // partials stay in the cluster's shared memory
+    case DEP_KIND_TC_XM: return 0;       // whole K per block: no partials, no counters
     case DEP_KIND_TC_SPLIT: return dep::tcs_counters(t, N);
     default: return 2;  // tile dispenser and finish count (the last two counters)
     }
@@ -234,6 +238,25 @@ dep_tactic_t cluster_tactic(int32_t rows, int32_t cols, int32_t groups_of_tiles,
     return t;
 }
 
+dep_tactic_t xm_tactic(int32_t rows, int32_t cols, int32_t tile_n, int32_t tile_k, int32_t stages, int32_t ctas)
+{
+    dep_tactic_t t = tc_tactic(rows, cols, stages, ctas, tile_k);
+    t.kind = DEP_KIND_TC_XM;
+    t.tile_n = tile_n;
+    return t;
+}
+
+// Weight rows per tile of the x-on-M kind: the smallest multiple of 16 that
+// deals the rows out in as few waves of the SMs as tiles of at most 128 rows
+// allow (128 keeps two accumulator buffers in TMEM).  DSA 14560: 96 (152
+// tiles); KDA 49376: 112 (441 tiles, three waves); o_proj 7168: 48 (150).
+int32_t xm_rows_per_tile(int64_t N, int sm_count)
+{
+    const int64_t waves = std::max<int64_t>(1, (N + 128 * (int64_t)sm_count - 1) / (128 * (int64_t)sm_count));
+    const int64_t per = (N + waves * sm_count - 1) / (waves * sm_count);
+    return (int32_t)std::max<int64_t>(16, (per + 15) / 16 * 16);
+}
+
 // Deepest pipeline of the tensor-core kernel that fits in shared memory.
 int32_t tc_default_stages(int32_t cols)
 {
@@ -274,6 +297,29 @@ dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
     }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128, t64 = (N + 63) / 64;
+    // 17 to 256 batch rows: x on the MMA's M side (tc_xm.cu) against tiles of
+    // R weight rows that fill the SMs, no K split, where the x bytes of a
+    // 64-column step are at most 1.5x the weight's (x rows padded to 64, 128 or
+    // 256).  Stages of four 64-column slices where three of them fit beside x
+    // of 64 rows, two slices otherwise, as many as fit.  Measured on GB300 per
+    // call (CUDA graph + PDL, weights past L2): DSA 14560 x 7168 B = 32 / 64 /
+    // 128: 32.4 / 32.6 / 33.4 us against 33.1 / 35.9 / 39.7 us for the stream-K
+    // and cluster kinds; KDA 49376 x 7168 B = 64 / 128: 100.8 / 107.6 against
+    // 108.4 / 112.5 us; o_proj 7168 x 12288 B = 32 / 64: 28.8 / 28.8 against
+    // 29.5 / 33.1 us.  Not at 256 rows (DSA 50.7 against 45.7 us for the cluster
+    // kind) nor o_proj at 128 (38.2 against 36.4 us): x bytes dominate there.
+    if (rows > 16 && rows <= 256) {
+        const int32_t R = xm_rows_per_tile(N, sm_count);
+        const int32_t xrows = rows <= 64 ? 64 : (rows <= 128 ? 128 : 256);
+        const int32_t xcols = rows <= 128 ? 128 : 256;  // one or two blocks of 128 rows per pass
+        if (R <= 256 && 2 * xrows <= 3 * R) {
+            const int32_t xr = rows <= 64 ? 64 : 128;
+            const int32_t tk = dep::xm_stages_fit(R, 256, xcols, xr) >= 3 ? 256 : 128;
+            const int32_t st = dep::xm_stages_fit(R, tk, xcols, 128);  // the tactic's depth is at 128 rows
+            if (st >= 2)
+                return xm_tactic(rows, xcols, R, tk, st, sm_count);
+        }
+    }
     // Up to 32 batch rows on long weight rows (K >= 3072) whose 64-row tiles fit
     // on the SMs: 64-row K-piece tiles in as few pieces as fill the SMs (o_proj:
     // 112 tiles, one piece each, no exchange).  Measured on GB300 per call (CUDA
@@ -497,7 +543,7 @@ dep_status_t make_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_b
         }
         if (dep::fma_prepare_device() != cudaSuccess || dep::tc_prepare_device() != cudaSuccess ||
             dep::tcs_prepare_device() != cudaSuccess || dep::wide_prepare_device() != cudaSuccess ||
-            dep::cluster_prepare_device() != cudaSuccess ||
+            dep::cluster_prepare_device() != cudaSuccess || dep::xm_prepare_device() != cudaSuccess ||
             dep::rows_prepare_device() != cudaSuccess) {
             cudaGetLastError();
             delete p;
@@ -574,6 +620,7 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
                     : t->kind == DEP_KIND_TC_SPLIT ? dep::tcs_run(*t, a)
                     : t->kind == DEP_KIND_TC_WIDE  ? dep::wide_run(*t, a)
                     : t->kind == DEP_KIND_TC_CLUSTER ? dep::cluster_run(*t, a)
+                    : t->kind == DEP_KIND_TC_XM    ? dep::xm_run(*t, a)
                                                    : dep::rows_run(*t, a);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -659,6 +706,27 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
                     t.tile_n = grows;
                     c.push_back(t);
                 }
+    // x on the MMA's M side: tiles of 16..256 weight rows (the default's R and
+    // its neighbours, and the multiples of 16 that fill the SMs in one, two or
+    // three waves), two or four slices per stage, every depth that fits.
+    if (rows > 16) {
+        const int32_t xcols = rows <= 128 ? 128 : 256;
+        std::vector<int32_t> rs;
+        const int32_t r0 = xm_rows_per_tile(N, sm_count);
+        for (int32_t r : {r0 - 16, r0, r0 + 16, r0 + 32})
+            rs.push_back(r);
+        for (int64_t w : {1, 2, 3}) {
+            const int64_t per = (N + w * sm_count - 1) / (w * sm_count);
+            rs.push_back((int32_t)((per + 15) / 16 * 16));
+        }
+        std::sort(rs.begin(), rs.end());
+        rs.erase(std::unique(rs.begin(), rs.end()), rs.end());
+        for (int32_t r : rs)
+            for (int32_t tk : {128, 256})
+                for (int32_t st : {2, 3, 4, 5, 6})
+                    if (r >= 16 && r <= 256)
+                        c.push_back(xm_tactic(rows, xcols, r, tk, st, sm_count));
+    }
     // K pieces keep every piece's partial: leave out tactics whose exchange words
     // would take more than 64 MB.
     constexpr size_t kMaxPieceWords = (64u << 20) / 8;

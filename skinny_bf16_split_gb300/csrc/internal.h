@@ -86,6 +86,7 @@ cudaError_t rows_prepare_device();
 cudaError_t tcs_prepare_device();
 cudaError_t wide_prepare_device();
 cudaError_t cluster_prepare_device();
+cudaError_t xm_prepare_device();
 
 // Launch with the programmatic-stream-serialisation attribute when `pdl` is set.
 template <typename Kernel, typename... Args>
@@ -204,6 +205,15 @@ cudaError_t wide_run(const dep_tactic_t &t, const RunArgs &a);
 // ---- tcgen05 tactic for wide batches, a cluster of CTAs per group (tc_cluster.cu) ----
 bool cluster_valid(const dep_tactic_t &t);
 cudaError_t cluster_run(const dep_tactic_t &t, const RunArgs &a);
+
+// ---- tcgen05 tactic for wide batches, x on the MMA's M side (tc_xm.cu) ----
+bool xm_valid(const dep_tactic_t &t);
+int64_t xm_tiles(const dep_tactic_t &t, int64_t N);
+// Deepest ring (2..16 stages, 0 if none) of tiles of tile_n weight rows, stages
+// of tile_k columns and cols = 128 or 256 batch rows per pass, when the pass's
+// x blocks have mr = 64 or 128 rows.
+int xm_stages_fit(int32_t tile_n, int32_t tile_k, int32_t cols, int mr);
+cudaError_t xm_run(const dep_tactic_t &t, const RunArgs &a);
 
 // ---- whole-row tactic (rows_gemv.cu) ----
 bool rows_valid(const dep_tactic_t &t);

@@ -53,6 +53,10 @@ def main():
                             stages=4, cols=256, splits=3)),
             ("cluster-192", T(max_rows=512, kind=dep.DEP_KIND_TC_CLUSTER, ctas=2 * -(-N // 192), tile_n=192,
                               tile_k=64, stages=5, cols=256, splits=2)),
+            ("x-on-m", T(max_rows=1024, kind=dep.DEP_KIND_TC_XM, ctas=7, tile_n=48, tile_k=128, stages=3,
+                         cols=128)),
+            ("x-on-m-2", T(max_rows=2048, kind=dep.DEP_KIND_TC_XM, ctas=sms, tile_n=96, tile_k=64, stages=3,
+                           cols=256)),
         ]
 
     # K = 2048 and 1088 (multiples of 64) take the one-copy column-block stage

@@ -72,7 +72,7 @@ def test_default_many_tiles_take_three_pieces(dep):
         kinds = {t.max_rows: (t.kind, t.splits) for t in dep.dep_projection_plan_table(plan)}
         assert kinds[1] == (dep.DEP_KIND_ROWS, 0)
         assert kinds[4] == kinds[16] == (dep.DEP_KIND_TC_SPLIT, 3)  # 386 tiles > 152 SMs
-        assert kinds[32] == (dep.DEP_KIND_TC, 0)
+        assert kinds[32] == (dep.DEP_KIND_TC_XM, 0)  # x on the MMA's M side, tiles of 112 rows
     finally:
         dep.dep_projection_plan_destroy(plan)
 
@@ -84,49 +84,42 @@ def test_default_batches_when_none_given(dep):
         assert [t.max_rows for t in table] == [1, 2, 4, 8, 16, 32, 64, 128, 256]
         # 114 tiles of 128 rows nearly fill 152 SMs: whole tiles, one per block
         assert all((t.kind, t.splits) == (dep.DEP_KIND_TC_SPLIT, 1) for t in table if 2 < t.max_rows <= 16)
-        # 32 and 64 rows: one 128-row tile per block (114 tiles), no K split
-        assert all((t.kind, t.ctas) == (dep.DEP_KIND_TC, 114) for t in table if t.max_rows in (32, 64))
-        # 128 rows: 57 groups of two tiles, a cluster of two CTAs each; 256 rows:
-        # 76 groups of 192 rows (a 128-row and a 64-row tile), 152 CTAs
-        wide = [t for t in table if t.max_rows == 128]
-        assert all((t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, 256, 2, 114) for t in wide)
+        # 32 to 128 rows: x on the MMA's M side against 152 tiles of 96 weight rows
+        xm = [t for t in table if 32 <= t.max_rows <= 128]
+        assert all((t.kind, t.tile_n, t.cols, t.ctas, t.splits) == (dep.DEP_KIND_TC_XM, 96, 128, 152, 0)
+                   for t in xm)
+        # 256 rows: 76 groups of 192 rows (a 128-row and a 64-row tile), a cluster
+        # of two CTAs each, 152 CTAs
         t = table[-1]
         assert (t.max_rows, t.kind, t.tile_n, t.splits, t.ctas) == (256, dep.DEP_KIND_TC_CLUSTER, 192, 2, 152)
     finally:
         dep.dep_projection_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("N,sms,expect", [
-    (7168, 152, (256, 4, 112)),    # o_proj: 28 groups, clusters of four
-    (14560, 152, (256, 2, 114)),   # DSA: 57 groups, clusters of two
-    (49376, 152, None),            # KDA: 193 groups do not fit in one wave (see below)
-    (1000, 8, (256, 2, 8)),        # 4 groups on 8 SMs
+@pytest.mark.parametrize("N,sms,xm_rows,cluster", [
+    (7168, 152, {64: 48}, {128: (256, 4, 112), 256: (256, 4, 112)}),  # o_proj: x dominates at 128 rows
+    (14560, 152, {64: 96, 128: 96}, {256: (192, 2, 152)}),             # DSA: 152 tiles of 96 rows
+    (49376, 152, {64: 112, 128: 112}, {256: (256, 2, 152)}),           # KDA: 441 tiles, three waves
+    (1000, 8, {64: 128, 128: 128}, {256: (256, 2, 8)}),                # 8 tiles of 128 rows on 8 SMs
 ])
-def test_default_rule_wide_batches(dep, N, sms, expect):
-    """The default rule for 64-256 rows: a cluster of k = SMs / groups (at most
+def test_default_rule_wide_batches(dep, N, sms, xm_rows, cluster):
+    """The default rule for 64-256 rows: x on the MMA's M side (tiles of R weight
+    rows, the smallest multiple of 16 that fills the SMs in as few waves as
+    tiles of at most 128 rows allow) wherever x's bytes per 64-column step are
+    at most 1.5x the weight's; otherwise a cluster of k = SMs / groups (at most
     4) CTAs per group of two 128-row tiles while the groups fit on the SMs in
-    clusters of two; otherwise clusters of two at 256 rows, groups of four tiles
-    one CTA each at 128 rows if they fit, the one-tile stream-K kernel else.  At
-    64 rows, where the 128-row tiles nearly fill the SMs, one tile per block of
-    the stream-K kernel."""
+    clusters of two, clusters of two at 256 rows, and on DSA's 14560 rows groups
+    of 192 (a 128-row and a 64-row tile)."""
     plan = dep.dep_projection_plan_host(N, 7168, [64, 128, 256], sms)
     try:
         table = {t.max_rows: t for t in dep.dep_projection_plan_table(plan)}
-        if expect is not None:
-            for b in (64, 128, 256):
-                t = table[b]
-                if b == 256 and N == 14560:  # 76 groups of 192 rows fill the SMs
-                    assert (t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, 192, 2, 152), t
-                    continue
-                if b == 64 and 4 * -(-N // 128) >= 3 * sms:  # 128-row tiles nearly fill the SMs
-                    assert (t.kind, t.ctas) == (dep.DEP_KIND_TC, -(-N // 128)), t
-                    continue
-                assert (t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, *expect), (b, t)
-        else:
-            assert (table[256].kind, table[256].splits, table[256].ctas) == (dep.DEP_KIND_TC_CLUSTER, 2, 152)
-            assert (table[128].kind, table[128].tile_n, table[128].splits, table[128].ctas) == \
-                (dep.DEP_KIND_TC_CLUSTER, 512, 1, 97)
-            assert table[64].kind == dep.DEP_KIND_TC
+        for b, R in xm_rows.items():
+            t = table[b]
+            assert (t.kind, t.tile_n, t.cols, t.ctas, t.splits) == (dep.DEP_KIND_TC_XM, R, 128, sms, 0), (b, t)
+            assert 2 * (64 if b <= 64 else 128) <= 3 * R
+        for b, (rows, k, ctas) in cluster.items():
+            t = table[b]
+            assert (t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, rows, k, ctas), (b, t)
     finally:
         dep.dep_projection_plan_destroy(plan)
 

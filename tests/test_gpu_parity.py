@@ -399,13 +399,13 @@ def test_tc_parity_vs_oracle(dep, orc, plan_cache, N, K, NT, tile_k):
 def test_tc_determinism_and_graph_replay(dep, plan_cache, B, which):
     """The tensor-core kernels' split-K combinations are order-fixed: repeated
     runs and CUDA-graph replays give identical bits (the default plan takes the
-    K-piece kernel for this weight up to 16 rows and clusters of CTAs past them;
-    the stream-K kernel is installed explicitly)."""
+    K-piece kernel for this weight up to 16 rows and x on the MMA's M side at 64
+    rows; the stream-K kernel is installed explicitly)."""
     N, K = 7168, 4096
     x, W = to_dev(synth.normal_bf16(B, 2, (B, K))), to_dev(synth.normal_bf16(5, 1, (N, K), 0.02))
     if which == "default":
         plan = get_plan(dep, plan_cache, N, K)
-        want = dep.DEP_KIND_TC_SPLIT if B <= 16 else dep.DEP_KIND_TC_CLUSTER
+        want = dep.DEP_KIND_TC_SPLIT if B <= 16 else dep.DEP_KIND_TC_XM
         assert dep.dep_projection_plan_query(plan, B).kind == want
     else:
         plan = get_plan(dep, plan_cache, N, K, (B,))
