@@ -94,10 +94,14 @@ typedef enum {
                                  side: blocks of 128 batch rows (cols = 128 or 256:
                                  one or two per pass) against tiles of tile_n weight
                                  rows (MMA N, a multiple of 16 up to 256), dealt out
-                                 statically over `ctas` blocks; each block sums its
-                                 tiles' whole K (no split, no workspace); `stages`
-                                 = weight stages of tile_k = 64, 128 or 256 columns
-                                 (x has its own ring of 64-column slices) */
+                                 statically over `ctas` blocks; splits = 0: each
+                                 block sums its tiles' whole K; splits = 2: a
+                                 thread-block cluster of two per tile (tile_n a
+                                 multiple of 32, ctas even), each half of K, the
+                                 halves added in order through distributed shared
+                                 memory; no workspace either way; `stages` of
+                                 tile_k = 64, 128 or 256 columns of the weight and
+                                 of x */
 
 /* One table entry: the tactic that serves batches of up to max_rows rows. */
 typedef struct {
@@ -113,7 +117,8 @@ typedef struct {
     int32_t cols;     /* batch rows per pass (FMA/ROWS: x rows held; TC: MMA N;
                          TC_XM: 128 or 256, MMA M = 128 per block of rows) */
     int32_t splits;   /* TC_SPLIT: K pieces per tile, 1..64 (capped at the tile's
-                         k-tiles, ceil(K / tile_k)); 0 for the other kinds */
+                         k-tiles, ceil(K / tile_k)); TC_CLUSTER: CTAs per cluster;
+                         TC_XM: 0, or 2 for pairs of blocks; 0 for the other kinds */
 } dep_tactic_t;
 
 /* Plan flags. */
@@ -188,14 +193,16 @@ dep_status_t dep_projection_run_tactic(dep_plan_t plan, const dep_tactic_t *tact
  *     staging buffer, chained to the projection by programmatic dependent
  *     launch, so the projection streams its first weight stages while x
  *     arrives and consecutive calls leave no launch gap.  The projection
- *     stores y straight into y_host, except the cluster kind
- *     (DEP_KIND_TC_CLUSTER), whose y a second small kernel copies back.
+ *     stores y straight into y_host, except the cluster and x-on-M kinds
+ *     (DEP_KIND_TC_CLUSTER, DEP_KIND_TC_XM), whose y a second small kernel
+ *     copies back from the staging buffer.
  *     Stream order holds as for memcpys: each copy reads only after the
  *     preceding work in the stream has completed, so one call's y_host may be
  *     the next call's x_host.
  *   - Any other host memory: cudaMemcpyAsync both ways.
  *   Both give the same bits as dep_projection_run.  The environment variable
- *   DEP_STAGING=copy forces the copy path (for comparisons).
+ *   DEP_STAGING=copy forces the copy path, DEP_STAGING=stage the copy-back of
+ *   y for every kind (both for comparisons).
  */
 dep_status_t dep_projection_run_host(dep_plan_t plan, const void *x_host, const void *W,
                                      void *y_host, int32_t B, void *stream);

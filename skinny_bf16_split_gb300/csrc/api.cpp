@@ -257,6 +257,18 @@ int32_t xm_rows_per_tile(int64_t N, int sm_count)
     return (int32_t)std::max<int64_t>(16, (per + 15) / 16 * 16);
 }
 
+// Weight rows per tile of the x-on-M kind in pairs of blocks (a cluster of two,
+// each half of K): the smallest multiple of 32 that deals the rows out to the
+// SMs / 2 pairs in as few waves as tiles of at most 256 rows allow.  DSA 14560:
+// 192 (76 tiles); o_proj 7168: 96 (75); KDA 49376: 224 (221 tiles, three waves).
+int32_t xm_pair_rows_per_tile(int64_t N, int sm_count)
+{
+    const int64_t pairs = std::max(1, sm_count / 2);
+    const int64_t waves = std::max<int64_t>(1, (N + 256 * pairs - 1) / (256 * pairs));
+    const int64_t per = (N + waves * pairs - 1) / (waves * pairs);
+    return (int32_t)std::max<int64_t>(32, (per + 31) / 32 * 32);
+}
+
 // Deepest pipeline of the tensor-core kernel that fits in shared memory.
 int32_t tc_default_stages(int32_t cols)
 {
@@ -298,27 +310,44 @@ dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128, t64 = (N + 63) / 64;
     // 17 to 256 batch rows: x on the MMA's M side (tc_xm.cu) against tiles of
-    // R weight rows that fill the SMs, no K split, where the x bytes of a
-    // 64-column step are at most 1.5x the weight's (x rows padded to 64, 128 or
-    // 256).  Stages of four 64-column slices where three of them fit beside x
-    // of 64 rows, two slices otherwise, as many as fit.  Measured on GB300 per
-    // call (CUDA graph + PDL, weights past L2): DSA 14560 x 7168 B = 32 / 64 /
-    // 128: 32.4 / 32.6 / 33.4 us against 33.1 / 35.9 / 39.7 us for the stream-K
-    // and cluster kinds; KDA 49376 x 7168 B = 64 / 128: 100.8 / 107.6 against
-    // 108.4 / 112.5 us; o_proj 7168 x 12288 B = 32 / 64: 28.8 / 28.8 against
-    // 29.5 / 33.1 us.  Not at 256 rows (DSA 50.7 against 45.7 us for the cluster
-    // kind) nor o_proj at 128 (38.2 against 36.4 us): x bytes dominate there.
+    // R weight rows that fill the SMs, where the x bytes of a 64-column step are
+    // at most 1.5x the weight's (x rows padded to 64, 128 or 256): whole K per
+    // block where R allows that, else a pair of blocks (a cluster of two, each
+    // half of K) per tile of up to twice the rows.  Stages of the widest slice
+    // count that still gives a ring of three beside x of the pass's height, the
+    // deepest ring that fits.  Measured on GB300 per call (CUDA graph + PDL,
+    // weights past L2): DSA 14560 x 7168 B = 32 / 64 / 128: 32.4 / 32.6 / 33.4 us
+    // against 33.1 / 35.9 / 39.7 us for the stream-K and cluster kinds, B = 256
+    // (pairs, R = 192): 41.3 against 45.8 us; KDA 49376 x 7168 B = 64 / 128:
+    // 100.8 / 107.6 against 108.4 / 112.5 us, B = 256 (pairs, R = 224): 142.8
+    // against 147.7 us; o_proj 7168 x 12288 B = 32 / 64: 28.8 / 28.8 against
+    // 29.5 / 33.1 us, B = 128 (pairs, R = 96): 32.4 against 37.1 us.  o_proj at
+    // 256 rows keeps the cluster kind (x's bytes would be 2.7x the weight's).
     if (rows > 16 && rows <= 256) {
-        const int32_t R = xm_rows_per_tile(N, sm_count);
         const int32_t xrows = rows <= 64 ? 64 : (rows <= 128 ? 128 : 256);
         const int32_t xcols = rows <= 128 ? 128 : 256;  // one or two blocks of 128 rows per pass
-        if (R <= 256 && 2 * xrows <= 3 * R) {
-            const int32_t xr = rows <= 64 ? 64 : 128;
-            const int32_t tk = dep::xm_stages_fit(R, 256, xcols, xr) >= 3 ? 256 : 128;
-            const int32_t st = dep::xm_stages_fit(R, tk, xcols, 128);  // the tactic's depth is at 128 rows
-            if (st >= 2)
-                return xm_tactic(rows, xcols, R, tk, st, sm_count);
+        const int32_t xr = rows <= 64 ? 64 : 128;       // x rows per block of a pass
+        auto pick = [&](int32_t R, int32_t splits, int32_t ctas) {
+            dep_tactic_t none{};
+            if (R > 256 || 2 * xrows > 3 * R)
+                return none;
+            for (int32_t tk : {256, 128, 64})
+                if (dep::xm_stages_fit(R, tk, xcols, xr) >= 3) {
+                    dep_tactic_t t = xm_tactic(rows, xcols, R, tk, dep::xm_stages_fit(R, tk, xcols, 128), ctas);
+                    t.splits = splits;
+                    if (dep::xm_valid(t))
+                        return t;
+                }
+            return none;
+        };
+        dep_tactic_t t = pick(xm_rows_per_tile(N, sm_count), 0, sm_count);
+        if (t.kind == 0) {
+            const int32_t R2 = xm_pair_rows_per_tile(N, sm_count);
+            const int64_t pairs = std::min<int64_t>((N + R2 - 1) / R2, sm_count / 2);
+            t = pick(R2, 2, (int32_t)(2 * pairs));
         }
+        if (t.kind != 0)
+            return t;
     }
     // Up to 32 batch rows on long weight rows (K >= 3072) whose 64-row tiles fit
     // on the SMs: 64-row K-piece tiles in as few pieces as fill the SMs (o_proj:
@@ -726,6 +755,19 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
                 for (int32_t st : {2, 3, 4, 5, 6})
                     if (r >= 16 && r <= 256)
                         c.push_back(xm_tactic(rows, xcols, r, tk, st, sm_count));
+        // pairs of blocks per tile (each half of K)
+        const int32_t p0 = xm_pair_rows_per_tile(N, sm_count);
+        for (int32_t r : {p0 - 32, p0, p0 + 32}) {
+            if (r < 32 || r > 256)
+                continue;
+            const int64_t pairs = std::min<int64_t>((N + r - 1) / r, sm_count / 2);
+            for (int32_t tk : {64, 128})
+                for (int32_t st : {2, 3, 4, 5, 6}) {
+                    dep_tactic_t t = xm_tactic(rows, xcols, r, tk, st, (int32_t)(2 * pairs));
+                    t.splits = 2;
+                    c.push_back(t);
+                }
+        }
     }
     // K pieces keep every piece's partial: leave out tactics whose exchange words
     // would take more than 64 MB.
@@ -938,11 +980,16 @@ dep_status_t dep_projection_run_host(dep_plan_t plan, const void *x_host, const 
         }
         // The projection may start while the gather runs: it streams W first and
         // reads x only after waiting for the gather (the gather does not write W).
-        // Kernels that store y with plain stores write it straight into the
-        // mapped y_host (one kernel and one dependent-launch hop fewer per call);
-        // the cluster kernel stores y by bulk tensor copies from shared memory
-        // into device memory, and a copy kernel takes it back.
-        const bool direct = t && t->kind != DEP_KIND_TC_CLUSTER;
+        // Kernels whose warps store runs of contiguous y bytes write it straight
+        // into the mapped y_host (one kernel and one dependent-launch hop fewer
+        // per call).  The cluster kernel stores y by bulk tensor copies from
+        // shared memory into device memory, and the x-on-M kernel 32 bytes per
+        // lane into 32 different rows, which over the host link took ~1.7x the
+        // time of a copy (DSA at 32-256 rows, end to end: 473 against 274 us per
+        // step): both write the staging area, and a copy kernel takes y back.
+        // DEP_STAGING=stage takes that route for every kind (for comparisons).
+        const bool direct = t && t->kind != DEP_KIND_TC_CLUSTER && t->kind != DEP_KIND_TC_XM &&
+                            !env_is("DEP_STAGING", "stage");
         dep_status_t st = run_impl(plan, t, plan->x_stage, W, direct ? ay.devicePointer : plan->y_stage, B, stream,
                                    true);
         if (st != DEP_OK)

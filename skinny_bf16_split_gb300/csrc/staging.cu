@@ -3,8 +3,9 @@
 // When the caller's host buffers are pinned (mapped into the device's address
 // space), x is gathered into the plan's device staging area by a small kernel
 // instead of a memcpy; the projection stores y into the mapped buffer itself,
-// or (the cluster kind, whose y leaves by bulk tensor stores) writes the staging
-// area and the same kernel copies y back.  Chained by programmatic
+// or (the cluster and x-on-M kinds, whose y stores are not rows of contiguous
+// bytes across a warp) writes the staging area and the same kernel copies y
+// back.  Chained by programmatic
 // dependent launch: each copy triggers its dependents at once and waits for
 // the preceding grid before it reads (so a source written by earlier work in
 // the stream is complete, and the staging area is no longer read by an earlier
@@ -33,17 +34,29 @@ __global__ void __launch_bounds__(kStageThreads)
     const size_t nv = n / 8;  // 16-byte vectors (both pointers are 16-byte aligned)
     const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
     uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-    for (size_t i = tid; i < nv; i += stride)
+    // Four loads in flight per thread before their stores: reads of mapped host
+    // memory take microseconds.
+    size_t i = tid;
+    for (; i + 3 * stride < nv; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            v[u] = s4[i + u * stride];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            d4[i + u * stride] = v[u];
+    }
+    for (; i < nv; i += stride)
         d4[i] = s4[i];
-    for (size_t i = nv * 8 + tid; i < n; i += stride)
-        dst[i] = src[i];
+    for (size_t j = nv * 8 + tid; j < n; j += stride)
+        dst[j] = src[j];
 }
 
 int copy_grid(size_t n)
 {
     const size_t vecs = (n + 7) / 8;
     const size_t blocks = (vecs + kStageThreads - 1) / kStageThreads;
-    return (int)(blocks < 1 ? 1 : blocks > 256 ? 256 : blocks);
+    return (int)(blocks < 1 ? 1 : blocks > 608 ? 608 : blocks);
 }
 
 }  // namespace

@@ -49,6 +49,7 @@
 //    in increasing order: results do not depend on the grid or on timing.
 #include <cuda_bf16.h>
 
+#include "cluster.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -83,11 +84,16 @@ __host__ __device__ inline uint32_t xm_tmem_cols(int R)
     return c;
 }
 // Shared memory: the 1 KB-aligned ring; then full[stages], empty[stages],
-// accf[2], acce[2], done; then the TMEM address and the abort flag.
+// accf[2], acce[2], done, ring_free, rx_full, peer_free; then the TMEM address
+// and the abort flag.
 __host__ __device__ constexpr size_t xm_smem_bytes(int stages, int atoms, int mb, int R, int mr)
 {
-    return 1024 + (size_t)stages * xm_stage(atoms, mb, R, mr) + (size_t)(2 * stages + 5) * 8 + 16;
+    return 1024 + (size_t)stages * xm_stage(atoms, mb, R, mr) + (size_t)(2 * stages + 8) * 8 + 16;
 }
+// Bytes one CTA of a pair receives from the other: half the R accumulator
+// columns of every block of 128 batch rows, FP32 (laid out [block][lane
+// quadrant][column / 4][lane][4]).
+__host__ __device__ constexpr size_t xm_recv_bytes(int mb, int R) { return (size_t)mb * kXRows * (R / 2) * 4; }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
@@ -102,7 +108,7 @@ __device__ __forceinline__ uint32_t idesc_mn(int m, int n)
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-template <int MB>
+template <int MB, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_xm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
                  uint16_t *__restrict__ y, int B, int N, int K, int R, int MR, int stages, int atoms, int tma3,
@@ -123,11 +129,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t accf0 = empty0 + 8 * stages;  // accumulator final, 2 buffers
     const uint32_t acce0 = accf0 + 16;           // accumulator drained, 2 buffers
     const uint32_t done = acce0 + 16;            // all MMAs complete
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 5);
+    const uint32_t ring_free = done + 8;         // pairs: the epilogue no longer uses the ring
+    const uint32_t rx_full = done + 16;          // pairs: the other CTA's partials have landed
+    const uint32_t peer_free = done + 24;        // pairs: the other CTA's ring is idle
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * stages + 8);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int T = (N + R - 1) / R;            // weight tiles
-    const int KT = (K + kBK - 1) / kBK;       // 64-column slices
+    // A pair (a cluster of two CTAs) shares each tile: rank r sums the 64-column
+    // slices [r KT / 2, (r + 1) KT / 2) and the halves meet in shared memory.
+    const int rank = PAIR ? (int)cluster_rank() : 0;
+    const int KT_ALL = (K + kBK - 1) / kBK;
+    const int S0 = PAIR ? rank * KT_ALL / 2 : 0;  // this CTA's first slice
+    const int KT = PAIR ? (rank + 1) * KT_ALL / 2 - S0 : KT_ALL;  // its slices of a tile
+    // Tiles are dealt out per block, or per pair: t0, t0 + TS, ...
+    const int t0 = PAIR ? (int)cluster_id() : (int)blockIdx.x;
+    const int TS = PAIR ? (int)cluster_count() : (int)gridDim.x;
     const int KS = (KT + atoms - 1) / atoms;  // stages per tile
     const int ACC = xm_acc(R);                // TMEM columns of one accumulator buffer
     const int BUFS = xm_bufs(R);
@@ -149,10 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int na = slices_of(k);
         mbar_arrive_expect_tx(bar, (uint32_t)stage_bytes(na));
         if (tma3) {  // the stage's slices in one copy; blocks past K read as zero
-            tma_load_3d(dst, &tmW, 0, t * R, k * atoms, bar, pol_w);
+            tma_load_3d(dst, &tmW, 0, t * R, S0 + k * atoms, bar, pol_w);
         } else {
             for (int a = 0; a < na; ++a)
-                tma_load_2d(dst + (uint32_t)(a * WSLICE), &tmW, (k * atoms + a) * kBK, t * R, bar, pol_w);
+                tma_load_2d(dst + (uint32_t)(a * WSLICE), &tmW, (S0 + k * atoms + a) * kBK, t * R, bar, pol_w);
         }
     };
     auto issue_x = [&](int st, int k) {
@@ -160,10 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int na = slices_of(k);
         for (int m = 0; m < MBV; ++m) {
             if (tma3) {
-                tma_load_3d(dst + (uint32_t)(m * atoms * XBOX), &tmX, 0, m * kXRows, k * atoms, bar, pol_x);
+                tma_load_3d(dst + (uint32_t)(m * atoms * XBOX), &tmX, 0, m * kXRows, S0 + k * atoms, bar, pol_x);
             } else {
                 for (int a = 0; a < na; ++a)
-                    tma_load_2d(dst + (uint32_t)((m * atoms + a) * XBOX), &tmX, (k * atoms + a) * kBK, m * kXRows,
+                    tma_load_2d(dst + (uint32_t)((m * atoms + a) * XBOX), &tmX, (S0 + k * atoms + a) * kBK, m * kXRows,
                                 bar, pol_x);
             }
         }
@@ -180,6 +197,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acce0 + 8 * b, kEpiWarps);
         }
         mbar_init(done, kIssuers);
+        mbar_init(ring_free, kEpiWarps);
+        mbar_init(rx_full, 1);    // armed per tile with the bytes the other CTA stores
+        mbar_init(peer_free, 1);  // arrived on by the other CTA
         *abort_flag = 0;
         fence_mbar_init();
         griddep_launch_dependents();
@@ -190,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pol_w = policy_evict_first();
         pol_x = policy_evict_last();
         for (int i = 0; i < pre; ++i)
-            issue_w(i, (int)blockIdx.x, i);
+            issue_w(i, t0, i);
     }
     if (warp == 1) {
         tc::alloc(smem_u32(tmem_slot), TMEM_COLS);
@@ -199,6 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    if (PAIR)
+        cluster_sync();  // both CTAs of the pair have set up their barriers
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
@@ -207,15 +229,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             griddep_wait();  // x may be written by the preceding grid
             for (int i = 0; i < pre; ++i)
                 issue_x(i, i);
-            int t = (int)blockIdx.x, k = pre, s = pre % stages;
+            int t = t0, k = pre, s = pre % stages, gi = 0;
             uint32_t ph = pre == stages ? 1u : 0u;
             int64_t issued = pre;
             for (;;) {
                 if (k == KS) {  // the tile is fully issued: the next one of this block
-                    t += (int)gridDim.x;
+                    t += TS;
                     if (t >= T)
                         break;
                     k = 0;
+                    // A pair's partials of the previous tile pass through the ring:
+                    // refill it once the epilogue is done with them.
+                    if (PAIR && !mbar_wait(ring_free, (uint32_t)(gi & 1), limit_ns)) {
+                        record_status(status, DEP_DEV_TIMEOUT_PRODUCER);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    ++gi;
                 }
                 if (*abort_flag)
                     break;
@@ -259,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             int s = 0, buf = 0;
             uint32_t ph = 0, acce_ph = 0;
             bool ok = true;
-            for (int t = (int)blockIdx.x; t < T && ok; t += (int)gridDim.x) {
+            for (int t = t0; t < T && ok; t += TS) {
                 if (!mbar_wait(acce0 + 8 * buf, ((acce_ph >> buf) & 1u) ^ 1u, limit_ns)) {
                     record_status(status, DEP_DEV_TIMEOUT_MMA);
                     *abort_flag = 1;
@@ -318,11 +348,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;             // TMEM lane quadrant this warp may read
         const int h = (warp - kEpi0) >> 2;  // which of the two warps of the quadrant
         const int CPB = R / 16;             // 16-column chunks of one accumulator
-        const int NC = MB * CPB;            // MB = 1: both issuers' chunks summed; MB = 2: per block
         const bool vec = (N & 7) == 0;      // y rows are 16-byte multiples: vector stores
         uint32_t accf_ph = 0;
-        int buf = 0;
-        for (int t = (int)blockIdx.x; t < T; t += (int)gridDim.x) {
+        int buf = 0, gi = 0;
+        uint32_t tq = 0;  // this warp's TMEM lanes of the current accumulator buffer
+        // This CTA's FP32 partial of block m, accumulator columns col..col+15
+        // (one block of rows: issuer 0's accumulator, then issuer 1's added).
+        auto partial = [&](int m, int col, float (&f)[16]) {
+            __syncwarp();  // tcgen05.ld is warp-collective: every lane, converged
+            uint32_t v[16];
+            tc::ld16(tq + (uint32_t)(m * R + col), v);
+            tc::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                f[j] = __uint_as_float(v[j]);
+            if (MB == 1) {
+                tc::ld16(tq + (uint32_t)(R + col), v);
+                tc::wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    f[j] = f[j] + __uint_as_float(v[j]);
+            }
+        };
+        // Round and store the sums of block m, weight rows t R + col .. + 15.
+        auto store = [&](int m, int col, int t, const float (&f)[16]) {
+            // batch row of this lane in the pass (M = 64: lanes 16-31 hold none)
+            const int b = m * kXRows + (MR == kXRows ? 32 * q + lane : (lane < 16 ? 16 * q + lane : kXRows));
+            const int n0 = t * R + col;  // first weight row of the chunk
+            if (b >= B || n0 >= N)
+                return;
+            uint16_t *yr = y + (int64_t)b * N + n0;
+            if (vec && n0 + 16 <= N && dbg_ok((int64_t)b * N + n0 + 15, bd.y, status)) {
+                uint4 lo, hi;
+                lo.x = pack_bf16x2(f[0], f[1]);
+                lo.y = pack_bf16x2(f[2], f[3]);
+                lo.z = pack_bf16x2(f[4], f[5]);
+                lo.w = pack_bf16x2(f[6], f[7]);
+                hi.x = pack_bf16x2(f[8], f[9]);
+                hi.y = pack_bf16x2(f[10], f[11]);
+                hi.z = pack_bf16x2(f[12], f[13]);
+                hi.w = pack_bf16x2(f[14], f[15]);
+                reinterpret_cast<uint4 *>(yr)[0] = lo;
+                reinterpret_cast<uint4 *>(yr)[1] = hi;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (n0 + j < N && dbg_ok((int64_t)b * N + n0 + j, bd.y, status))
+                        yr[j] = __bfloat16_as_ushort(__float2bfloat16_rn(f[j]));
+            }
+        };
+        for (int t = t0; t < T; t += TS, ++gi) {
             const bool got = mbar_wait(accf0 + 8 * buf, (accf_ph >> buf) & 1u, limit_ns);
             if (!__all_sync(0xffffffffu, got)) {
                 record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
@@ -331,64 +406,104 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             accf_ph ^= 1u << buf;
             tc::fence_after();
-            const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * ACC);
-            for (int c = h; c < NC; c += 2) {
-                const int m = c / CPB, col = (c - m * CPB) * 16;
-                if (MB == 2 && m >= MBV)
-                    break;  // a block past this pass's rows: nothing was summed into it
-                __syncwarp();  // tcgen05.ld is warp-collective: every lane, converged
-                float f[16];
-                uint32_t v[16];
-                tc::ld16(tq + (uint32_t)(m * R + col), v);
-                tc::wait_ld();
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    f[j] = __uint_as_float(v[j]);
-                if (MB == 1) {  // issuer 1's accumulator, added after issuer 0's
-                    tc::ld16(tq + (uint32_t)(R + col), v);
-                    tc::wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        f[j] = f[j] + __uint_as_float(v[j]);
+            tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * ACC);
+            bool ok = true;
+            if (PAIR) {
+                // Rank r reduces and stores accumulator columns [r R/2, (r + 1) R/2)
+                // of every block; it sends the other half of its partials to the
+                // other CTA's (idle) ring and adds the half it receives, rank 0's
+                // K half first.
+                const int HALF = R / 2, CPH = HALF / 16, NCH = MBV * CPH;
+                const int own0 = rank * HALF, oth0 = HALF - own0;
+                const uint32_t par = (uint32_t)(gi & 1), other = (uint32_t)(rank ^ 1);
+                auto roff = [&](int m, int c) {  // [block][quadrant][column / 4][lane] float4
+                    return (uint32_t)((((m * 4 + q) * (HALF / 4) + c / 4) * 32 + lane) * 16);
+                };
+                // 1. This CTA's MMAs of the tile are done, so its ring is idle: arm
+                //    the receive barrier with the bytes the other CTA will store,
+                //    then tell it.
+                if (warp == kEpi0 && lane == 0) {
+                    mbar_arrive_expect_tx(rx_full, (uint32_t)(MBV * kXRows * HALF * 4));
+                    mbar_arrive_peer(peer_addr(peer_free, other));
                 }
-                // batch row of this lane in the pass (M = 64: lanes 16-31 hold none)
-                const int b = m * kXRows + (MR == kXRows ? 32 * q + lane : (lane < 16 ? 16 * q + lane : kXRows));
-                const int n0 = t * R + col;  // first weight row of the chunk
-                if (b >= B || n0 >= N)
-                    continue;
-                uint16_t *yr = y + (int64_t)b * N + n0;
-                if (vec && n0 + 16 <= N && dbg_ok((int64_t)b * N + n0 + 15, bd.y, status)) {
-                    uint4 lo, hi;
-                    lo.x = pack_bf16x2(f[0], f[1]);
-                    lo.y = pack_bf16x2(f[2], f[3]);
-                    lo.z = pack_bf16x2(f[4], f[5]);
-                    lo.w = pack_bf16x2(f[6], f[7]);
-                    hi.x = pack_bf16x2(f[8], f[9]);
-                    hi.y = pack_bf16x2(f[10], f[11]);
-                    hi.z = pack_bf16x2(f[12], f[13]);
-                    hi.w = pack_bf16x2(f[14], f[15]);
-                    reinterpret_cast<uint4 *>(yr)[0] = lo;
-                    reinterpret_cast<uint4 *>(yr)[1] = hi;
-                } else {
+                // 2. The other CTA's half of this CTA's partials into its ring.
+                if (!mbar_wait_cluster(peer_free, par, limit_ns)) {
+                    record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
+                    ok = false;
+                }
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok) {
+                    const uint32_t pbar = peer_addr(rx_full, other), pbase = peer_addr(base, other);
+                    for (int c = h; c < NCH; c += 2) {
+                        const int m = c / CPH, col = (c - m * CPH) * 16;
+                        float f[16];
+                        partial(m, oth0 + col, f);
+                        if (!dbg_range(roff(m, col + 12), 16, (unsigned)(stages * STAGE), status))
+                            continue;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            st_async_peer_v4(pbase + roff(m, col + 4 * i), f[4 * i], f[4 * i + 1], f[4 * i + 2],
+                                             f[4 * i + 3], pbar);
+                    }
+                }
+                // 3. The other CTA's half of this CTA's columns has landed.
+                if (ok && !mbar_wait_cluster(rx_full, par, limit_ns)) {
+                    record_status(status, DEP_DEV_TIMEOUT_EPILOGUE);
+                    ok = false;
+                }
+                ok = __all_sync(0xffffffffu, ok);
+                // 4. This CTA's columns: the two K halves in rank order.
+                for (int c = h; c < NCH && ok; c += 2) {
+                    const int m = c / CPH, col = (c - m * CPH) * 16;
+                    float f[16], g[16];
+                    partial(m, own0 + col, f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (dbg_range(roff(m, col + 4 * i), 16, (unsigned)(stages * STAGE), status))
+                            r = *reinterpret_cast<const float4 *>(smem + roff(m, col + 4 * i));
+                        g[4 * i] = r.x;
+                        g[4 * i + 1] = r.y;
+                        g[4 * i + 2] = r.z;
+                        g[4 * i + 3] = r.w;
+                    }
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
-                        if (n0 + j < N && dbg_ok((int64_t)b * N + n0 + j, bd.y, status))
-                            yr[j] = __bfloat16_as_ushort(__float2bfloat16_rn(f[j]));
+                        f[j] = rank == 0 ? f[j] + g[j] : g[j] + f[j];
+                    store(m, own0 + col, t, f);
+                }
+            } else {
+                for (int c = h; c < MB * CPB; c += 2) {
+                    const int m = c / CPB, col = (c - m * CPB) * 16;
+                    if (MB == 2 && m >= MBV)
+                        break;  // a block past this pass's rows: nothing was summed into it
+                    float f[16];
+                    partial(m, col, f);
+                    store(m, col, t, f);
                 }
             }
-            // The accumulator buffer is free again.
+            if (!ok)
+                *abort_flag = 1;
+            // The ring (pairs) and the accumulator buffer are free again.
             tc::fence_before();
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0) {
+                if (PAIR)
+                    mbar_arrive(ring_free);
                 mbar_arrive(acce0 + 8 * buf);
+            }
             if (BUFS == 2)
                 buf ^= 1;
+            if (!ok)
+                break;
         }
     }
 
     __syncwarp();
     tc::fence_before();
     __syncthreads();
+    if (PAIR)
+        cluster_sync();  // no CTA leaves while the other may still write into it
     if (warp == 1) {
         tc::fence_after();
         tc::dealloc(tmem, TMEM_COLS);
@@ -401,11 +516,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 namespace dep {
 namespace {
 
-template <int MB>
+template <int MB, bool PAIR>
 cudaError_t prepare()
 {
     static std::atomic<uint64_t> devices{0};
-    return set_smem_attr(tc_xm_kernel<MB>, devices);
+    return set_smem_attr(tc_xm_kernel<MB, PAIR>, devices);
 }
 
 // Stages of a launch whose x blocks have mr rows: the tactic's (which fit at
@@ -423,10 +538,10 @@ int stages_for(const dep_tactic_t &t, int mr)
     return st;
 }
 
-template <int MB>
+template <int MB, bool PAIR>
 cudaError_t run_mb(const dep_tactic_t &t, const RunArgs &a)
 {
-    cudaError_t e = prepare<MB>();
+    cudaError_t e = prepare<MB, PAIR>();
     if (e != cudaSuccess)
         return e;
     const int R = t.tile_n, atoms = t.tile_k / kBK;
@@ -440,7 +555,9 @@ cudaError_t run_mb(const dep_tactic_t &t, const RunArgs &a)
                                CU_TENSOR_MAP_SWIZZLE_128B)) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     const int64_t T = (a.N + R - 1) / R;
-    const int grid = (int)(T < t.ctas ? T : t.ctas);
+    // blocks (or pairs of blocks) dealing out the tiles
+    const int64_t per = PAIR ? t.ctas / 2 : t.ctas;
+    const int units = (int)(T < per ? T : per);
     constexpr int32_t kPass = MB * kXRows;
     for (int32_t r0 = 0; r0 < a.B; r0 += kPass) {
         const int32_t rows = a.B - r0 < kPass ? a.B - r0 : kPass;
@@ -452,9 +569,23 @@ cudaError_t run_mb(const dep_tactic_t &t, const RunArgs &a)
                   : encode_bf16_2d(&tmX, xr, (uint64_t)a.K, (uint64_t)rows, kBK, (uint32_t)mr,
                                    CU_TENSOR_MAP_SWIZZLE_128B)) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        e = launch(tc_xm_kernel<MB>, dim3(grid), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
-                   a.y + (size_t)r0 * a.N, (int)rows, (int)a.N, (int)a.K, R, mr, st, atoms, tma3, a.status,
-                   a.bounds(rows, smem), a.wait_limit_ns);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(PAIR ? 2 * units : units));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = a.stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 2;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = PAIR ? 2 : 1;
+        e = cudaLaunchKernelEx(&cfg, tc_xm_kernel<MB, PAIR>, tmW, tmX, a.y + (size_t)r0 * a.N, (int)rows,
+                               (int)a.N, (int)a.K, R, mr, st, atoms, tma3, a.status, a.bounds(rows, smem),
+                               a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }
@@ -465,8 +596,8 @@ cudaError_t run_mb(const dep_tactic_t &t, const RunArgs &a)
 
 bool xm_valid(const dep_tactic_t &t)
 {
-    if (t.kind != DEP_KIND_TC_XM || t.splits != 0 || t.ctas < 1)
-        return false;
+    if (t.kind != DEP_KIND_TC_XM || t.ctas < 1 || t.splits < 0 || t.splits > 2)
+        return false;  // splits: 0 or 1 = whole K per block; 2 = a pair of blocks per tile
     if (t.tile_n < 16 || t.tile_n > kMaxRows || t.tile_n % 16 != 0)
         return false;  // MMA N: a multiple of 16 up to 256 weight rows
     if (t.cols != kXRows && t.cols != 2 * kXRows)
@@ -475,12 +606,21 @@ bool xm_valid(const dep_tactic_t &t)
         return false;  // 1, 2 or 4 slices of 64 columns per stage
     if (t.stages < 2 || t.stages > kMaxStages)
         return false;
-    return xm_smem_bytes(t.stages, t.tile_k / kBK, t.cols / kXRows, t.tile_n, kXRows) <= (size_t)kMaxDynamicSmem;
+    const int atoms = t.tile_k / kBK, mb = t.cols / kXRows;
+    if (t.splits == 2) {
+        if (t.tile_n % 32 != 0 || t.ctas < 2)
+            return false;  // each CTA of a pair stores whole 16-column chunks of a half tile
+        // the other CTA's partials land in the idle ring (at 64-row x blocks the ring is smaller)
+        if (xm_recv_bytes(mb, t.tile_n) > (size_t)t.stages * xm_stage(atoms, mb, t.tile_n, 64))
+            return false;
+    }
+    return xm_smem_bytes(t.stages, atoms, mb, t.tile_n, kXRows) <= (size_t)kMaxDynamicSmem;
 }
 
 int64_t xm_tiles(const dep_tactic_t &t, int64_t N)
 {
-    return (N + t.tile_n - 1) / t.tile_n;
+    const int64_t T = (N + t.tile_n - 1) / t.tile_n;
+    return t.splits == 2 ? 2 * T : T;  // blocks a launch can use
 }
 
 int xm_stages_fit(int32_t tile_n, int32_t tile_k, int32_t cols, int mr)
@@ -494,13 +634,22 @@ int xm_stages_fit(int32_t tile_n, int32_t tile_k, int32_t cols, int mr)
 
 cudaError_t xm_prepare_device()
 {
-    cudaError_t e = prepare<1>();
-    return e == cudaSuccess ? prepare<2>() : e;
+    cudaError_t e = prepare<1, false>();
+    if (e == cudaSuccess)
+        e = prepare<2, false>();
+    if (e == cudaSuccess)
+        e = prepare<1, true>();
+    return e == cudaSuccess ? prepare<2, true>() : e;
 }
 
 cudaError_t xm_run(const dep_tactic_t &t, const RunArgs &a)
 {
-    return t.cols == kXRows ? run_mb<1>(t, a) : run_mb<2>(t, a);
+    // A pair splits K in two halves of 64-column slices: with fewer than two
+    // slices the tactic runs unsplit.
+    const bool pair = t.splits == 2 && (a.K + kBK - 1) / kBK >= 2;
+    if (t.cols == kXRows)
+        return pair ? run_mb<1, true>(t, a) : run_mb<1, false>(t, a);
+    return pair ? run_mb<2, true>(t, a) : run_mb<2, false>(t, a);
 }
 
 }  // namespace dep

@@ -57,6 +57,8 @@ def main():
                          cols=128)),
             ("x-on-m-2", T(max_rows=2048, kind=dep.DEP_KIND_TC_XM, ctas=sms, tile_n=96, tile_k=64, stages=3,
                            cols=256)),
+            ("x-on-m-pairs", T(max_rows=4096, kind=dep.DEP_KIND_TC_XM, ctas=6, tile_n=64, tile_k=64, stages=4,
+                               cols=256, splits=2)),
         ]
 
     # K = 2048 and 1088 (multiples of 64) take the one-copy column-block stage

@@ -88,35 +88,38 @@ def test_default_batches_when_none_given(dep):
         xm = [t for t in table if 32 <= t.max_rows <= 128]
         assert all((t.kind, t.tile_n, t.cols, t.ctas, t.splits) == (dep.DEP_KIND_TC_XM, 96, 128, 152, 0)
                    for t in xm)
-        # 256 rows: 76 groups of 192 rows (a 128-row and a 64-row tile), a cluster
-        # of two CTAs each, 152 CTAs
+        # 256 rows: pairs of CTAs (each half of K) on 76 tiles of 192 rows, 152 CTAs
         t = table[-1]
-        assert (t.max_rows, t.kind, t.tile_n, t.splits, t.ctas) == (256, dep.DEP_KIND_TC_CLUSTER, 192, 2, 152)
+        assert (t.max_rows, t.kind, t.tile_n, t.cols, t.splits, t.ctas) == (256, dep.DEP_KIND_TC_XM, 192, 256, 2, 152)
     finally:
         dep.dep_projection_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("N,sms,xm_rows,cluster", [
-    (7168, 152, {64: 48}, {128: (256, 4, 112), 256: (256, 4, 112)}),  # o_proj: x dominates at 128 rows
-    (14560, 152, {64: 96, 128: 96}, {256: (192, 2, 152)}),             # DSA: 152 tiles of 96 rows
-    (49376, 152, {64: 112, 128: 112}, {256: (256, 2, 152)}),           # KDA: 441 tiles, three waves
-    (1000, 8, {64: 128, 128: 128}, {256: (256, 2, 8)}),                # 8 tiles of 128 rows on 8 SMs
+@pytest.mark.parametrize("N,sms,whole,pairs,cluster", [
+    (7168, 152, {64: 48}, {128: (96, 128, 150)}, {256: (256, 4, 112)}),  # o_proj: clusters at 256 rows
+    (14560, 152, {64: 96, 128: 96}, {256: (192, 256, 152)}, {}),           # DSA: 152 tiles of 96 rows
+    (49376, 152, {64: 112, 128: 112}, {256: (224, 256, 152)}, {}),         # KDA: 441 tiles, three waves
+    (1000, 8, {64: 128, 128: 128}, {256: (256, 256, 8)}, {}),              # 8 tiles of 128 rows on 8 SMs
 ])
-def test_default_rule_wide_batches(dep, N, sms, xm_rows, cluster):
-    """The default rule for 64-256 rows: x on the MMA's M side (tiles of R weight
-    rows, the smallest multiple of 16 that fills the SMs in as few waves as
-    tiles of at most 128 rows allow) wherever x's bytes per 64-column step are
-    at most 1.5x the weight's; otherwise a cluster of k = SMs / groups (at most
-    4) CTAs per group of two 128-row tiles while the groups fit on the SMs in
-    clusters of two, clusters of two at 256 rows, and on DSA's 14560 rows groups
-    of 192 (a 128-row and a 64-row tile)."""
+def test_default_rule_wide_batches(dep, N, sms, whole, pairs, cluster):
+    """The default rule for 64-256 rows: x on the MMA's M side wherever x's
+    bytes per 64-column step are at most 1.5x the weight's -- whole K per block
+    on tiles of R rows (the smallest multiple of 16 that fills the SMs in as few
+    waves as tiles of at most 128 rows allow), else pairs of blocks (a cluster
+    of two, each half of K) on tiles of up to twice that (multiples of 32 up to
+    256); otherwise a cluster of k = SMs / groups (at most 4) CTAs per group of
+    two 128-row tiles."""
     plan = dep.dep_projection_plan_host(N, 7168, [64, 128, 256], sms)
     try:
         table = {t.max_rows: t for t in dep.dep_projection_plan_table(plan)}
-        for b, R in xm_rows.items():
+        for b, R in whole.items():
             t = table[b]
             assert (t.kind, t.tile_n, t.cols, t.ctas, t.splits) == (dep.DEP_KIND_TC_XM, R, 128, sms, 0), (b, t)
             assert 2 * (64 if b <= 64 else 128) <= 3 * R
+        for b, (R, cols, ctas) in pairs.items():
+            t = table[b]
+            assert (t.kind, t.tile_n, t.cols, t.ctas, t.splits) == (dep.DEP_KIND_TC_XM, R, cols, ctas, 2), (b, t)
+            assert R % 32 == 0 and 2 * (b if b > 64 else 64) <= 3 * R
         for b, (rows, k, ctas) in cluster.items():
             t = table[b]
             assert (t.kind, t.tile_n, t.splits, t.ctas) == (dep.DEP_KIND_TC_CLUSTER, rows, k, ctas), (b, t)

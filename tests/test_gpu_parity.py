@@ -245,18 +245,22 @@ def test_argument_errors_on_device(dep, plan_cache):
 
 
 @pytest.mark.parametrize("B,N", [(5, 640), (1, 333), (16, 7168), (40, 1001), (255, 14561)])
-@pytest.mark.parametrize("memory", ["pinned", "pageable", "pinned-copy"])
+@pytest.mark.parametrize("memory", ["pinned", "pageable", "pinned-copy", "pinned-stage"])
 def test_run_host_end_to_end(dep, orc, plan_cache, monkeypatch, B, N, memory):
     """The host-buffer entry point gives the device entry point's bits: pinned
     buffers through the zero-copy gather, y stored by the projection or (the
-    cluster kind, B = 40 and 255) copied back by the staging kernel, chained by
+    cluster kind at B = 40, the x-on-M kind at B = 255; every kind under
+    DEP_STAGING=stage) copied back by the staging kernel, chained by
     programmatic dependent launch (N odd included: a 2-byte tail; B = 255: a
-    7.4 MB y, several 16-byte vectors per copying thread), pageable buffers and
-    DEP_STAGING=copy through memcpys.  Ten calls back to back, one sync."""
+    7.4 MB y, several rounds of four 16-byte vectors per copying thread),
+    pageable buffers and DEP_STAGING=copy through memcpys.  Ten calls back to
+    back, one sync."""
     K = 2048
     plan = get_plan(dep, plan_cache, N, K)
     if memory == "pinned-copy":
         monkeypatch.setenv("DEP_STAGING", "copy")
+    if memory == "pinned-stage":
+        monkeypatch.setenv("DEP_STAGING", "stage")
     xs = [synth.normal_bf16(2 + i, 2, (B, K)) for i in range(10)]
     W = synth.normal_bf16(2, 1, (N, K), sigma=0.02)
     Wd = to_dev(W)
