@@ -16,7 +16,7 @@
 // R = 96, 152 tiles).  Every block streams its tiles' whole K: no K split, no
 // partials, no exchange, no cluster.
 //
-// Design (sm_103a, one CTA per SM, no clusters, no multicast):
+// Design (sm_103a, one CTA per SM, no multicast):
 //  * Tiles of R weight rows are dealt out statically: block b takes tiles
 //    b, b + grid, ...
 //  * A stage holds `atoms` 64-column slices of the tile's weight rows [R x 64]
@@ -42,6 +42,16 @@
 //    16-column chunks (= 16 consecutive weight rows), round to BF16 and store
 //    32 contiguous bytes of a y row per lane.  M = 128 puts batch row r in
 //    TMEM lane r; M = 64 puts it in lane 32 (r / 16) + r % 16.
+//  * Pairs (splits = 2): where x's bytes per step would outweigh the weight's
+//    at tiles that fill the SMs, a thread-block cluster of two CTAs shares each
+//    tile of up to twice the rows, rank r summing the first or second half of
+//    the 64-column slices.  Once its MMAs of the tile are done a CTA's ring is
+//    idle: it arms a barrier with the bytes to come, tells the other CTA, sends
+//    the other CTA's half of its accumulator columns into that CTA's ring
+//    (st.async, counted on its barrier), waits for its own half, adds the two K
+//    halves (rank 0's first) and stores its half of the tile's y.  The producer
+//    refills the ring for the next tile only after the epilogue is done with
+//    the received partials.  Cluster barriers after set-up and before exit.
 //  * Batches wider than 128 MB rows run in passes.
 //  * Every wait on a barrier is bounded in time; on a give-up the block records
 //    a code, lets every role stop, waits for its own copies and MMAs, and frees
