@@ -493,19 +493,25 @@ def test_tuned_plan_is_valid_and_correct(dep, orc):
         dep.dep_projection_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("B", [2, 8, 40])
-def test_pdl_chain_respects_data_dependencies(dep, B):
+@pytest.mark.parametrize("B,N,splits", [(2, 2048, None), (8, 2048, None), (40, 2048, None), (64, 7168, 0),
+                                         (128, 7168, 2)])
+def test_pdl_chain_respects_data_dependencies(dep, B, N, splits):
     """With DEP_PLAN_PDL each kernel streams its first weight tiles before the
     preceding kernel finishes, but reads x only after it: a chain where every
     call's output is the next call's input (kernels back to back, outputs
     allocated beforehand) gives exactly the bits of the same chain without
-    overlap -- eagerly and replayed from a CUDA graph."""
-    N = K = 2048
+    overlap -- eagerly and replayed from a CUDA graph.  At 7168 x 7168 the x-on-M
+    kind serves 64 rows with whole K per block and 128 rows in pairs of blocks
+    (splits = 2), whose epilogue exchanges partials inside each cluster."""
+    K = N
     Ws = [to_dev(synth.normal_bf16(20 + i, 1, (N, K), sigma=0.02)) for i in range(6)]
     x0 = to_dev(synth.normal_bf16(20, 2, (B, K)))
     plain = dep.dep_projection_plan(N, K, [B])
     pdl = dep.dep_projection_plan(N, K, [B], dep.DEP_PLAN_PDL)
     try:
+        if splits is not None:
+            t = dep.dep_projection_plan_query(pdl, B)
+            assert (t.kind, t.splits) == (dep.DEP_KIND_TC_XM, splits)
         def chain(plan, outs, stream=None):
             x = x0
             for W, y in zip(Ws, outs):
