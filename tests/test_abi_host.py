@@ -184,6 +184,40 @@ def test_plan_set_validates_and_inserts(dep):
         dep.dep_projection_plan_destroy(plan)
 
 
+@pytest.mark.parametrize("fields,ok", [
+    ({}, True),                                            # 96-row tiles, one block of rows, 4 stages of 2 slices
+    ({"tile_n": 104}, False),                              # MMA N must be a multiple of 16
+    ({"tile_n": 272}, False),                              # ... up to 256
+    ({"cols": 192}, False),                                # one or two blocks of 128 rows
+    ({"tile_k": 192}, False),                              # 1, 2 or 4 slices per stage
+    ({"stages": 5}, False),                                # 5 x 56 KB does not fit in shared memory
+    ({"splits": 1}, True),                                 # 1 = whole K, as 0
+    ({"splits": 3}, False),                                # pairs only
+    ({"splits": 2}, True),                                 # pairs of blocks on 96-row tiles
+    ({"splits": 2, "tile_n": 80}, False),                  # pairs need a multiple of 32
+    ({"splits": 2, "ctas": 1}, False),                     # ... and at least one pair
+    ({"splits": 2, "cols": 256, "tile_n": 192, "tile_k": 64, "stages": 4}, True),  # DSA at 256 rows
+    ({"splits": 2, "cols": 256, "tile_n": 256, "tile_k": 64, "stages": 2}, False),  # partials > the ring
+])
+def test_x_on_m_tactic_validation(dep, fields, ok):
+    """The x-on-M kind's tactic fields (DEP_KIND_TC_XM): MMA N (tile_n), blocks
+    of batch rows per pass (cols), slices per stage (tile_k), ring depth that
+    fits beside x at 128 rows, and pairs (splits = 2), whose ring must also hold
+    the other block's partials."""
+    plan = dep.dep_projection_plan_host(14560, 7168, [128], 152)
+    try:
+        t = dep.dep_tactic_t(**{**dict(max_rows=100, kind=dep.DEP_KIND_TC_XM, ctas=152, tile_n=96, tile_k=128,
+                                       stages=4, cols=128, splits=0), **fields})
+        if ok:
+            dep.dep_projection_plan_set(plan, t)
+            assert dep.dep_projection_plan_query(plan, 100).as_dict() == t.as_dict()
+        else:
+            with pytest.raises(dep.DepError):
+                dep.dep_projection_plan_set(plan, t)
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
 def test_plan_save_format(dep, tmp_path):
     plan = dep.dep_projection_plan_host(49376, 7168, [1, 4, 8, 16], 152)
     try:
