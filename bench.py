@@ -68,7 +68,8 @@ TUNED_BY_DEFAULT = {"dsa_verify", "tp_sharded"}
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (context beside the measured ceilings)
 KERNEL_SOURCES = {"splitk_fma": ["splitk_fma.cu"], "tc_gemm": ["tc_gemm.cu", "exchange.cuh"],
                   "tc_split": ["tc_split.cu", "exchange.cuh"], "rows_gemv": ["rows_gemv.cu"],
-                  "tc_wide": ["tc_wide.cu"], "tc_cluster": ["tc_cluster.cu", "cluster.cuh"], "tc_xm": ["tc_xm.cu", "cluster.cuh"]}
+                  "tc_wide": ["tc_wide.cu"], "tc_cluster": ["tc_cluster.cu", "cluster.cuh"], "tc_xm": ["tc_xm.cu", "cluster.cuh"],
+                  "mma_rows": ["mma_rows.cu"]}
 SHARED_SOURCES = ["ptx.cuh", "internal.h"]
 
 
@@ -442,6 +443,8 @@ def kernel_name(t) -> str:
     if t.kind == dep.DEP_KIND_TC_CLUSTER:
         g = "1.5" if t.tile_n == 192 else str(t.tile_n // 128)  # 192 rows: a 128-row and a 64-row tile
         return f"tc_cluster_n{t.cols}_g{g}_k{t.splits}"
+    if t.kind == dep.DEP_KIND_WARP_MMA:  # warp-level MMAs on 16-row tiles, no tensor memory
+        return f"mma_rows_k{t.tile_k}"
     if t.kind == dep.DEP_KIND_TC_XM:  # x on the MMA's M side: blocks of 128 batch rows, tiles of tile_n rows
         return f"tc_xm_m{t.cols}_r{t.tile_n}" + ("_pairs" if t.splits == 2 else "")
     return f"tc_gemm_n{t.cols}"

@@ -102,6 +102,13 @@ typedef enum {
                                  memory; no workspace either way; `stages` of
                                  tile_k = 64, 128 or 256 columns of the weight and
                                  of x */
+#define DEP_KIND_WARP_MMA 8   /* warp-level mma.sync for small weights at up to 16
+                                 rows: one block per tile of tile_n = 16 weight
+                                 rows, whole K per block, cols = 16 batch rows per
+                                 pass, stages of tile_k = 64, 128 or 256 columns;
+                                 no tensor memory, a small ring, so several blocks
+                                 (of one call and of the next) share an SM; `ctas`
+                                 is not used (one block per tile) */
 
 /* One table entry: the tactic that serves batches of up to max_rows rows. */
 typedef struct {

@@ -32,6 +32,7 @@ DEP_KIND_TC_SPLIT = 4
 DEP_KIND_TC_WIDE = 5
 DEP_KIND_TC_CLUSTER = 6
 DEP_KIND_TC_XM = 7
+DEP_KIND_WARP_MMA = 8
 DEP_PLAN_DEFAULT = 0
 DEP_PLAN_TUNE = 1
 DEP_PLAN_PDL = 2

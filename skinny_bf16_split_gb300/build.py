@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libdep_projection.so")
-SOURCES = ["api.cpp", "tma.cpp", "splitk_fma.cu", "tc_gemm.cu", "tc_split.cu", "tc_wide.cu", "tc_cluster.cu", "tc_xm.cu", "rows_gemv.cu", "staging.cu", "probe.cu"]
+SOURCES = ["api.cpp", "tma.cpp", "splitk_fma.cu", "tc_gemm.cu", "tc_split.cu", "tc_wide.cu", "tc_cluster.cu", "tc_xm.cu", "mma_rows.cu", "rows_gemv.cu", "staging.cu", "probe.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "exchange.cuh", "cluster.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -82,6 +82,8 @@ bool tactic_valid(const dep_tactic_t &t)
         return dep::cluster_valid(t);
     if (t.kind == DEP_KIND_TC_XM)
         return dep::xm_valid(t);
+    if (t.kind == DEP_KIND_WARP_MMA)
+        return dep::mma_rows_valid(t);
     if (t.splits != 0)
         return false;  // only the K-piece tactic has pieces
     if (t.kind == DEP_KIND_SPLITK_FMA)
@@ -109,6 +111,7 @@ int64_t effective_ctas(const dep_tactic_t &t, int64_t N, int64_t K)
                       : t.kind == DEP_KIND_TC       ? dep::tc_units(t, N, K)
                       : t.kind == DEP_KIND_TC_WIDE  ? dep::wide_units(t, N, K)
                       : t.kind == DEP_KIND_TC_XM    ? dep::xm_tiles(t, N)
+                      : t.kind == DEP_KIND_WARP_MMA ? dep::mma_rows_tiles(t, N)
                                                     : dep::rows_tiles(t, N);
     return U < t.ctas ? U : t.ctas;
 }
@@ -163,6 +166,7 @@ size_t tactic_counters(const dep_tactic_t &t, int64_t N, int64_t K)
     case DEP_KIND_TC_WIDE: return (size_t)effective_ctas(t, N, K) * dep::wide_flags_per_cta(t);  // flags
     case DEP_KIND_TC_CLUSTER: return 0;  // partials stay in the cluster's shared memory
     case DEP_KIND_TC_XM: return 0;       // whole K per block: no partials, no counters
+    case DEP_KIND_WARP_MMA: return 0;    // whole K per block
     case DEP_KIND_TC_SPLIT: return dep::tcs_counters(t, N);
     default: return 2;  // tile dispenser and finish count (the last two counters)
     }
@@ -257,6 +261,19 @@ int32_t xm_rows_per_tile(int64_t N, int sm_count)
     return (int32_t)std::max<int64_t>(16, (per + 15) / 16 * 16);
 }
 
+dep_tactic_t mma_rows_tactic(int32_t rows, int32_t tile_k, int32_t stages)
+{
+    dep_tactic_t t{};
+    t.max_rows = rows;
+    t.kind = DEP_KIND_WARP_MMA;
+    t.ctas = 1;  // one block per 16-row tile whatever this says
+    t.tile_n = 16;
+    t.tile_k = tile_k;
+    t.stages = stages;
+    t.cols = 16;
+    return t;
+}
+
 // Weight rows per tile of the x-on-M kind in pairs of blocks (a cluster of two,
 // each half of K): the smallest multiple of 32 that deals the rows out to the
 // SMs / 2 pairs in as few waves as tiles of at most 256 rows allow.  DSA 14560:
@@ -348,6 +365,25 @@ dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
         }
         if (t.kind != 0)
             return t;
+    }
+    // 6 to 16 rows where tiles of 16 weight rows number 2.5 to 4 per SM (o_proj
+    // 7168 rows and its TP shards, the TP-2 DSA shard: 448-455 tiles on 152
+    // SMs): the warp-level MMA kind, which holds no tensor memory, so three of
+    // its blocks share an SM and the next call's blocks stream beside the
+    // current call's.  Measured on GB300 per call (CUDA graph + PDL, weights
+    // past L2), B = 16: o_proj 27.7 against 28.5 us for 64-row K-piece tiles;
+    // the 8-layer chain as one graph 489.5 against 496.8 us; TP shards o_proj
+    // K = 6144 / 3072 / 1536: 15.0 / 8.8 / 5.3 against 16.3 / 9.8 / 5.9 us, DSA
+    // 7280 rows 17.2 against 18.6 us.  Slower with fewer tiles per SM (3640 DSA
+    // rows: 13.9 against 11.6 us), with more (14560: 33.6 against 32.7 us), and
+    // at up to 4 rows (o_proj B = 4: 33.1 against 28.3 us).
+    if (rows >= 6 && rows <= 16) {
+        const int64_t t16 = (N + 15) / 16;
+        if (2 * t16 >= 5 * (int64_t)sm_count && t16 <= 4 * (int64_t)sm_count) {
+            const dep_tactic_t t = mma_rows_tactic(rows, 256, K <= 2048 ? 3 : 4);
+            if (dep::mma_rows_valid(t))
+                return t;
+        }
     }
     // Up to 32 batch rows on long weight rows (K >= 3072) whose 64-row tiles fit
     // on the SMs: 64-row K-piece tiles in as few pieces as fill the SMs (o_proj:
@@ -573,6 +609,7 @@ dep_status_t make_plan(int64_t N, int64_t K, const int32_t *batches, int32_t n_b
         if (dep::fma_prepare_device() != cudaSuccess || dep::tc_prepare_device() != cudaSuccess ||
             dep::tcs_prepare_device() != cudaSuccess || dep::wide_prepare_device() != cudaSuccess ||
             dep::cluster_prepare_device() != cudaSuccess || dep::xm_prepare_device() != cudaSuccess ||
+            dep::mma_rows_prepare_device() != cudaSuccess ||
             dep::rows_prepare_device() != cudaSuccess) {
             cudaGetLastError();
             delete p;
@@ -650,6 +687,7 @@ dep_status_t run_impl(dep_plan_t p, const dep_tactic_t *t, const void *x, const 
                     : t->kind == DEP_KIND_TC_WIDE  ? dep::wide_run(*t, a)
                     : t->kind == DEP_KIND_TC_CLUSTER ? dep::cluster_run(*t, a)
                     : t->kind == DEP_KIND_TC_XM    ? dep::xm_run(*t, a)
+                    : t->kind == DEP_KIND_WARP_MMA ? dep::mma_rows_run(*t, a)
                                                    : dep::rows_run(*t, a);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -769,6 +807,11 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
                 }
         }
     }
+    // Warp-level MMAs on 16-row tiles (no tensor memory), up to 16 rows.
+    if (rows <= 16)
+        for (int32_t tk : {128, 256})
+            for (int32_t st : {3, 4, 6})
+                c.push_back(mma_rows_tactic(rows, tk, st));
     // K pieces keep every piece's partial: leave out tactics whose exchange words
     // would take more than 64 MB.
     constexpr size_t kMaxPieceWords = (64u << 20) / 8;

@@ -87,6 +87,7 @@ cudaError_t tcs_prepare_device();
 cudaError_t wide_prepare_device();
 cudaError_t cluster_prepare_device();
 cudaError_t xm_prepare_device();
+cudaError_t mma_rows_prepare_device();
 
 // Launch with the programmatic-stream-serialisation attribute when `pdl` is set.
 template <typename Kernel, typename... Args>
@@ -214,6 +215,11 @@ int64_t xm_tiles(const dep_tactic_t &t, int64_t N);
 // x blocks have mr = 64 or 128 rows.
 int xm_stages_fit(int32_t tile_n, int32_t tile_k, int32_t cols, int mr);
 cudaError_t xm_run(const dep_tactic_t &t, const RunArgs &a);
+
+// ---- warp-level MMA tactic for small weights (mma_rows.cu) ----
+bool mma_rows_valid(const dep_tactic_t &t);
+int64_t mma_rows_tiles(const dep_tactic_t &t, int64_t N);
+cudaError_t mma_rows_run(const dep_tactic_t &t, const RunArgs &a);
 
 // ---- whole-row tactic (rows_gemv.cu) ----
 bool rows_valid(const dep_tactic_t &t);

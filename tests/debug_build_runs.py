@@ -59,6 +59,8 @@ def main():
                            cols=256)),
             ("x-on-m-pairs", T(max_rows=4096, kind=dep.DEP_KIND_TC_XM, ctas=6, tile_n=64, tile_k=64, stages=4,
                                cols=256, splits=2)),
+            ("warp-mma", T(max_rows=8192, kind=dep.DEP_KIND_WARP_MMA, ctas=1, tile_n=16, tile_k=256, stages=3,
+                           cols=16)),
         ]
 
     # K = 2048 and 1088 (multiples of 64) take the one-copy column-block stage

@@ -53,15 +53,34 @@ def test_default_table_follows_split_rule(dep):
         table = dep.dep_projection_plan_table(plan)
         assert [t.max_rows for t in table] == [1, 2, 4, 8, 16]
         for t in table:
-            assert t.ctas >= 152 and t.stages >= 2
-            assert t.kind in (dep.DEP_KIND_SPLITK_FMA, dep.DEP_KIND_TC, dep.DEP_KIND_ROWS,
-                              dep.DEP_KIND_TC_SPLIT)
+            assert t.stages >= 2
             if t.max_rows <= 2:  # the smallest batches: warp split-K over whole rows
-                assert t.kind == dep.DEP_KIND_ROWS
-            else:  # long rows, 112 tiles of 64 rows on 152 SMs: one tile per block, one piece
+                assert t.kind == dep.DEP_KIND_ROWS and t.ctas >= 152
+            elif t.max_rows <= 4:  # long rows, 112 tiles of 64 rows on 152 SMs: one tile per block, one piece
                 assert (t.kind, t.tile_n, t.splits, t.cols) == (dep.DEP_KIND_TC_SPLIT, 64, 1, 16)
+            else:  # 448 tiles of 16 rows, about 3 per SM: warp-level MMAs, no tensor memory
+                assert (t.kind, t.tile_n, t.tile_k, t.stages, t.cols) == (dep.DEP_KIND_WARP_MMA, 16, 256, 4, 16)
         for B, key in [(1, 1), (3, 4), (5, 8), (16, 16), (17, 16), (1000, 16)]:
             assert dep.dep_projection_plan_query(plan, B).max_rows == key
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("N,K,rows,expect", [
+    (7168, 12288, 16, True), (7168, 1536, 8, True), (7280, 7168, 16, True),   # 448-455 tiles of 16 rows
+    (7168, 12288, 4, False),                                                   # too few rows
+    (3640, 7168, 16, False), (14560, 7168, 16, False),                         # 228 / 910 tiles
+])
+def test_default_rule_warp_mma(dep, N, K, rows, expect):
+    """The warp-level MMA kind (DEP_KIND_WARP_MMA) is the default for 6-16 rows
+    where tiles of 16 weight rows number 2.5 to 4 per SM, with 3 stages of 256
+    columns at K <= 2048 and 4 above."""
+    plan = dep.dep_projection_plan_host(N, K, [rows], 152)
+    try:
+        t = dep.dep_projection_plan_query(plan, rows)
+        assert (t.kind == dep.DEP_KIND_WARP_MMA) == expect, t
+        if expect:
+            assert (t.tile_n, t.cols, t.tile_k, t.stages) == (16, 16, 256, 3 if K <= 2048 else 4)
     finally:
         dep.dep_projection_plan_destroy(plan)
 

@@ -398,18 +398,19 @@ def test_tc_parity_vs_oracle(dep, orc, plan_cache, N, K, NT, tile_k):
     assert dep.dep_projection_device_status(plan) == 0
 
 
-@pytest.mark.parametrize("B", [5, 16, 64])
+@pytest.mark.parametrize("B", [4, 16, 64])
 @pytest.mark.parametrize("which", ["default", "stream-k"])
 def test_tc_determinism_and_graph_replay(dep, plan_cache, B, which):
     """The tensor-core kernels' split-K combinations are order-fixed: repeated
     runs and CUDA-graph replays give identical bits (the default plan takes the
-    K-piece kernel for this weight up to 16 rows and x on the MMA's M side at 64
-    rows; the stream-K kernel is installed explicitly)."""
+    K-piece kernel for this weight at 4 rows, warp-level MMAs on its 448 tiles of
+    16 rows at 16, and x on the MMA's M side at 64 rows; the stream-K kernel is
+    installed explicitly)."""
     N, K = 7168, 4096
     x, W = to_dev(synth.normal_bf16(B, 2, (B, K))), to_dev(synth.normal_bf16(5, 1, (N, K), 0.02))
     if which == "default":
         plan = get_plan(dep, plan_cache, N, K)
-        want = dep.DEP_KIND_TC_SPLIT if B <= 16 else dep.DEP_KIND_TC_XM
+        want = {4: dep.DEP_KIND_TC_SPLIT, 16: dep.DEP_KIND_WARP_MMA, 64: dep.DEP_KIND_TC_XM}[B]
         assert dep.dep_projection_plan_query(plan, B).kind == want
     else:
         plan = get_plan(dep, plan_cache, N, K, (B,))
@@ -493,25 +494,28 @@ def test_tuned_plan_is_valid_and_correct(dep, orc):
         dep.dep_projection_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("B,N,splits", [(2, 2048, None), (8, 2048, None), (40, 2048, None), (64, 7168, 0),
-                                         (128, 7168, 2)])
-def test_pdl_chain_respects_data_dependencies(dep, B, N, splits):
+@pytest.mark.parametrize("B,N,kind", [(2, 2048, None), (8, 2048, None), (40, 2048, None), (16, 7168, "warp"),
+                                       (64, 7168, "xm"), (128, 7168, "xm-pairs")])
+def test_pdl_chain_respects_data_dependencies(dep, B, N, kind):
     """With DEP_PLAN_PDL each kernel streams its first weight tiles before the
     preceding kernel finishes, but reads x only after it: a chain where every
     call's output is the next call's input (kernels back to back, outputs
     allocated beforehand) gives exactly the bits of the same chain without
-    overlap -- eagerly and replayed from a CUDA graph.  At 7168 x 7168 the x-on-M
-    kind serves 64 rows with whole K per block and 128 rows in pairs of blocks
-    (splits = 2), whose epilogue exchanges partials inside each cluster."""
+    overlap -- eagerly and replayed from a CUDA graph.  At 7168 x 7168 the warp
+    MMA kind serves 16 rows (its blocks of consecutive calls share SMs), the x-on-M
+    kind 64 rows with whole K per block and 128 rows in pairs of blocks, whose
+    epilogue exchanges partials inside each cluster."""
     K = N
     Ws = [to_dev(synth.normal_bf16(20 + i, 1, (N, K), sigma=0.02)) for i in range(6)]
     x0 = to_dev(synth.normal_bf16(20, 2, (B, K)))
     plain = dep.dep_projection_plan(N, K, [B])
     pdl = dep.dep_projection_plan(N, K, [B], dep.DEP_PLAN_PDL)
     try:
-        if splits is not None:
-            t = dep.dep_projection_plan_query(pdl, B)
-            assert (t.kind, t.splits) == (dep.DEP_KIND_TC_XM, splits)
+        t = dep.dep_projection_plan_query(pdl, B)
+        if kind == "warp":
+            assert t.kind == dep.DEP_KIND_WARP_MMA
+        elif kind is not None:
+            assert (t.kind, t.splits) == (dep.DEP_KIND_TC_XM, 2 if kind == "xm-pairs" else 0)
         def chain(plan, outs, stream=None):
             x = x0
             for W, y in zip(Ws, outs):
