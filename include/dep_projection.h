@@ -104,11 +104,13 @@ typedef enum {
                                  of x */
 #define DEP_KIND_WARP_MMA 8   /* warp-level mma.sync for small weights at up to 16
                                  rows: one block per tile of tile_n = 16 weight
-                                 rows, whole K per block, cols = 16 batch rows per
-                                 pass, stages of tile_k = 64, 128 or 256 columns;
-                                 no tensor memory, a small ring, so several blocks
-                                 (of one call and of the next) share an SM; `ctas`
-                                 is not used (one block per tile) */
+                                 rows and whole K (splits = 0 or 1), or a cluster of
+                                 splits = 2 or 4 blocks per tile, each a K piece,
+                                 added in rank order in the first block's shared
+                                 memory; cols = 16 batch rows per pass, stages of
+                                 tile_k = 64, 128 or 256 columns; no tensor memory,
+                                 a small ring, so several blocks (of one call and
+                                 of the next) share an SM; `ctas` is not used */
 
 /* One table entry: the tactic that serves batches of up to max_rows rows. */
 typedef struct {
@@ -125,7 +127,8 @@ typedef struct {
                          TC_XM: 128 or 256, MMA M = 128 per block of rows) */
     int32_t splits;   /* TC_SPLIT: K pieces per tile, 1..64 (capped at the tile's
                          k-tiles, ceil(K / tile_k)); TC_CLUSTER: CTAs per cluster;
-                         TC_XM: 0, or 2 for pairs of blocks; 0 for the other kinds */
+                         TC_XM: 0, or 2 for pairs of blocks; WARP_MMA: K pieces
+                         per tile, 0/1, 2 or 4; 0 for the other kinds */
 } dep_tactic_t;
 
 /* Plan flags. */

@@ -807,11 +807,16 @@ std::vector<dep_tactic_t> candidates(int32_t rows, int64_t N, int64_t K, int sm_
                 }
         }
     }
-    // Warp-level MMAs on 16-row tiles (no tensor memory), up to 16 rows.
+    // Warp-level MMAs on 16-row tiles (no tensor memory), up to 16 rows: whole
+    // K per block, or two K pieces per tile in a cluster.
     if (rows <= 16)
-        for (int32_t tk : {128, 256})
-            for (int32_t st : {3, 4, 6})
-                c.push_back(mma_rows_tactic(rows, tk, st));
+        for (int32_t sp : {0, 2})
+            for (int32_t tk : {128, 256})
+                for (int32_t st : {3, 4, 6}) {
+                    dep_tactic_t t = mma_rows_tactic(rows, tk, st);
+                    t.splits = sp;
+                    c.push_back(t);
+                }
     // K pieces keep every piece's partial: leave out tactics whose exchange words
     // would take more than 64 MB.
     constexpr size_t kMaxPieceWords = (64u << 20) / 8;

@@ -17,8 +17,11 @@
 // the next, under programmatic dependent launch -- share an SM.
 //
 // Design (sm_103a):
-//  * One block per tile of 16 weight rows; the block sums the tile's whole K
-//    (no split, no workspace).  Warp 0 lane 0 issues TMA copies: per stage a
+//  * One block per tile of 16 weight rows sums the tile's whole K, or (splits
+//    = 2 or 4, for long rows on few tiles) the S blocks of a thread-block
+//    cluster each sum a contiguous piece of the 64-column slices and store
+//    their 16 x 16 FP32 partials into rank 0's shared memory, which adds them
+//    in rank order after a cluster barrier (no workspace either way).  Warp 0 lane 0 issues TMA copies: per stage a
 //    box of `atoms` 64-column slices of the tile's 16 rows (one copy through the
 //    column-block view when K % 64 == 0) and the same slices of x (16 rows,
 //    rows past B zero), 128-byte swizzle.  Weight first, before waiting for the
@@ -33,6 +36,7 @@
 //  * Every wait on a barrier is bounded in time.
 #include <cuda_bf16.h>
 
+#include "cluster.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -46,13 +50,16 @@ constexpr int kComp = 4;             // compute warps
 constexpr int kThreads = 32 * (1 + kComp);
 constexpr int kSlice = kTR * kBK * 2;  // one weight slice: 2 KB (x slices are the same size)
 constexpr int kMaxStages = 16;
+constexpr int kMaxPieces = 4;        // K pieces of a tile: blocks of one cluster
 
 __host__ __device__ constexpr int mr_stage(int atoms) { return 2 * atoms * kSlice; }
 // Shared memory: the 1 KB-aligned ring (per stage: the weight slices, then the
-// x slices), the four warps' partials, full[stages], empty[stages], the abort flag.
+// x slices), the four warps' partials, the K pieces' partials (rank 0 of a
+// cluster), full[stages], empty[stages], the abort flag.
 __host__ __device__ constexpr size_t mr_smem_bytes(int stages, int atoms)
 {
-    return 1024 + (size_t)stages * mr_stage(atoms) + (size_t)kComp * kTR * kXR * 4 + (size_t)2 * stages * 8 + 16;
+    return 1024 + (size_t)stages * mr_stage(atoms) + (size_t)(kComp + kMaxPieces) * kTR * kXR * 4 +
+           (size_t)2 * stages * 8 + 16;
 }
 
 // Four 8x8 BF16 matrices from shared memory (rows addressed per lane).
@@ -79,6 +86,12 @@ __device__ __forceinline__ uint32_t swz(uint32_t slice, int r, int c)
     return slice + (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// Store into the shared memory of a CTA of this cluster (a mapped address).
+__device__ __forceinline__ void st_cluster_f32(uint32_t a, float v)
+{
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
 // Compute warps only (named barrier 1).
 __device__ __forceinline__ void comp_sync()
 {
@@ -87,7 +100,7 @@ __device__ __forceinline__ void comp_sync()
 
 __global__ void __launch_bounds__(kThreads)
     mma_rows_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms, int tma3,
+                    uint16_t *__restrict__ y, int B, int N, int K, int stages, int atoms, int tma3, int S,
                     int *__restrict__ status, const Bounds bd, uint64_t limit_ns)
 {
     extern __shared__ uint8_t smem_raw[];
@@ -98,13 +111,19 @@ __global__ void __launch_bounds__(kThreads)
         return;
     const int STAGE = mr_stage(atoms), XOFF = atoms * kSlice;
     float *part = reinterpret_cast<float *>(smem + (size_t)stages * STAGE);  // [warp][row][batch row]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(part + kComp * kTR * kXR);
+    float *red = part + kComp * kTR * kXR;                                    // [piece][row][batch row]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(red + kMaxPieces * kTR * kXR);
     const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * stages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * stages);
 
-    const int KT = (K + kBK - 1) / kBK;       // 64-column slices
-    const int KS = (KT + atoms - 1) / atoms;  // stages
-    const int row0 = (int)blockIdx.x * kTR;   // this block's tile
+    // With S > 1 the S blocks of a cluster share a tile: rank r sums the
+    // 64-column slices [r KT / S, (r + 1) KT / S) and rank 0 adds the pieces.
+    const int rank = S > 1 ? (int)cluster_rank() : 0;
+    const int KT_ALL = (K + kBK - 1) / kBK;
+    const int S0 = rank * KT_ALL / S;                   // this block's first slice
+    const int KT = (rank + 1) * KT_ALL / S - S0;        // its slices
+    const int KS = (KT + atoms - 1) / atoms;            // stages
+    const int row0 = (int)(blockIdx.x / (unsigned)S) * kTR;  // the tile
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     auto slices_of = [&](int k) { return KT - k * atoms < atoms ? KT - k * atoms : atoms; };
     const int pre = KS < stages ? KS : stages;
@@ -115,19 +134,19 @@ __global__ void __launch_bounds__(kThreads)
         const int na = slices_of(k);
         mbar_arrive_expect_tx(bar, (uint32_t)((tma3 ? atoms : na) * 2 * kSlice));  // weight and x
         if (tma3) {
-            tma_load_3d(dst, &tmW, 0, row0, k * atoms, bar, pol_w);
+            tma_load_3d(dst, &tmW, 0, row0, S0 + k * atoms, bar, pol_w);
         } else {
             for (int a = 0; a < na; ++a)
-                tma_load_2d(dst + (uint32_t)(a * kSlice), &tmW, (k * atoms + a) * kBK, row0, bar, pol_w);
+                tma_load_2d(dst + (uint32_t)(a * kSlice), &tmW, (S0 + k * atoms + a) * kBK, row0, bar, pol_w);
         }
     };
     auto issue_x = [&](int st, int k) {
         const uint32_t dst = base + (uint32_t)(st * STAGE + XOFF), bar = full0 + 8 * st;
         if (tma3) {
-            tma_load_3d(dst, &tmX, 0, 0, k * atoms, bar, pol_x);
+            tma_load_3d(dst, &tmX, 0, 0, S0 + k * atoms, bar, pol_x);
         } else {
             for (int a = 0; a < slices_of(k); ++a)
-                tma_load_2d(dst + (uint32_t)(a * kSlice), &tmX, (k * atoms + a) * kBK, 0, bar, pol_x);
+                tma_load_2d(dst + (uint32_t)(a * kSlice), &tmX, (S0 + k * atoms + a) * kBK, 0, bar, pol_x);
         }
     };
 
@@ -148,7 +167,13 @@ __global__ void __launch_bounds__(kThreads)
             issue_w(i, i);
     }
     __syncthreads();
+    if (S > 1)
+        cluster_sync();  // every block of the cluster has started
 
+    // Epilogue state of a compute thread: its batch row, first weight row, sums.
+    int en = 0, er = 0;
+    float ev[2] = {0.f, 0.f};
+    bool eok = false;
     if (warp == 0) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
@@ -241,27 +266,45 @@ __global__ void __launch_bounds__(kThreads)
             p[(r + 8) * kXR + 8 + c + 1] = acc1[3];
         }
         comp_sync();
-        griddep_wait();  // y may still be in use by the preceding grid
-        const int t = threadIdx.x - 32;     // 0..127
-        const int n = t >> 3, r = 2 * (t & 7);  // batch row, first of two weight rows
-        if (ok && n < B && row0 + r < N) {
-            float v[2];
+        const int t = threadIdx.x - 32;          // 0..127
+        en = t >> 3;                             // batch row
+        er = 2 * (t & 7);                        // first of two weight rows
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int i = (r + j) * kXR + n;
-                v[j] = ((part[i] + part[kTR * kXR + i]) + part[2 * kTR * kXR + i]) + part[3 * kTR * kXR + i];
+        for (int j = 0; j < 2; ++j) {
+            const int i = (er + j) * kXR + en;
+            ev[j] = ((part[i] + part[kTR * kXR + i]) + part[2 * kTR * kXR + i]) + part[3 * kTR * kXR + i];
+        }
+        eok = ok;
+        if (S > 1) {  // this block's piece into rank 0's slot `rank`
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                st_cluster_f32(peer_addr(smem_u32(red + (rank * kTR + er + j) * kXR + en), 0u), ev[j]);
+        }
+    }
+    if (S > 1) {
+        cluster_sync();  // the pieces are in rank 0; no block leaves while another may write into it
+        if (rank == 0 && warp >= 1) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {  // the pieces in rank order
+                float v = red[(er + j) * kXR + en];
+                for (int p = 1; p < S; ++p)
+                    v = v + red[(p * kTR + er + j) * kXR + en];
+                ev[j] = v;
             }
-            uint16_t *yr = y + (int64_t)n * N + row0 + r;
-            const bool pair = row0 + r + 1 < N;
-            if (pair && (N & 1) == 0 && dbg_ok((int64_t)n * N + row0 + r + 1, bd.y, status)) {
-                *reinterpret_cast<uint32_t *>(yr) = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[0])) |
-                                                    ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(v[1])) << 16);
-            } else {
-                if (dbg_ok((int64_t)n * N + row0 + r, bd.y, status))
-                    yr[0] = __bfloat16_as_ushort(__float2bfloat16_rn(v[0]));
-                if (pair && dbg_ok((int64_t)n * N + row0 + r + 1, bd.y, status))
-                    yr[1] = __bfloat16_as_ushort(__float2bfloat16_rn(v[1]));
-            }
+        }
+    }
+    if (warp >= 1 && rank == 0 && eok && en < B && row0 + er < N) {
+        griddep_wait();  // y may still be in use by the preceding grid
+        uint16_t *yr = y + (int64_t)en * N + row0 + er;
+        const bool two = row0 + er + 1 < N;
+        if (two && (N & 1) == 0 && dbg_ok((int64_t)en * N + row0 + er + 1, bd.y, status)) {
+            *reinterpret_cast<uint32_t *>(yr) = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ev[0])) |
+                                                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(ev[1])) << 16);
+        } else {
+            if (dbg_ok((int64_t)en * N + row0 + er, bd.y, status))
+                yr[0] = __bfloat16_as_ushort(__float2bfloat16_rn(ev[0]));
+            if (two && dbg_ok((int64_t)en * N + row0 + er + 1, bd.y, status))
+                yr[1] = __bfloat16_as_ushort(__float2bfloat16_rn(ev[1]));
         }
     }
 }
@@ -282,8 +325,10 @@ cudaError_t prepare()
 
 bool mma_rows_valid(const dep_tactic_t &t)
 {
-    if (t.kind != DEP_KIND_WARP_MMA || t.ctas < 1 || t.splits != 0 || t.tile_n != kTR || t.cols != kXR)
+    if (t.kind != DEP_KIND_WARP_MMA || t.ctas < 1 || t.tile_n != kTR || t.cols != kXR)
         return false;  // tiles of 16 weight rows, passes of 16 batch rows
+    if (t.splits != 0 && t.splits != 1 && t.splits != 2 && t.splits != kMaxPieces)
+        return false;  // K pieces per tile: 1 (0), 2 or 4 blocks of a cluster
     if (t.tile_k != kBK && t.tile_k != 2 * kBK && t.tile_k != 4 * kBK)
         return false;  // 1, 2 or 4 slices of 64 columns per stage
     if (t.stages < 2 || t.stages > kMaxStages)
@@ -291,9 +336,9 @@ bool mma_rows_valid(const dep_tactic_t &t)
     return mr_smem_bytes(t.stages, t.tile_k / kBK) <= (size_t)kMaxDynamicSmem;
 }
 
-int64_t mma_rows_tiles(const dep_tactic_t &, int64_t N)
+int64_t mma_rows_tiles(const dep_tactic_t &t, int64_t N)
 {
-    return (N + kTR - 1) / kTR;
+    return (N + kTR - 1) / kTR * (t.splits > 1 ? t.splits : 1);  // blocks of a launch
 }
 
 cudaError_t mma_rows_prepare_device()
@@ -315,8 +360,13 @@ cudaError_t mma_rows_run(const dep_tactic_t &t, const RunArgs &a)
               : encode_bf16_2d(&tmW, a.W, (uint64_t)a.K, (uint64_t)a.N, kBK, kTR, CU_TENSOR_MAP_SWIZZLE_128B)) !=
         CUDA_SUCCESS)
         return cudaErrorInvalidValue;
-    const int64_t T = (a.N + kTR - 1) / kTR;  // one block per tile
+    const int64_t T = (a.N + kTR - 1) / kTR;  // tiles
     const size_t smem = mr_smem_bytes(t.stages, atoms);
+    // K pieces per tile, each at least one 64-column slice
+    const int64_t KT = (a.K + kBK - 1) / kBK;
+    int S = t.splits > 1 ? t.splits : 1;
+    while (S > 1 && KT < S)
+        S /= 2;
     for (int32_t r0 = 0; r0 < a.B; r0 += kXR) {
         const int32_t rows = a.B - r0 < kXR ? a.B - r0 : kXR;
         const uint16_t *xr = a.x + (size_t)r0 * a.K;
@@ -324,9 +374,22 @@ cudaError_t mma_rows_run(const dep_tactic_t &t, const RunArgs &a)
                   : encode_bf16_2d(&tmX, xr, (uint64_t)a.K, (uint64_t)rows, kBK, kXR, CU_TENSOR_MAP_SWIZZLE_128B)) !=
             CUDA_SUCCESS)
             return cudaErrorInvalidValue;
-        e = launch(mma_rows_kernel, dim3((unsigned)T), dim3(kThreads), smem, a.stream, a.pdl, tmW, tmX,
-                   a.y + (size_t)r0 * a.N, (int)rows, (int)a.N, (int)a.K, t.stages, atoms, tma3, a.status,
-                   a.bounds(rows, smem), a.wait_limit_ns);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(T * S));  // one block per tile and K piece
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = a.stream;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = a.pdl ? 1 : 0;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)S;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = S > 1 ? 2 : 1;
+        e = cudaLaunchKernelEx(&cfg, mma_rows_kernel, tmW, tmX, a.y + (size_t)r0 * a.N, (int)rows, (int)a.N,
+                               (int)a.K, t.stages, atoms, tma3, S, a.status, a.bounds(rows, smem), a.wait_limit_ns);
         if (e != cudaSuccess)
             return e;
     }

@@ -61,6 +61,8 @@ def main():
                                cols=256, splits=2)),
             ("warp-mma", T(max_rows=8192, kind=dep.DEP_KIND_WARP_MMA, ctas=1, tile_n=16, tile_k=256, stages=3,
                            cols=16)),
+            ("warp-mma-pieces", T(max_rows=16384, kind=dep.DEP_KIND_WARP_MMA, ctas=1, tile_n=16, tile_k=128,
+                                  stages=4, cols=16, splits=4)),
         ]
 
     # K = 2048 and 1088 (multiples of 64) take the one-copy column-block stage

@@ -24,4 +24,4 @@ def test_every_kind_on_ragged_shapes_under_bounds_checks():
                        text=True, timeout=1200)
     print(r.stdout[-4000:])
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
-    assert r.stdout.count("status 0, within tolerance True") == 5 * 18  # 5 shapes x (default + 17 tactics)
+    assert r.stdout.count("status 0, within tolerance True") == 5 * 19  # 5 shapes x (default + 18 tactics)

@@ -1,9 +1,10 @@
 """The warp-level MMA tactic for small weights (DEP_KIND_WARP_MMA) against the oracle.
 
-One block per tile of 16 weight rows sums the tile's whole K with mma.sync
-(m16n8k16, BF16 in, FP32 accumulators in registers): four compute warps take
-the 64-column slices g with g % 4 = warp, each in increasing K order, and the
-four partials are added in warp order.  Checked here: the acceptance tolerance
+One block per tile of 16 weight rows sums the tile's whole K (or 2 or 4 blocks
+of a cluster each a K piece, added in rank order in the first block) with
+mma.sync (m16n8k16, BF16 in, FP32 accumulators in registers): four compute
+warps take the 64-column slices g with g % 4 = warp, each in increasing K
+order, and the four partials are added in warp order.  Checked here: the acceptance tolerance
 against the exact oracle on ragged N, K and B (passes of 16 rows), one, two or
 four slices per stage, shallow and deep rings; identical bits whatever the
 stage width and the ring depth; exact small-integer sums; sign symmetry; the
@@ -23,9 +24,9 @@ from skinny_bf16_split_gb300 import synth  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 
-def mma_tactic(dep, tile_k, stages, max_rows=16):
+def mma_tactic(dep, tile_k, stages, max_rows=16, splits=0):
     return dep.dep_tactic_t(max_rows=max_rows, kind=dep.DEP_KIND_WARP_MMA, ctas=1, tile_n=16, tile_k=tile_k,
-                            stages=stages, cols=16)
+                            stages=stages, cols=16, splits=splits)
 
 
 def run(dep, plan, x, W, N, tactic):
@@ -51,12 +52,15 @@ def plans(dep):
         dep.dep_projection_plan_destroy(p)
 
 
-@pytest.mark.parametrize("N,K", [(333, 1000), (97, 264), (1000, 3136), (700, 2048), (7168, 1536)])
-def test_warp_mma_parity_vs_oracle(dep, orc, plans, N, K):
+@pytest.mark.parametrize("N,K", [(333, 1000), (97, 264), (1000, 3136), (700, 2048), (7168, 1536), (3640, 128)])
+@pytest.mark.parametrize("splits", [0, 2, 4])
+def test_warp_mma_parity_vs_oracle(dep, orc, plans, N, K, splits):
     """Ragged last tile (N % 16 != 0), K not a multiple of 64 (one copy per slice,
     a ragged last slice) or of the stage width (one copy per stage, the last
     stage partly past K), batches of 1, 5, 16 rows and 17, 40 (two and three
-    passes); 1, 2 or 4 slices per stage, rings of 2 and 6."""
+    passes); 1, 2 or 4 slices per stage, rings of 2 and 6; whole K per block or
+    2 and 4 K pieces per tile in a cluster (K = 128: two slices, so four pieces
+    run as two)."""
     plan = plans(N, K)
     W = synth.normal_bf16(N + K, 1, (N, K), sigma=0.02)
     for B in (1, 5, 16, 17, 40):
@@ -64,24 +68,26 @@ def test_warp_mma_parity_vs_oracle(dep, orc, plans, N, K):
         ref = orc.linear(x, W)
         for tile_k in (64, 128, 256):
             for st in (2, 6):
-                y = run(dep, plan, x, W, N, mma_tactic(dep, tile_k, st))
+                y = run(dep, plan, x, W, N, mma_tactic(dep, tile_k, st, splits=splits))
                 ok, worst, idx = within_tolerance(y, ref)
                 assert ok, (B, tile_k, st, worst, idx)
 
 
 @pytest.mark.parametrize("B", [3, 16, 29])
-def test_warp_mma_bits_independent_of_stage_width_and_depth(dep, plans, B):
-    """Slice g of a tile goes to compute warp g % 4 whatever the stage width, and
-    each warp adds its slices in K order: identical bits for every tile_k and
-    ring depth."""
+@pytest.mark.parametrize("splits", [0, 2, 4])
+def test_warp_mma_bits_independent_of_stage_width_and_depth(dep, plans, B, splits):
+    """Slice g of a block's piece goes to compute warp g % 4 whatever the stage
+    width, each warp adds its slices in K order, and the pieces are added in
+    rank order: identical bits for every tile_k and ring depth at a given number
+    of pieces."""
     N, K = 1000, 3136
     plan = plans(N, K)
     W = synth.normal_bf16(61, 1, (N, K), sigma=0.02)
     x = synth.normal_bf16(62, 2, (B, K))
-    ref = run(dep, plan, x, W, N, mma_tactic(dep, 256, 4))
+    ref = run(dep, plan, x, W, N, mma_tactic(dep, 256, 4, splits=splits))
     for tile_k in (64, 128, 256):
         for st in (2, 3, 8):
-            np.testing.assert_array_equal(run(dep, plan, x, W, N, mma_tactic(dep, tile_k, st)), ref,
+            np.testing.assert_array_equal(run(dep, plan, x, W, N, mma_tactic(dep, tile_k, st, splits=splits)), ref,
                                           err_msg=str((tile_k, st)))
 
 
@@ -92,7 +98,9 @@ def test_warp_mma_small_integers_exact_and_negation(dep, orc, plans):
     x = np.vectorize(exact_bf16)(rng.integers(-8, 9, (16, K))).astype(np.uint16)
     W = np.vectorize(exact_bf16)(rng.integers(-8, 9, (N, K))).astype(np.uint16)
     plan = plans(N, K)
-    np.testing.assert_array_equal(run(dep, plan, x, W, N, mma_tactic(dep, 256, 4)), orc.linear(x, W))
+    for splits in (0, 2, 4):
+        np.testing.assert_array_equal(run(dep, plan, x, W, N, mma_tactic(dep, 256, 4, splits=splits)),
+                                      orc.linear(x, W))
     xg = synth.normal_bf16(68, 2, (16, K))
     Wg = synth.normal_bf16(68, 1, (N, K), sigma=0.02)
     t = mma_tactic(dep, 128, 4)
