@@ -871,31 +871,48 @@ dep_status_t tune_plan(dep_plan_s *p)
         fill_bf16_kernel<<<64, 256, 0, s>>>(xs, xbytes / 2, 777);
         ok = cudaGetLastError() == cudaSuccess && cudaStreamSynchronize(s) == cudaSuccess;
     }
+    size_t turn = 0;
+    // Batches of 8 back-to-back launches between one pair of events (event
+    // timestamps are coarse, about 2 us on GB300), the best of 3 batches after 2
+    // warm-up launches.  (Timing the same 8 launches as a captured CUDA graph
+    // ranked the candidates of each call alike within 0.1-0.3 us, but the
+    // tables it chose ran the tensor-parallel shard step 9 % slower as one
+    // graph, measured on one GB300, so the launches stay eager.)
+    auto time_launches = [&](const dep_tactic_t &c, int32_t B, float &ms_out) -> bool {
+        for (int w = 0; w < 2; ++w)
+            if (run_impl(p, &c, xs, Wc + (turn++ % copies) * (wbytes / 2), ys, B, s) != DEP_OK)
+                return false;
+        float best_ms = 1e30f;
+        for (int rep = 0; rep < 3; ++rep) {
+            if (cudaEventRecord(e0, s) != cudaSuccess)
+                return false;
+            for (int l = 0; l < 8; ++l)
+                if (run_impl(p, &c, xs, Wc + (turn++ % copies) * (wbytes / 2), ys, B, s) != DEP_OK)
+                    return false;
+            float t = 0;
+            if (cudaEventRecord(e1, s) != cudaSuccess || cudaEventSynchronize(e1) != cudaSuccess ||
+                cudaEventElapsedTime(&t, e0, e1) != cudaSuccess)
+                return false;
+            best_ms = std::min(best_ms, t / 8);
+        }
+        ms_out = best_ms;
+        return true;
+    };
     for (size_t i = 0; ok && i < p->table.size(); ++i) {
         const int32_t B = p->table[i].max_rows;
         float best = 1e30f;
         dep_tactic_t best_t = p->table[i];
-        size_t turn = 0;
-        for (const auto &c : cands[i]) {
-            // Event timestamps are coarse (about 2 us on GB300): time batches of
-            // 8 back-to-back launches between one pair of events; keep the best
-            // of 3 batches, after 2 warm-up launches.
-            for (int w = 0; w < 2 && ok; ++w)
-                ok = run_impl(p, &c, xs, Wc + (turn++ % copies) * (wbytes / 2), ys, B, s) == DEP_OK;
-            std::vector<float> ms;
-            for (int rep = 0; rep < 3 && ok; ++rep) {
-                ok = cudaEventRecord(e0, s) == cudaSuccess;
-                for (int l = 0; l < 8 && ok; ++l)
-                    ok = run_impl(p, &c, xs, Wc + (turn++ % copies) * (wbytes / 2), ys, B, s) == DEP_OK;
-                ok = ok && cudaEventRecord(e1, s) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess;
-                float t = 0;
-                if (ok && cudaEventElapsedTime(&t, e0, e1) == cudaSuccess)
-                    ms.push_back(t / 8);
-            }
-            if (!ok || ms.empty())
+        // The default rule's tactic is timed too, so that a tuned entry is never
+        // slower than the default's in the tuner's own measurement.
+        std::vector<dep_tactic_t> cs;
+        if (tactic_valid(p->table[i]))
+            cs.push_back(p->table[i]);
+        cs.insert(cs.end(), cands[i].begin(), cands[i].end());
+        for (const auto &c : cs) {
+            float med = 0;
+            ok = time_launches(c, B, med);
+            if (!ok)
                 break;
-            std::sort(ms.begin(), ms.end());
-            const float med = ms[0];
             if (p->log)
                 std::fprintf(stderr,
                              "[dep] tune N=%lld K=%lld B=%d kind=%d cols=%d tile_n=%d tile_k=%d stages=%d ctas=%d "
