@@ -315,14 +315,19 @@ int32_t tc_default_stages(int32_t cols)
 dep_tactic_t default_tactic(int32_t rows, int64_t N, int64_t K, int sm_count)
 {
     if (rows <= 2) {
-        // Whole rows, no cross-block split: 16-row tiles, 4 stages of 1024
+        // Whole rows, no cross-block split: 16-row tiles, stages of 1024
         // columns, handed out dynamically (measured on GB300: 5-8 % faster than
-        // the stream-K FMA kernel at one x row, on all three weights).  Falls
-        // through where x does not fit in shared memory.
+        // the stream-K FMA kernel at one x row, on all three weights).  One x
+        // row takes six stages (per call, CUDA graph + PDL: o_proj / DSA / KDA
+        // 25.6 / 29.8 / 94.7 us against 26.0 / 30.0 / 95.0 at four), two rows
+        // four (DSA: 32.6 against 32.9 at six; o_proj: six do not fit beside
+        // x).  Falls through where x does not fit in shared memory.
         const int32_t cols = pow2_at_least(rows);
-        const dep_tactic_t t = rows_tactic(rows, cols, 16, 1024, 4, sm_count);
-        if (dep::rows_fits(t, K))
-            return t;
+        for (int32_t st : {rows == 1 ? 6 : 4, 4}) {
+            const dep_tactic_t t = rows_tactic(rows, cols, 16, 1024, st, sm_count);
+            if (dep::rows_fits(t, K))
+                return t;
+        }
     }
     const int32_t cols = std::min<int32_t>(256, std::max<int32_t>(16, pow2_at_least(rows)));
     const int64_t tiles = (N + 127) / 128, t64 = (N + 63) / 64;
