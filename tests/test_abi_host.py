@@ -85,6 +85,27 @@ def test_default_rule_warp_mma(dep, N, K, rows, expect):
         dep.dep_projection_plan_destroy(plan)
 
 
+@pytest.mark.parametrize("N,K", [(14560, 7168), (7168, 12288), (49376, 7168), (333, 40000), (333, 60000)])
+def test_default_rule_whole_rows(dep, N, K):
+    """One and two x rows take the whole-row kind on 16-row tiles and stages of
+    1024 columns: six stages at one row where they fit beside x in shared memory
+    (else four), four at two rows; where x does not fit at all, another kind."""
+    plan = dep.dep_projection_plan_host(N, K, [1, 2], 152)
+    try:
+        t1, t2 = (dep.dep_projection_plan_query(plan, B) for B in (1, 2))
+        ring = 16 * 1024 * 2  # bytes of one stage
+        for t, rows, want in ((t1, 1, 6), (t2, 2, 4)):
+            x_bytes = rows * K * 2
+            if x_bytes + 4 * ring > 227 * 1024:
+                assert t.kind != dep.DEP_KIND_ROWS, t  # x and four stages do not fit
+                continue
+            assert (t.kind, t.tile_n, t.tile_k, t.cols) == (dep.DEP_KIND_ROWS, 16, 1024, rows), t
+            fits6 = x_bytes + 6 * ring + 4096 <= 227 * 1024  # with room for barriers and alignment
+            assert t.stages == (want if want == 4 or fits6 else 4), t
+    finally:
+        dep.dep_projection_plan_destroy(plan)
+
+
 def test_default_many_tiles_take_three_pieces(dep):
     plan = dep.dep_projection_plan_host(49376, 7168, [1, 4, 16, 32], 152)
     try:
